@@ -1,0 +1,219 @@
+/*
+ * pgqa.h -- C ABI of the paged grouped-query attention library (libpgqa.so).
+ *
+ * Attention over a paged KV cache, as the LLM-serving pages on PagedAttention
+ * and FlashAttention describe it:
+ *  - "Llama 4 inference speed-up: FlashAttention-3 + PagedAttention + vLLM"
+ *    (rkmt.cn), sec. 3.1: the KV cache is a logical address space cut into
+ *    fixed 16-token pages; a page table maps logical page numbers to physical
+ *    block numbers (int32, -1 = unallocated); sec. 2.4: variable-length batches
+ *    given by cumulative sequence lengths, causal masking, outputs out and the
+ *    log-sum-exp.
+ *  - "PageAttention + FlashAttention, the golden combination" (lpnh.cn),
+ *    sec. 2.1: per-request block tables, block_size 16, copy-on-write sharing
+ *    of a prompt's blocks between sequences.
+ *  - "LLM inference surgery log" (xdnf.cn), sec. 3.1: an int32 block table per
+ *    sequence and a pre-allocated pool of KV blocks updated in place at decode.
+ *  - "LLaMA structure and inference performance" (wmrh.cn), sec. 2.1: grouped-
+ *    query attention (query heads of one group share one K/V head); sec. 3.1:
+ *    scores Q.K^T * scale, mask, softmax in float32, weighted sum of V.
+ *
+ * Conventions shared by every call
+ *  - Tensors are dense, row-major, in DEVICE memory owned by the caller. The
+ *    library never allocates, frees or keeps a pointer past the call, and it
+ *    keeps no state between calls other than a host-side cache of TMA tensor
+ *    descriptors keyed by (address, shape).
+ *  - The KV cache is two tensors, k_cache and v_cache, each
+ *      [num_blocks][num_kv_heads][block_size][head_dim]
+ *    so one (block, kv-head) page of block_size x head_dim elements is
+ *    contiguous (4 KB for bf16 at 16 x 128). Element type cache_dtype:
+ *      PGQA_DTYPE_BF16  bfloat16
+ *      PGQA_DTYPE_E4M3  FP8 E4M3 codes (OCP OFP8); the real value of a code in
+ *                       kv-head h is E4M3(code) * scale[h], with separate fp32
+ *                       k_scale[num_kv_heads] and v_scale[num_kv_heads].
+ *  - Logical token j of sequence s is row j % block_size of physical block
+ *    block_tables[s * max_blocks_per_seq + j / block_size]. Entries at or past
+ *    ceil(context_len / block_size) are never read and may hold -1.
+ *  - Query head hq uses kv-head hq / (num_q_heads / num_kv_heads).
+ *  - scores are scale * q.k (times k_scale[h] for E4M3); lse is the natural
+ *    log of the sum of exp(score) over the attended keys.
+ *  - All calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and run on the current CUDA device.
+ *  - Supported now: head_dim 64 or 128, block_size 16, 1 <= num_q_heads /
+ *    num_kv_heads <= 8 for decode (any group size for prefill), bf16 q/out.
+ *
+ * Errors
+ *  - Argument errors found on the host return a negative pgqa_status_t and
+ *    launch nothing.
+ *  - Errors found on the device (a block id < 0 or >= num_blocks inside a
+ *    context, a slot past the pool, a context longer than max_context_len or
+ *    than the block table) never fault: the kernel skips the affected rows
+ *    (attention rows are written as out = 0, lse = -inf) and, when dev_status is
+ *    non-NULL, stores the first such code into *dev_status (a device int the
+ *    caller zeroes; later errors do not overwrite it). A bounded wait inside a
+ *    kernel that gives up stores PGQA_ETIMEOUT the same way.
+ */
+#ifndef PGQA_H
+#define PGQA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int pgqa_status_t;
+
+#define PGQA_OK 0
+#define PGQA_EINVAL (-1)        /* null pointer, negative size, inconsistent shapes, misalignment */
+#define PGQA_EUNSUPPORTED (-2)  /* valid request this build does not implement */
+#define PGQA_ENOWORKSPACE (-3)  /* workspace_bytes smaller than the matching *_workspace_size */
+#define PGQA_ECUDA (-4)         /* a CUDA runtime call or kernel launch failed */
+#define PGQA_EBADINDEX (-5)     /* device: block id or slot out of range */
+#define PGQA_ETIMEOUT (-6)      /* device: a bounded wait on a barrier gave up */
+
+#define PGQA_DTYPE_BF16 0
+#define PGQA_DTYPE_E4M3 1
+
+#define PGQA_ABI_VERSION 1
+
+/* ABI version of the loaded library (PGQA_ABI_VERSION it was built with). */
+int pgqa_abi_version(void);
+
+/* Static, NUL-terminated description of a status code. Never NULL. */
+const char* pgqa_status_string(pgqa_status_t status);
+
+/* Bytes of KV cache for `num_layers` layers of `tokens` cached tokens:
+ * 2 (K and V) * layers * tokens * kv-heads * head_dim * element size
+ * ("LLaMA structure and inference performance", sec. 5, sizes a 4K-context
+ * 32-layer cache at about 2.1 GB for 32 heads and about 0.5 GB for 8 kv-heads).
+ * Returns -1 for a negative argument or an unknown dtype. Host only. */
+int64_t pgqa_kv_cache_bytes(int num_layers, int64_t tokens, int num_kv_heads, int head_dim,
+                            int cache_dtype);
+
+/*
+ * Scatter new K/V rows into the paged cache (the in-place update at decode of
+ * "LLM inference surgery log", sec. 3.1; slot = physical block * block_size +
+ * row, from the page-table description of the rkmt.cn article, sec. 3.1).
+ *
+ *   key, value    [num_tokens][num_kv_heads][head_dim] bf16, read.
+ *   slot_mapping  [num_tokens] int64, read. slot < 0: token skipped.
+ *                 Otherwise block = slot / block_size (must be < num_blocks),
+ *                 row = slot % block_size. Two tokens must not share a slot.
+ *   k_cache, v_cache  the cache described above, written at those slots only.
+ *   cache_dtype   PGQA_DTYPE_BF16: bit-exact copy.
+ *                 PGQA_DTYPE_E4M3: code = E4M3 round-to-nearest-even, saturated
+ *                 to +-448, of float(x) / scale[h] (binary32 division);
+ *                 k_scale / v_scale [num_kv_heads] fp32 device arrays, read.
+ *                 Must be NULL for bf16.
+ *   dev_status    optional device int, see "Errors".
+ * head_dim must be a multiple of 8; key/value 16-byte aligned.
+ */
+pgqa_status_t pgqa_kv_cache_write(const void* key, const void* value,
+                                  const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                  int head_dim, void* k_cache, void* v_cache, int num_blocks,
+                                  int block_size, int cache_dtype, const float* k_scale,
+                                  const float* v_scale, int* dev_status, void* stream);
+
+/*
+ * Gather the pages of each sequence into contiguous K and V (a debugging and
+ * testing aid that exercises exactly the block-table addressing the attention
+ * kernels use).
+ *
+ *   k_out, v_out  [num_seqs][num_kv_heads][max_context_len][head_dim] in the
+ *                 cache's element type, written: rows j < context_lens[s] are a
+ *                 bit-exact copy of the cache; rows past it are zero.
+ * Other arguments as for pgqa_paged_attention_decode.
+ */
+pgqa_status_t pgqa_paged_kv_gather(const void* k_cache, const void* v_cache, int cache_dtype,
+                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* context_lens, int num_seqs, int num_kv_heads,
+                                   int head_dim, int num_blocks, int block_size,
+                                   int max_context_len, void* k_out, void* v_out,
+                                   int* dev_status, void* stream);
+
+/*
+ * Split plan of paged decode (host logic, no device access): how many key
+ * ranges ("splits") each (sequence, kv-head) is cut into so that a device with
+ * `num_sms` multiprocessors is filled. Returns the number of splits (>= 1) and
+ * stores the pages per split in *pages_per_split; returns PGQA_EINVAL on a bad
+ * argument.
+ */
+int pgqa_decode_split_plan(int num_seqs, int num_kv_heads, int max_context_len, int block_size,
+                           int num_sms, int* pages_per_split);
+
+/* Workspace bytes pgqa_paged_attention_decode needs on the current device for
+ * these sizes (0 when no sequence is split). */
+size_t pgqa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int max_context_len);
+
+/*
+ * Paged decode attention: one new query token per sequence attends to its
+ * whole cached context ("LLaMA structure and inference performance", sec. 3.1
+ * steps 2-6 with repeat_kv as the index map of sec. 2.1, read through the block
+ * table of the rkmt.cn article, sec. 3.1). Each KV byte is read once: one
+ * thread block serves all query heads of a kv-head.
+ *
+ *   out           [num_seqs][num_q_heads][head_dim] bf16, written
+ *                 (fp32 accumulation, rounded to nearest even).
+ *   lse           [num_seqs][num_q_heads] fp32, written; may be NULL.
+ *   q             [num_seqs][num_q_heads][head_dim] bf16, read.
+ *   block_tables  [num_seqs][max_blocks_per_seq] int32, read.
+ *   context_lens  [num_seqs] int32, read; 0 gives out = 0, lse = -inf.
+ *   scale         softmax scale (usually 1/sqrt(head_dim)).
+ *   cache_dtype, k_scale, v_scale   as for pgqa_kv_cache_write.
+ *   max_context_len  an upper bound on context_lens (sizes the split plan);
+ *                 a longer context is a device error.
+ *   workspace     device scratch of at least pgqa_decode_workspace_size()
+ *                 bytes, 256-byte aligned, ZERO-FILLED before its first use;
+ *                 every call that completes leaves it ready for the next call.
+ *                 May be NULL when that size is 0. Calls that share one
+ *                 workspace must not overlap in time.
+ * k_cache/v_cache must be 16-byte aligned, q/out 16-byte aligned.
+ */
+pgqa_status_t pgqa_paged_attention_decode(void* out, float* lse, const void* q,
+                                          const void* k_cache, const void* v_cache,
+                                          const int32_t* block_tables, int max_blocks_per_seq,
+                                          const int32_t* context_lens, int num_seqs,
+                                          int num_q_heads, int num_kv_heads, int head_dim,
+                                          int num_blocks, int block_size, float scale,
+                                          int cache_dtype, const float* k_scale,
+                                          const float* v_scale, int max_context_len,
+                                          void* workspace, size_t workspace_bytes,
+                                          int* dev_status, void* stream);
+
+/* Workspace bytes pgqa_paged_prefill_varlen needs (currently 0). */
+size_t pgqa_prefill_workspace_size(int num_seqs, int num_q_heads, int max_seqlen);
+
+/*
+ * Causal variable-length prefill over the paged cache (the varlen call with
+ * cumulative lengths, causal=True, returning out and lse, of the rkmt.cn
+ * article, sec. 2.4; keys read through the block tables of sec. 3.1).
+ * The prompt's K/V must already be in the cache (pgqa_kv_cache_write).
+ *
+ *   out           [T][num_q_heads][head_dim] bf16, written; T = cu_seqlens[num_seqs].
+ *   lse           [T][num_q_heads] fp32, written; may be NULL.
+ *   q             [T][num_q_heads][head_dim] bf16, read.
+ *   cu_seqlens    [num_seqs + 1] int32, read: sequence i owns tokens
+ *                 cu_seqlens[i] .. cu_seqlens[i+1]-1; the token at position p
+ *                 of sequence i attends to keys 0..p of sequence i.
+ *   max_seqlen    an upper bound on the sequence lengths (sizes the grid).
+ *   block_tables  [num_seqs][max_blocks_per_seq] int32, read.
+ *   workspace     may be NULL while pgqa_prefill_workspace_size() is 0.
+ * bf16 cache only; q/out/k_cache/v_cache 16-byte aligned.
+ */
+pgqa_status_t pgqa_paged_prefill_varlen(void* out, float* lse, const void* q,
+                                        const void* k_cache, const void* v_cache,
+                                        const int32_t* block_tables, int max_blocks_per_seq,
+                                        const int32_t* cu_seqlens, int num_seqs, int max_seqlen,
+                                        int num_q_heads, int num_kv_heads, int head_dim,
+                                        int num_blocks, int block_size, float scale,
+                                        void* workspace, size_t workspace_bytes,
+                                        int* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PGQA_H */

@@ -1,0 +1,96 @@
+// Host-side plumbing shared by the translation units of libpgqa: TMA descriptor
+// encoding (through the driver entry point, cached by address and shape), device
+// properties, and the launchers each kernel file exports to the C ABI layer.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pgqa.h"
+
+namespace pgqa {
+
+// Row-major 2-D view [rows][inner] of `base` with a row pitch of row_bytes, tiled
+// in boxes of box_inner x box_rows elements. Returns false if the driver refuses.
+bool tensor_map_2d(CUtensorMap* out, const void* base, CUtensorMapDataType dtype, uint64_t inner,
+                   uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
+                   CUtensorMapSwizzle swizzle);
+
+// 3-D view [d2][d1][d0] with pitches (bytes) for dims 1 and 2.
+bool tensor_map_3d(CUtensorMap* out, const void* base, CUtensorMapDataType dtype, uint64_t d0,
+                   uint64_t d1, uint64_t d2, uint64_t pitch1, uint64_t pitch2, uint32_t box0,
+                   uint32_t box1, uint32_t box2, CUtensorMapSwizzle swizzle);
+
+// Multiprocessor count of the current device (cached per device); 0 on error.
+int num_sms_current_device();
+
+// Raises a kernel's dynamic shared memory limit to `bytes` on the current device
+// (once per device and kernel). Returns false if the runtime refuses.
+bool smem_attr_ready(const void* kernel, int bytes);
+
+// ----------------------------------------------------------- launchers
+
+pgqa_status_t launch_kv_cache_write(const void* key, const void* value,
+                                    const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                    int head_dim, void* k_cache, void* v_cache, int num_blocks,
+                                    int block_size, int cache_dtype, const float* k_scale,
+                                    const float* v_scale, int* dev_status, cudaStream_t stream);
+
+pgqa_status_t launch_kv_gather(const void* k_cache, const void* v_cache, int cache_dtype,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int num_seqs, int num_kv_heads,
+                               int head_dim, int num_blocks, int block_size, int max_context_len,
+                               void* k_out, void* v_out, int* dev_status, cudaStream_t stream);
+
+struct DecodeArgs {
+  void* out;
+  float* lse;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  int max_blocks_per_seq;
+  const int32_t* context_lens;
+  int num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size;
+  float scale;
+  int cache_dtype;
+  const float* k_scale;
+  const float* v_scale;
+  int max_context_len;
+  void* workspace;
+  size_t workspace_bytes;
+  int* dev_status;
+  cudaStream_t stream;
+};
+
+// Split plan + workspace layout of paged decode.
+struct DecodePlan {
+  int num_splits;
+  int pages_per_split;
+  size_t counters_off, lse_off, o_off, bytes;
+};
+DecodePlan decode_plan(int num_seqs, int num_kv_heads, int head_dim, int max_context_len,
+                       int block_size, int num_sms);
+
+pgqa_status_t launch_paged_decode(const DecodeArgs& a, const DecodePlan& plan);
+
+struct PrefillArgs {
+  void* out;
+  float* lse;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  int max_blocks_per_seq;
+  const int32_t* cu_seqlens;
+  int num_seqs, max_seqlen, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size;
+  float scale;
+  int* dev_status;
+  cudaStream_t stream;
+};
+
+pgqa_status_t launch_paged_prefill(const PrefillArgs& a);
+
+}  // namespace pgqa

@@ -1,0 +1,115 @@
+"""CPU-only checks of the library boundary: it loads, exports every symbol the
+public header declares, and its host logic (size helpers, split plan, status
+strings, argument validation that returns before any launch) behaves."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_gqa_10_gb300 as pgqa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pgqa.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pgqa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("pgqa_kv_cache_write", "pgqa_paged_attention_decode", "pgqa_paged_prefill_varlen",
+              "pgqa_paged_kv_gather", "pgqa_decode_workspace_size", "pgqa_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(pgqa.library_path())
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_abi_version_and_status_strings():
+    assert pgqa.abi_version() == pgqa.ABI_VERSION
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert pgqa.status_string(code) and pgqa.status_string(code) != "unknown status"
+    assert pgqa.status_string(-99) == "unknown status"
+
+
+def test_kv_cache_bytes_matches_printed_figures():
+    with open(os.path.join(GOLDEN, "kv_cache_size.txt")) as f:
+        rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    for layers, tokens, heads, dim, elem, printed, tol in rows:
+        dt = pgqa.BF16 if int(elem) == 2 else pgqa.E4M3
+        got = pgqa.kv_cache_bytes(int(layers), int(tokens), int(heads), int(dim), dt) / 1e9
+        assert abs(got - float(printed)) <= float(tol), (got, printed)
+    assert pgqa.kv_cache_bytes(1, 16, 1, 128, pgqa.BF16) == 8192  # one 16-token K+V page
+    assert pgqa.kv_cache_bytes(1, 16, 1, 128, pgqa.E4M3) == 4096
+    assert pgqa.kv_cache_bytes(-1, 1, 1, 1) == -1
+
+
+@pytest.mark.parametrize("B,Hkv,ctx", [(64, 8, 1024), (32, 8, 4096), (16, 8, 8192), (2, 2, 50),
+                                       (1, 1, 1), (512, 8, 128), (3, 1, 100000)])
+@pytest.mark.parametrize("sms", [1, 148, 152])
+def test_split_plan_covers_every_page(B, Hkv, ctx, sms):
+    n, pps = pgqa.decode_split_plan(B, Hkv, ctx, sms)
+    pages = -(-ctx // 16)
+    assert n >= 1 and pps >= 1
+    assert n * pps >= pages and (n - 1) * pps < pages       # no empty trailing split
+    assert n == 1 or pps >= 8                                # never below 128 tokens
+
+
+def test_split_plan_rejects_bad_arguments():
+    with pytest.raises(pgqa.PgqaError):
+        pgqa.decode_split_plan(1, 0, 10, 152)
+
+
+def _call_decode(**over):
+    a = dict(out=1 << 20, lse=None, q=1 << 20, k=1 << 20, v=1 << 20, bt=1 << 20, maxb=4,
+             cl=1 << 20, B=2, Hq=8, Hkv=2, D=128, NB=16, bs=16, scale=0.1, dtype=0, ks=None,
+             vs=None, maxctx=64, ws=None, wsb=0, st=None)
+    a.update(over)
+    f = pgqa.lib.pgqa_paged_attention_decode
+    return f(a["out"], a["lse"], a["q"], a["k"], a["v"], a["bt"], a["maxb"], a["cl"], a["B"],
+             a["Hq"], a["Hkv"], a["D"], a["NB"], a["bs"], a["scale"], a["dtype"], a["ks"], a["vs"],
+             a["maxctx"], a["ws"], a["wsb"], a["st"], None)
+
+
+@pytest.mark.parametrize("over,want", [
+    (dict(Hq=7), pgqa.EINVAL),                 # heads not a multiple of kv heads
+    (dict(Hq=32, Hkv=2), pgqa.EUNSUPPORTED),   # group of 16
+    (dict(D=96), pgqa.EUNSUPPORTED),
+    (dict(bs=32), pgqa.EUNSUPPORTED),
+    (dict(dtype=7), pgqa.EUNSUPPORTED),
+    (dict(dtype=1), pgqa.EINVAL),              # E4M3 without scales
+    (dict(ks=1 << 20, vs=1 << 20), pgqa.EINVAL),  # scales given for bf16
+    (dict(B=-1), pgqa.EINVAL),
+    (dict(scale=float("nan")), pgqa.EINVAL),
+    (dict(q=None), pgqa.EINVAL),
+    (dict(q=(1 << 20) + 8), pgqa.EINVAL),      # misaligned
+    (dict(B=0), pgqa.OK),                      # nothing to do, nothing launched
+])
+def test_decode_argument_validation(over, want):
+    assert _call_decode(**over) == want
+
+
+def test_kv_write_argument_validation():
+    f = pgqa.lib.pgqa_kv_cache_write
+    P = 1 << 20
+    assert f(P, P, P, 4, 2, 100, P, P, 8, 16, 0, None, None, None, None) == pgqa.EUNSUPPORTED
+    assert f(P, P, P, 4, 2, 128, P, P, 8, 16, 1, None, None, None, None) == pgqa.EINVAL
+    assert f(P, P, P, 0, 2, 128, P, P, 8, 16, 0, None, None, None, None) == pgqa.OK
+    assert f(None, P, P, 4, 2, 128, P, P, 8, 16, 0, None, None, None, None) == pgqa.EINVAL
+
+
+def test_prefill_argument_validation():
+    f = pgqa.lib.pgqa_paged_prefill_varlen
+    P = 1 << 20
+    args = [P, None, P, P, P, P, 4, P, 2, 64, 8, 2, 128, 16, 16, 0.1, None, 0, None, None]
+    assert f(*args[:12], 96, *args[13:]) == pgqa.EUNSUPPORTED
+    assert f(*args[:10], 7, *args[11:]) == pgqa.EINVAL
+    assert f(*args[:8], 0, *args[9:]) == pgqa.OK
