@@ -183,6 +183,44 @@ pgqa_status_t pgqa_paged_attention_decode(void* out, float* lse, const void* q,
                                           void* workspace, size_t workspace_bytes,
                                           int* dev_status, void* stream);
 
+/* Size of the library-owned scratch array used by
+ * pgqa_paged_attention_decode_noalloc (8 MiB per GPU that loads the library). */
+#define PGQA_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/*
+ * pgqa_paged_attention_decode_noalloc -- the same paged decode attention as
+ * pgqa_paged_attention_decode, for callers that cannot allocate device memory.
+ * The pages have no counterpart for this entry point; it exists for users of the
+ * library: a serving engine that sizes its KV block pool to fill the GPU's free
+ * memory at start-up (so a later cudaMalloc fails), or a plugin hosted inside
+ * another framework whose device memory belongs to that framework's allocator,
+ * has nowhere to get the split-K workspace from.
+ *
+ * Arguments are those of pgqa_paged_attention_decode without the workspace; the
+ * caller still passes every input and output. The split-K scratch is a static
+ * device array of PGQA_NOALLOC_SCRATCH_BYTES owned by the library:
+ *  - sizes whose workspace (pgqa_decode_workspace_size) exceeds that limit are
+ *    rejected with PGQA_ENOWORKSPACE before anything is launched;
+ *  - the first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture;
+ *  - each call clears the array's merge counters with cudaMemsetAsync on
+ *    `stream`, then launches the decode kernel; it never calls cudaMalloc,
+ *    cudaFree or any allocating routine;
+ *  - all calls share the one array, so calls that overlap on the GPU (other
+ *    streams, other host threads) race and must be serialised by the caller.
+ */
+pgqa_status_t pgqa_paged_attention_decode_noalloc(void* out, float* lse, const void* q,
+                                                  const void* k_cache, const void* v_cache,
+                                                  const int32_t* block_tables,
+                                                  int max_blocks_per_seq,
+                                                  const int32_t* context_lens, int num_seqs,
+                                                  int num_q_heads, int num_kv_heads, int head_dim,
+                                                  int num_blocks, int block_size, float scale,
+                                                  int cache_dtype, const float* k_scale,
+                                                  const float* v_scale, int max_context_len,
+                                                  int* dev_status, void* stream);
+
 /* Workspace bytes pgqa_paged_prefill_varlen needs (currently 0). */
 size_t pgqa_prefill_workspace_size(int num_seqs, int num_q_heads, int max_seqlen);
 

@@ -10,7 +10,8 @@ raises ImportError if the library has not been built
 
 Functions (same names as the C entry points, without the ``pgqa_`` prefix):
   kv_cache_write, paged_kv_gather, paged_attention_decode,
-  paged_prefill_varlen, decode_workspace_size, decode_split_plan,
+  paged_attention_decode_noalloc, paged_prefill_varlen, decode_workspace_size,
+  decode_split_plan,
   prefill_workspace_size, kv_cache_bytes, status_string, abi_version.
 """
 import ctypes
@@ -20,7 +21,8 @@ import torch
 
 __all__ = [
     "PgqaError", "BF16", "E4M3", "kv_cache_write", "paged_kv_gather",
-    "paged_attention_decode", "paged_prefill_varlen", "decode_workspace_size",
+    "paged_attention_decode", "paged_attention_decode_noalloc", "paged_prefill_varlen",
+    "decode_workspace_size",
     "decode_split_plan", "prefill_workspace_size", "kv_cache_bytes", "status_string",
     "abi_version", "library_path", "lib",
 ]
@@ -28,6 +30,7 @@ __all__ = [
 BF16 = 0
 E4M3 = 1
 ABI_VERSION = 1
+NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 OK, EINVAL, EUNSUPPORTED, ENOWORKSPACE, ECUDA, EBADINDEX, ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
 
@@ -59,6 +62,8 @@ def _load():
         "pgqa_decode_workspace_size": ([I, I, I, I, I], SZ),
         "pgqa_paged_attention_decode": ([P, P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, P, P,
                                          I, P, SZ, P, P], I),
+        "pgqa_paged_attention_decode_noalloc": ([P, P, P, P, P, P, I, P, I, I, I, I, I, I, F,
+                                                 I, P, P, I, P, P], I),
         "pgqa_prefill_workspace_size": ([I, I, I], SZ),
         "pgqa_paged_prefill_varlen": ([P, P, P, P, P, P, I, P, I, I, I, I, I, I, I, F, P, SZ,
                                        P, P], I),
@@ -227,6 +232,33 @@ def paged_attention_decode(out, lse, q, k_cache, v_cache, block_tables, context_
         _cache_dtype(k_cache), _ptr(k_scale), _ptr(v_scale), int(max_context_len),
         _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
     _check(rc, "paged_attention_decode")
+
+
+def paged_attention_decode_noalloc(out, lse, q, k_cache, v_cache, block_tables, context_lens,
+                                   scale, max_context_len, k_scale=None, v_scale=None,
+                                   dev_status=None, stream=None):
+    """paged_attention_decode for callers that cannot allocate device memory: the
+    split-K scratch is a fixed 8 MiB array owned by the library (see
+    pgqa_paged_attention_decode_noalloc in include/pgqa.h). Calls that overlap
+    on the GPU race on that array."""
+    _dev(out, "out", torch.bfloat16)
+    _dev(lse, "lse", torch.float32)
+    _dev(q, "q", torch.bfloat16)
+    _dev(k_cache, "k_cache")
+    _dev(v_cache, "v_cache")
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(context_lens, "context_lens", torch.int32)
+    _dev(k_scale, "k_scale", torch.float32)
+    _dev(v_scale, "v_scale", torch.float32)
+    _dev(dev_status, "dev_status", torch.int32)
+    B, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    rc = _handle().pgqa_paged_attention_decode_noalloc(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, NB, bs, float(scale),
+        _cache_dtype(k_cache), _ptr(k_scale), _ptr(v_scale), int(max_context_len),
+        _ptr(dev_status), _stream(stream))
+    _check(rc, "paged_attention_decode_noalloc")
 
 
 def paged_prefill_varlen(out, lse, q, k_cache, v_cache, block_tables, cu_seqlens, max_seqlen,
