@@ -45,13 +45,14 @@
  * Errors
  *  - Argument errors found on the host return a negative pgqa_status_t and
  *    launch nothing.
- *  - Errors found on the device (a block id < 0 or >= num_blocks inside a
- *    context, a slot past the pool, a context longer than max_context_len or
- *    than the block table) never fault: the kernel skips the affected rows
- *    (attention rows are written as out = 0, lse = -inf) and, when dev_status is
- *    non-NULL, stores the first such code into *dev_status (a device int the
- *    caller zeroes; later errors do not overwrite it). A bounded wait inside a
- *    kernel that gives up stores PGQA_ETIMEOUT the same way.
+ *  - Errors found on the device never fault: a block id < 0 or >= num_blocks
+ *    inside a context, or a slot past the pool, is PGQA_EBADINDEX; a context
+ *    longer than max_context_len or than the block table is PGQA_EINVAL. The
+ *    kernel skips the affected rows (attention rows are written as out = 0,
+ *    lse = -inf) and, when dev_status is non-NULL, stores the first such code
+ *    into *dev_status (a device int the caller zeroes; later errors do not
+ *    overwrite it). A bounded wait inside a kernel that gives up stores
+ *    PGQA_ETIMEOUT the same way.
  */
 #ifndef PGQA_H
 #define PGQA_H
@@ -233,15 +234,19 @@ size_t pgqa_prefill_workspace_size(int num_seqs, int num_q_heads, int max_seqlen
  *   out           [T][num_q_heads][head_dim] bf16, written; T = cu_seqlens[num_seqs].
  *   lse           [T][num_q_heads] fp32, written; may be NULL.
  *   q             [T][num_q_heads][head_dim] bf16, read.
+ *   num_tokens    T; must equal cu_seqlens[num_seqs] (checked on the device).
  *   cu_seqlens    [num_seqs + 1] int32, read: sequence i owns tokens
  *                 cu_seqlens[i] .. cu_seqlens[i+1]-1; the token at position p
  *                 of sequence i attends to keys 0..p of sequence i.
  *   max_seqlen    an upper bound on the sequence lengths (sizes the grid).
  *   block_tables  [num_seqs][max_blocks_per_seq] int32, read.
  *   workspace     may be NULL while pgqa_prefill_workspace_size() is 0.
- * bf16 cache only; q/out/k_cache/v_cache 16-byte aligned.
+ * bf16 cache only; q/out/k_cache/v_cache 16-byte aligned. Inconsistent
+ * cu_seqlens (negative lengths, a length above max_seqlen or beyond the block
+ * table, a last entry other than num_tokens) are a device error (PGQA_EINVAL in
+ * *dev_status); nothing is written for the sequences concerned.
  */
-pgqa_status_t pgqa_paged_prefill_varlen(void* out, float* lse, const void* q,
+pgqa_status_t pgqa_paged_prefill_varlen(void* out, float* lse, const void* q, int num_tokens,
                                         const void* k_cache, const void* v_cache,
                                         const int32_t* block_tables, int max_blocks_per_seq,
                                         const int32_t* cu_seqlens, int num_seqs, int max_seqlen,

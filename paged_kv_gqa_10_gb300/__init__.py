@@ -65,8 +65,8 @@ def _load():
         "pgqa_paged_attention_decode_noalloc": ([P, P, P, P, P, P, I, P, I, I, I, I, I, I, F,
                                                  I, P, P, I, P, P], I),
         "pgqa_prefill_workspace_size": ([I, I, I], SZ),
-        "pgqa_paged_prefill_varlen": ([P, P, P, P, P, P, I, P, I, I, I, I, I, I, I, F, P, SZ,
-                                       P, P], I),
+        "pgqa_paged_prefill_varlen": ([P, P, P, I, P, P, P, I, P, I, I, I, I, I, I, I, F, P,
+                                       SZ, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -278,7 +278,7 @@ def paged_prefill_varlen(out, lse, q, k_cache, v_cache, block_tables, cu_seqlens
     S = cu_seqlens.shape[0] - 1
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = _handle().pgqa_paged_prefill_varlen(
-        _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        _ptr(out), _ptr(lse), _ptr(q), T, _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
         block_tables.shape[1], _ptr(cu_seqlens), S, int(max_seqlen), Hq, Hkv, D, NB, bs,
         float(scale), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
     _check(rc, "paged_prefill_varlen")

@@ -338,7 +338,7 @@ size_t pgqa_prefill_workspace_size(int num_seqs, int num_q_heads, int max_seqlen
   return 0;
 }
 
-pgqa_status_t pgqa_paged_prefill_varlen(void* out, float* lse, const void* q,
+pgqa_status_t pgqa_paged_prefill_varlen(void* out, float* lse, const void* q, int num_tokens,
                                         const void* k_cache, const void* v_cache,
                                         const int32_t* block_tables, int max_blocks_per_seq,
                                         const int32_t* cu_seqlens, int num_seqs, int max_seqlen,
@@ -348,14 +348,16 @@ pgqa_status_t pgqa_paged_prefill_varlen(void* out, float* lse, const void* q,
                                         int* dev_status, void* stream) {
   (void)workspace;
   (void)workspace_bytes;
-  if (num_seqs < 0 || max_seqlen < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
-      num_blocks <= 0 || block_size <= 0 || max_blocks_per_seq < 0 || !isfinite(scale))
+  if (num_seqs < 0 || max_seqlen < 0 || num_tokens < 0 || num_q_heads <= 0 ||
+      num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || block_size <= 0 ||
+      max_blocks_per_seq < 0 || !isfinite(scale))
     return PGQA_EINVAL;
   if (num_q_heads % num_kv_heads != 0) return PGQA_EINVAL;
   if (head_dim != 128 && head_dim != 64) return PGQA_EUNSUPPORTED;
   if (block_size != 16) return PGQA_EUNSUPPORTED;
   if (static_cast<int64_t>(num_blocks) * num_kv_heads * 16 > INT32_MAX) return PGQA_EUNSUPPORTED;
-  if (num_seqs == 0 || max_seqlen == 0) return PGQA_OK;
+  if (num_seqs == 0 || max_seqlen == 0 || num_tokens == 0) return PGQA_OK;
+  if (num_seqs > 65535 * 64 || (max_seqlen + 127) / 128 > 65535) return PGQA_EUNSUPPORTED;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !cu_seqlens) return PGQA_EINVAL;
   if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
     return PGQA_EINVAL;
@@ -368,6 +370,7 @@ pgqa_status_t pgqa_paged_prefill_varlen(void* out, float* lse, const void* q,
   a.block_tables = block_tables;
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.cu_seqlens = cu_seqlens;
+  a.num_tokens = num_tokens;
   a.num_seqs = num_seqs;
   a.max_seqlen = max_seqlen;
   a.num_q_heads = num_q_heads;

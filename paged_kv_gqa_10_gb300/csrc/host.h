@@ -85,6 +85,7 @@ struct PrefillArgs {
   const int32_t* block_tables;
   int max_blocks_per_seq;
   const int32_t* cu_seqlens;
+  int num_tokens;
   int num_seqs, max_seqlen, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size;
   float scale;
   int* dev_status;

@@ -109,7 +109,9 @@ def test_kv_write_argument_validation():
 def test_prefill_argument_validation():
     f = pgqa.lib.pgqa_paged_prefill_varlen
     P = 1 << 20
-    args = [P, None, P, P, P, P, 4, P, 2, 64, 8, 2, 128, 16, 16, 0.1, None, 0, None, None]
-    assert f(*args[:12], 96, *args[13:]) == pgqa.EUNSUPPORTED
-    assert f(*args[:10], 7, *args[11:]) == pgqa.EINVAL
-    assert f(*args[:8], 0, *args[9:]) == pgqa.OK
+    #       out lse q  T    k  v  bt maxb cu S  maxL Hq Hkv D    NB  bs  scale ws  wsb st  stream
+    args = [P, None, P, 100, P, P, P, 4, P, 2, 64, 8, 2, 128, 16, 16, 0.1, None, 0, None, None]
+    assert f(*args[:13], 96, *args[14:]) == pgqa.EUNSUPPORTED
+    assert f(*args[:11], 7, *args[12:]) == pgqa.EINVAL
+    assert f(*args[:9], 0, *args[10:]) == pgqa.OK
+    assert f(*args[:3], -1, *args[4:]) == pgqa.EINVAL
