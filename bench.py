@@ -145,13 +145,16 @@ def _cpu_baseline(inp, target_s=10.0):
     import oracle
     cores = oracle.default_threads()
     args = (inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale)
+    kw = dict(threads=cores)
+    if inp.cache_dtype == "e4m3":
+        kw.update(dtype=oracle.E4M3, k_scale=inp.k_scale, v_scale=inp.v_scale)
     t0 = time.perf_counter()
-    oracle.paged_decode(*args, threads=cores)
+    oracle.paged_decode(*args, **kw)
     one = time.perf_counter() - t0
     reps = max(1, int(target_s / max(one, 1e-3)))
     t0 = time.perf_counter()
     for _ in range(reps):
-        oracle.paged_decode(*args, threads=cores)
+        oracle.paged_decode(*args, **kw)
     dt = (time.perf_counter() - t0) / reps
     gbs = workloads.kv_read_bytes(inp) / dt / 1e9
     return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
@@ -192,147 +195,284 @@ def run_reference(args):
     return 0
 
 
-def run_ours(args):
-    import paged_kv_gqa_10_gb300 as pgqa
+class DecodeBench:
+    """Device state of one decode workload and its step (append + decode)."""
 
-    dist, rank, local, world = _dist()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream()
+    def __init__(self, inp, dev):
+        import paged_kv_gqa_10_gb300 as pgqa
+        self.pgqa, self.inp, self.dev = pgqa, inp, dev
+        self.tables = [inp.block_tables] + inp.rotations
+        self.slots = [inp.step_slots] + inp.rotation_slots
+        self.R = len(self.tables)
+        B, Hq, D = inp.q.shape
+        self.kc, self.vc = inp.k_cache.to(dev), inp.v_cache.to(dev)
+        self.ks = None if inp.k_scale is None else inp.k_scale.to(dev)
+        self.vs = None if inp.v_scale is None else inp.v_scale.to(dev)
+        self.q = inp.q.to(dev)
+        self.cl = inp.context_lens.to(dev)
+        self.bts = [t.to(dev) for t in self.tables]
+        self.sls = [t.to(dev) for t in self.slots]
+        self.nk, self.nv = inp.step_key.to(dev), inp.step_value.to(dev)
+        self.out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+        self.ws_n = pgqa.decode_workspace_size(B, Hq, inp.num_kv_heads, D, inp.max_context_len)
+        self.ws = torch.zeros(max(self.ws_n, 256), dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.kv_bytes = workloads.kv_read_bytes(inp)
+        nblk = int(((inp.context_lens + 15) // 16).sum())
+        # one decode launch reads every cached KV byte once, q, the table entries and
+        # lengths, and writes out and lse
+        self.alg_bytes = (self.kv_bytes + self.q.numel() * 2 + self.out.numel() * 2 +
+                          self.lse.numel() * 4 + nblk * 4 + B * 4)
+        self.graphs = None
 
-    inp = workloads.llama3_8b_decode(rotations=ROTATIONS)
-    tables = [inp.block_tables] + inp.rotations
-    slots = [inp.step_slots] + inp.rotation_slots
-    R = len(tables)
-    B, Hq, D = inp.q.shape
-    Hkv = inp.num_kv_heads
-    kc, vc = inp.k_cache.to(dev), inp.v_cache.to(dev)
-    q = inp.q.to(dev)
-    cl = inp.context_lens.to(dev)
-    bts = [t.to(dev) for t in tables]
-    sls = [s.to(dev) for s in slots]
-    nk, nv = inp.step_key.to(dev), inp.step_value.to(dev)
-    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
-    ws_n = pgqa.decode_workspace_size(B, Hq, Hkv, D, inp.max_context_len)
-    ws = torch.zeros(max(ws_n, 256), dtype=torch.uint8, device=dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    maxctx = inp.max_context_len
+    def append(self, r, slots=None, key=None, value=None):
+        self.pgqa.kv_cache_write(self.nk if key is None else key, self.nv if value is None else value,
+                                 self.sls[r] if slots is None else slots, self.kc, self.vc,
+                                 k_scale=self.ks, v_scale=self.vs, dev_status=self.status)
 
-    def step(i, ev=None):
-        r = i % R
-        pgqa.kv_cache_write(nk, nv, sls[r], kc, vc, dev_status=status)
-        if ev is not None:
-            ev[0].record(stream)
-        pgqa.paged_attention_decode(out, lse, q, kc, vc, bts[r], cl, inp.scale, maxctx,
-                                    workspace=ws if ws_n else None, dev_status=status)
-        if ev is not None:
-            ev[1].record(stream)
+    def decode(self, r, table=None):
+        self.pgqa.paged_attention_decode(
+            self.out, self.lse, self.q, self.kc, self.vc, self.bts[r] if table is None else table,
+            self.cl, self.inp.scale, self.inp.max_context_len, k_scale=self.ks, v_scale=self.vs,
+            workspace=self.ws if self.ws_n else None, dev_status=self.status)
 
-    kv_bytes = workloads.kv_read_bytes(inp)
-    # algorithmic bytes of one decode launch: KV once + q + out + lse + table entries + lens
-    nblk = int(((inp.context_lens + 15) // 16).sum())
-    alg_bytes = kv_bytes + q.numel() * 2 + out.numel() * 2 + lse.numel() * 4 + nblk * 4 + B * 4
+    def step(self, i):
+        r = i % self.R
+        self.append(r)
+        self.decode(r)
 
-    for i in range(args.warmup):
-        step(i)
+    def capture(self):
+        """One CUDA graph per rotation, each holding one step (append + decode)."""
+        self.graphs = []
+        side = torch.cuda.Stream(self.dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for r in range(self.R):  # warm the capture stream
+                self.step(r)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        for r in range(self.R):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.step(r)
+            self.graphs.append(g)
+        torch.cuda.synchronize()
+
+    def check(self):
+        torch.cuda.synchronize()
+        st = int(self.status.item())
+        assert st == 0, f"device status {st}"
+
+
+def _elapsed(fn, n):
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for i in range(n):
+        fn(i)
+    e1.record(s)
     torch.cuda.synchronize()
-    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    return e0.elapsed_time(e1)
 
+
+def measure_decode(inp, args, dev, dist=None, clocks_index=None):
+    """Step time (CUDA-graph replays and eager), decode-kernel time (CUDA events
+    around each eager launch) and the end-to-end step through the public API."""
+    b = DecodeBench(inp, dev)
+    for i in range(args.warmup):
+        b.step(i)
+    b.check()
+    b.capture()
+    for i in range(args.warmup):
+        b.graphs[i % b.R].replay()
+    b.check()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = None
+    if clocks_index is not None:
+        with ClockSampler(clocks_index) as cs:
+            ms_graph = _elapsed(lambda i: b.graphs[(args.warmup + i) % b.R].replay(), args.steps)
+        clocks = cs.summary()
+    else:
+        ms_graph = _elapsed(lambda i: b.graphs[(args.warmup + i) % b.R].replay(), args.steps)
+    if dist:
+        dist.barrier()
+    b.check()
+    ms_eager = _elapsed(lambda i: b.step(args.warmup + i), args.steps)
+    # decode kernel alone: events around each launch (appends keep the cache identical)
+    stream = torch.cuda.current_stream()
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
+    for i in range(args.steps):
+        r = (args.warmup + i) % b.R
+        b.append(r)
+        kev[i][0].record(stream)
+        b.decode(r)
+        kev[i][1].record(stream)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        t_start.record(stream)
-        for i in range(args.steps):
-            step(args.warmup + i, kev[i])
-        t_end.record(stream)
-        torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    ms = t_start.elapsed_time(t_end)
-    dec_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    assert int(status.item()) == 0, f"device status {int(status.item())}"
-    ms_step = ms / args.steps
-    value = kv_bytes * world / (ms_step * 1e-3) / 1e9
+    dec_ms = sum(x.elapsed_time(y) for x, y in kev) / args.steps
+    b.check()
 
-    # ---- end to end through the public API with host buffers
+    # end to end through the public API: pinned host inputs in, out/lse back, eager calls
     pin = lambda t: t.pin_memory()
     h_q, h_k, h_v, h_cl = pin(inp.q), pin(inp.step_key), pin(inp.step_value), pin(inp.context_lens)
-    h_bt = [pin(t) for t in tables]
-    h_sl = [pin(s) for s in slots]
-    h_out = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
-    h_lse = torch.empty((B, Hq), dtype=torch.float32).pin_memory()
-    d_bt = torch.empty_like(bts[0])
-    d_sl = torch.empty_like(sls[0])
+    h_bt = [pin(t) for t in b.tables]
+    h_sl = [pin(t) for t in b.slots]
+    h_out = torch.empty(tuple(b.out.shape), dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty(tuple(b.lse.shape), dtype=torch.float32).pin_memory()
+    d_bt, d_sl = torch.empty_like(b.bts[0]), torch.empty_like(b.sls[0])
 
     def e2e_step(i):
-        r = i % R
-        q.copy_(h_q, non_blocking=True)
-        nk.copy_(h_k, non_blocking=True)
-        nv.copy_(h_v, non_blocking=True)
-        cl.copy_(h_cl, non_blocking=True)
+        r = i % b.R
+        b.q.copy_(h_q, non_blocking=True)
+        b.nk.copy_(h_k, non_blocking=True)
+        b.nv.copy_(h_v, non_blocking=True)
+        b.cl.copy_(h_cl, non_blocking=True)
         d_bt.copy_(h_bt[r], non_blocking=True)
         d_sl.copy_(h_sl[r], non_blocking=True)
-        pgqa.kv_cache_write(nk, nv, d_sl, kc, vc, dev_status=status)
-        pgqa.paged_attention_decode(out, lse, q, kc, vc, d_bt, cl, inp.scale, maxctx,
-                                    workspace=ws if ws_n else None, dev_status=status)
-        h_out.copy_(out, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        b.append(r, slots=d_sl)
+        b.decode(r, table=d_bt)
+        h_out.copy_(b.out, non_blocking=True)
+        h_lse.copy_(b.lse, non_blocking=True)
 
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_cl, h_bt[0], h_sl[0]))
     d2h = h_out.numel() * 2 + h_lse.numel() * 4
     for i in range(args.warmup):
         e2e_step(i)
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        e2e_step(args.warmup + i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_ms = _elapsed(lambda i: e2e_step(args.warmup + i), args.steps)
+    b.check()
+    res = {"bench": b, "ms_graph": ms_graph / args.steps, "ms_eager": ms_eager / args.steps,
+           "dec_ms": dec_ms, "e2e_ms": e2e_ms / args.steps, "h2d": h2d, "d2h": d2h,
+           "clocks": clocks}
     if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = kv_bytes * world / (e2e_ms * 1e-3) / 1e9
+        for k in ("ms_graph", "ms_eager", "dec_ms", "e2e_ms"):
+            t = torch.tensor([res[k]], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            res[k] = float(t.item())
+    return res
 
+
+def measure_prefill(args, dev):
+    """Varlen causal prefill workload: KV write of every prompt token, then prefill.
+    The inputs (q 35.6 MB, K/V 71 MB written and read, out 35.6 MB) exceed the L2."""
+    import paged_kv_gqa_10_gb300 as pgqa
+    inp = workloads.varlen_prefill()
+    kc, vc = inp.k_cache.to(dev), inp.v_cache.to(dev)
+    q, key, value = inp.q.to(dev), inp.key.to(dev), inp.value.to(dev)
+    slots, bt, cu = inp.slot_mapping.to(dev), inp.block_tables.to(dev), inp.cu_seqlens.to(dev)
+    T, Hq, D = inp.q.shape
+    out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def write():
+        pgqa.kv_cache_write(key, value, slots, kc, vc, dev_status=status)
+
+    def prefill():
+        pgqa.paged_prefill_varlen(out, lse, q, kc, vc, bt, cu, inp.max_seqlen, inp.scale,
+                                  dev_status=status)
+
+    for _ in range(args.warmup):
+        write()
+        prefill()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    n = max(3, args.steps // 5)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    for i in range(n):
+        ev[i][0].record(stream)
+        write()
+        ev[i][1].record(stream)
+        prefill()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    w_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / n
+    p_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / n
+    flops = workloads.causal_flops(inp.seq_lens, Hq, D)
+    tflops = flops / (p_ms * 1e-3) / 1e12
+    _, bf16_peak, kind = _peaks()
+    kv_bytes = 2 * 2 * (key.numel() * 2)  # K and V: read from the input, written to the cache
+    files = ["paged_kv_gqa_10_gb300/csrc/prefill.cu", "paged_kv_gqa_10_gb300/csrc/tc.cuh",
+             "paged_kv_gqa_10_gb300/csrc/ptx.cuh"]
+    return {
+        "workload": "varlen causal prefill: 16 seqs, L U[128,2048] (T=%d), Hq=32, Hkv=8, D=128" % T,
+        "value": tflops, "unit": "TFLOP/s", "ms": p_ms,
+        "flops": flops, "flops_rule": "4*Hq*D*L(L+1)/2 per sequence (unmasked pairs only)",
+        "roofline": {"bound": "tensor", "kernel": "paged_prefill_kernel<128>", "achieved": tflops,
+                     "peak": bf16_peak, "unit": "TFLOP/s", "frac": tflops / bf16_peak,
+                     "peak_kind": kind + " bf16 burst (cuBLAS)",
+                     "traffic": _profile_traffic("prefill_varlen.json", files)},
+        "kv_cache_write": {"ms": w_ms, "bytes": kv_bytes,
+                           "GB/s": kv_bytes / (w_ms * 1e-3) / 1e9},
+    }
+
+
+DECODE_WORKLOADS = {
+    "llama3_8b": (lambda: workloads.llama3_8b_decode(rotations=ROTATIONS), WORKLOAD),
+    "70b_bf16": (lambda: workloads.llama70b_decode(rotations=ROTATIONS),
+                 "70B decode: B=32, Hq=64, Hkv=8, D=128, ctx U[1024,4096], bf16 cache"),
+    "70b_e4m3": (lambda: workloads.llama70b_decode(cache_dtype="e4m3", rotations=ROTATIONS),
+                 "70B decode: B=32, Hq=64, Hkv=8, D=128, ctx U[1024,4096], E4M3 cache"),
+    "prefix": (lambda: workloads.prefix_sharing_decode(rotations=ROTATIONS),
+               "prefix-sharing decode: B=16, ctx 8192, Hq=32, Hkv=8, D=128, groups of 4 share "
+               "4096 tokens"),
+}
+
+
+def run_ours(args):
+    dist, rank, local, world = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    make, desc = DECODE_WORKLOADS[args.workload]
+    inp = make()
+    m = measure_decode(inp, args, dev, dist, clocks_index=local)
+    b = m["bench"]
+    kv_bytes = b.kv_bytes
+    value = kv_bytes * world / (m["ms_graph"] * 1e-3) / 1e9
+    pref = measure_prefill(args, dev) if (args.workload == "llama3_8b" and not args.no_prefill) \
+        else None
     if rank != 0:
+        if dist:
+            dist.destroy_process_group()
         return 0
     hbm_peak, _, peak_kind = _peaks()
-    achieved = alg_bytes / (dec_ms * 1e-3) / 1e9
+    achieved = b.alg_bytes / (m["dec_ms"] * 1e-3) / 1e9
     dec_files = ["paged_kv_gqa_10_gb300/csrc/decode.cu", "paged_kv_gqa_10_gb300/csrc/ptx.cuh"]
+    B, Hq, D = inp.q.shape
+    dt = "e4m3 KV, bf16 q/out" if inp.cache_dtype == "e4m3" else "bf16"
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["ms_graph"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dt,
         "data": "synthetic (seeded N(0,1) bf16 q/K/V, seeded shuffled block tables)",
-        "config": {"workload": WORKLOAD, "batch": B, "q_heads": Hq, "kv_heads": Hkv,
+        "config": {"workload": desc, "batch": B, "q_heads": Hq, "kv_heads": inp.num_kv_heads,
                    "head_dim": D, "block_size": 16, "kv_bytes_per_step": kv_bytes,
-                   "step": "kv_cache_write(64 new tokens) + paged_attention_decode",
-                   "l2": f"{R} rotating block-table sets over disjoint blocks "
-                         f"({R * kv_bytes / 1e6:.0f} MB > 129 MB L2)",
+                   "unique_kv_bytes_per_step": workloads.kv_read_bytes(inp, unique=True),
+                   "step": "kv_cache_write(one new token per sequence) + paged_attention_decode, "
+                           "replayed as one CUDA graph per step",
+                   "eager_ms_per_step": m["ms_eager"],
+                   "l2": f"{b.R} rotating block-table sets over disjoint blocks "
+                         f"({b.R * kv_bytes / 1e6:.0f} MB > 129 MB L2)",
                    "parallelism": f"replica per GPU x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel<128,bf16>",
+        "roofline": {"bound": "hbm", "kernel": f"paged_decode_kernel<{D},{inp.cache_dtype}>",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_kind": peak_kind,
-                     "alg_bytes_per_launch": alg_bytes, "launch_ms": dec_ms,
-                     "traffic": _profile_traffic("decode_llama3_8b.json", dec_files)},
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                     "alg_bytes_per_launch": b.alg_bytes, "launch_ms": m["dec_ms"],
+                     "traffic": _profile_traffic("decode_llama3_8b.json", dec_files)
+                     if args.workload == "llama3_8b" else None},
+        "e2e": {"value": kv_bytes * world / (m["e2e_ms"] * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"],
+                "ms_per_step": m["e2e_ms"], "calls": "eager C-ABI calls, pinned host buffers"},
         "gpu_launches": 2 * args.steps,
-        "clocks": clocks.summary(),
+        "clocks": m["clocks"],
     }
+    if pref is not None:
+        line["prefill"] = pref
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = _cpu_baseline(inp, args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -349,6 +489,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--workload", default="llama3_8b", choices=sorted(DECODE_WORKLOADS))
+    ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
