@@ -135,17 +135,18 @@ pgqa_status_t pgqa_paged_kv_gather(const void* k_cache, const void* v_cache, int
                                    int* dev_status, void* stream);
 
 /*
- * Split plan of paged decode (host logic, no device access): how many key
- * ranges ("splits") each (sequence, kv-head) is cut into so that a device with
- * `num_sms` multiprocessors is filled. Returns the number of splits (>= 1) and
- * stores the pages per split in *pages_per_split; returns PGQA_EINVAL on a bad
- * argument.
+ * Grid of paged decode (host logic, no device access): the number of CTAs the
+ * decode kernel launches on a device with `num_sms` multiprocessors for this
+ * head_dim and cache dtype. Each CTA owns an equal share of all cached pages of
+ * the batch (laid end to end in (sequence, kv-head) order), so ragged context
+ * lengths cannot unbalance the GPU. Returns PGQA_EINVAL on a bad argument.
  */
-int pgqa_decode_split_plan(int num_seqs, int num_kv_heads, int max_context_len, int block_size,
-                           int num_sms, int* pages_per_split);
+int pgqa_decode_grid_size(int num_sms, int head_dim, int cache_dtype);
 
 /* Workspace bytes pgqa_paged_attention_decode needs on the current device for
- * these sizes (0 when no sequence is split). */
+ * these sizes (any cache dtype): one ticket counter per (sequence, kv-head) and
+ * two partial-result slots of 8 x head_dim floats per CTA. max_context_len does
+ * not change it. */
 size_t pgqa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                   int max_context_len);
 
@@ -164,13 +165,12 @@ size_t pgqa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_head
  *   context_lens  [num_seqs] int32, read; 0 gives out = 0, lse = -inf.
  *   scale         softmax scale (usually 1/sqrt(head_dim)).
  *   cache_dtype, k_scale, v_scale   as for pgqa_kv_cache_write.
- *   max_context_len  an upper bound on context_lens (sizes the split plan);
- *                 a longer context is a device error.
+ *   max_context_len  an upper bound on context_lens; a longer context is a
+ *                 device error.
  *   workspace     device scratch of at least pgqa_decode_workspace_size()
  *                 bytes, 256-byte aligned, ZERO-FILLED before its first use;
  *                 every call that completes leaves it ready for the next call.
- *                 May be NULL when that size is 0. Calls that share one
- *                 workspace must not overlap in time.
+ *                 Calls that share one workspace must not overlap in time.
  * k_cache/v_cache must be 16-byte aligned, q/out 16-byte aligned.
  */
 pgqa_status_t pgqa_paged_attention_decode(void* out, float* lse, const void* q,

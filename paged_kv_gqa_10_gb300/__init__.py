@@ -11,7 +11,7 @@ raises ImportError if the library has not been built
 Functions (same names as the C entry points, without the ``pgqa_`` prefix):
   kv_cache_write, paged_kv_gather, paged_attention_decode,
   paged_attention_decode_noalloc, paged_prefill_varlen, decode_workspace_size,
-  decode_split_plan,
+  decode_grid_size,
   prefill_workspace_size, kv_cache_bytes, status_string, abi_version.
 """
 import ctypes
@@ -23,7 +23,7 @@ __all__ = [
     "PgqaError", "BF16", "E4M3", "kv_cache_write", "paged_kv_gather",
     "paged_attention_decode", "paged_attention_decode_noalloc", "paged_prefill_varlen",
     "decode_workspace_size",
-    "decode_split_plan", "prefill_workspace_size", "kv_cache_bytes", "status_string",
+    "decode_grid_size", "prefill_workspace_size", "kv_cache_bytes", "status_string",
     "abi_version", "library_path", "lib",
 ]
 
@@ -58,7 +58,7 @@ def _load():
         "pgqa_kv_cache_bytes": ([I, I64, I, I, I], I64),
         "pgqa_kv_cache_write": ([P, P, P, I, I, I, P, P, I, I, I, P, P, P, P], I),
         "pgqa_paged_kv_gather": ([P, P, I, P, I, P, I, I, I, I, I, I, P, P, P, P], I),
-        "pgqa_decode_split_plan": ([I, I, I, I, I, ctypes.POINTER(ctypes.c_int)], I),
+        "pgqa_decode_grid_size": ([I, I, I], I),
         "pgqa_decode_workspace_size": ([I, I, I, I, I], SZ),
         "pgqa_paged_attention_decode": ([P, P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, P, P,
                                          I, P, SZ, P, P], I),
@@ -149,14 +149,12 @@ def kv_cache_bytes(num_layers, tokens, num_kv_heads, head_dim, cache_dtype=BF16)
     return _handle().pgqa_kv_cache_bytes(num_layers, tokens, num_kv_heads, head_dim, cache_dtype)
 
 
-def decode_split_plan(num_seqs, num_kv_heads, max_context_len, num_sms, block_size=16):
-    """(num_splits, pages_per_split) of paged decode for a device with num_sms SMs."""
-    pps = ctypes.c_int(0)
-    n = _handle().pgqa_decode_split_plan(num_seqs, num_kv_heads, max_context_len, block_size,
-                                         num_sms, ctypes.byref(pps))
+def decode_grid_size(num_sms, head_dim=128, cache_dtype=BF16):
+    """CTAs the decode kernel launches on a device with num_sms SMs."""
+    n = _handle().pgqa_decode_grid_size(num_sms, head_dim, cache_dtype)
     if n < 0:
-        raise PgqaError(n, "decode_split_plan")
-    return n, pps.value
+        raise PgqaError(n, "decode_grid_size")
+    return n
 
 
 def decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len) -> int:
@@ -211,7 +209,7 @@ def paged_attention_decode(out, lse, q, k_cache, v_cache, block_tables, context_
                            dev_status=None, stream=None):
     """out [B, Hq, D] bf16 and lse [B, Hq] fp32 (or None) are written.
     workspace: a zero-initialised uint8 CUDA tensor of at least
-    decode_workspace_size(...) bytes (None when that is 0)."""
+    decode_workspace_size(...) bytes."""
     _dev(out, "out", torch.bfloat16)
     _dev(lse, "lse", torch.float32)
     _dev(q, "q", torch.bfloat16)

@@ -245,24 +245,24 @@ pgqa_status_t pgqa_paged_kv_gather(const void* k_cache, const void* v_cache, int
                                 static_cast<cudaStream_t>(stream));
 }
 
-int pgqa_decode_split_plan(int num_seqs, int num_kv_heads, int max_context_len, int block_size,
-                           int num_sms, int* pages_per_split) {
-  if (num_seqs < 0 || num_kv_heads <= 0 || max_context_len < 0 || block_size <= 0 ||
-      num_sms <= 0 || pages_per_split == nullptr)
+int pgqa_decode_grid_size(int num_sms, int head_dim, int cache_dtype) {
+  if (num_sms <= 0 || (head_dim != 64 && head_dim != 128) ||
+      (cache_dtype != PGQA_DTYPE_BF16 && cache_dtype != PGQA_DTYPE_E4M3))
     return PGQA_EINVAL;
-  const pgqa::DecodePlan plan =
-      pgqa::decode_plan(num_seqs, num_kv_heads, 128, max_context_len, block_size, num_sms);
-  *pages_per_split = plan.pages_per_split;
-  return plan.num_splits;
+  return pgqa::decode_plan(1, 1, head_dim, cache_dtype, num_sms).grid;
 }
 
 size_t pgqa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                   int max_context_len) {
   (void)num_q_heads;
-  if (num_seqs <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_context_len <= 0) return 0;
-  return pgqa::decode_plan(num_seqs, num_kv_heads, head_dim, max_context_len, 16,
-                           pgqa::num_sms_current_device())
-      .bytes;
+  (void)max_context_len;
+  if (num_seqs <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
+  const int sms = pgqa::num_sms_current_device();
+  const size_t a =
+      pgqa::decode_plan(num_seqs, num_kv_heads, head_dim, PGQA_DTYPE_BF16, sms).bytes;
+  const size_t b =
+      pgqa::decode_plan(num_seqs, num_kv_heads, head_dim, PGQA_DTYPE_E4M3, sms).bytes;
+  return a > b ? a : b;
 }
 
 pgqa_status_t pgqa_paged_attention_decode(void* out, float* lse, const void* q,
@@ -291,7 +291,6 @@ pgqa_status_t pgqa_paged_attention_decode(void* out, float* lse, const void* q,
   if (!(head_dim == 128 || (head_dim == 64 && cache_dtype == PGQA_DTYPE_BF16)))
     return PGQA_EUNSUPPORTED;
   if (static_cast<int64_t>(num_blocks) * num_kv_heads * 16 > INT32_MAX) return PGQA_EUNSUPPORTED;
-  if (num_seqs > 65535 || num_kv_heads > 65535) return PGQA_EUNSUPPORTED;
   if (num_seqs == 0) return PGQA_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PGQA_EINVAL;
   if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
@@ -299,11 +298,9 @@ pgqa_status_t pgqa_paged_attention_decode(void* out, float* lse, const void* q,
   const int sms = pgqa::num_sms_current_device();
   if (sms <= 0) return PGQA_ECUDA;
   const pgqa::DecodePlan plan =
-      pgqa::decode_plan(num_seqs, num_kv_heads, head_dim, max_context_len, block_size, sms);
-  if (plan.bytes > 0) {
-    if (workspace == nullptr || workspace_bytes < plan.bytes) return PGQA_ENOWORKSPACE;
-    if (!aligned(workspace, 256)) return PGQA_EINVAL;
-  }
+      pgqa::decode_plan(num_seqs, num_kv_heads, head_dim, cache_dtype, sms);
+  if (workspace == nullptr || workspace_bytes < plan.bytes) return PGQA_ENOWORKSPACE;
+  if (!aligned(workspace, 256)) return PGQA_EINVAL;
   pgqa::DecodeArgs a;
   a.out = out;
   a.lse = lse;

@@ -1,24 +1,28 @@
 // Paged decode attention for sm_103a.
 //
 // Computes, for every sequence b and query head hq, softmax(scale * q K^T) V over
-// the b's cached tokens read through its block table ("LLaMA structure and
-// inference performance" (wmrh.cn) sec. 3.1 steps 3-6, with repeat_kv of sec.
-// 2.1 as the index map kv_head = hq / G; pages addressed as in the rkmt.cn
-// article, sec. 3.1), plus lse = ln sum exp(score).
+// b's cached tokens read through its block table ("LLaMA structure and inference
+// performance" (wmrh.cn) sec. 3.1 steps 3-6, with repeat_kv of sec. 2.1 as the
+// index map kv_head = hq / G; pages addressed as in the rkmt.cn article, sec. 3.1),
+// plus lse = ln sum exp(score).
 //
-// Work decomposition (bandwidth-bound: every KV byte must be read exactly once)
-//  - One CTA per (split, kv-head, sequence). It serves all G = Hq/Hkv query
-//    heads of its kv-head, so a K/V page is fetched once for the whole group.
-//  - Long contexts are cut into splits of `pages_per_split` 16-token pages so
-//    that the grid fills the 152 SMs; split results are merged with their LSEs
-//    by whichever CTA of the (sequence, kv-head) finishes last (an atomic ticket,
-//    no CTA ever waits for another).
-//  - Warp roles: one producer warp streams pages with TMA (2-D tensor map over
-//    the cache viewed as [num_blocks*Hkv*16 rows][head_dim], 128-byte swizzle)
-//    into mbarrier-guarded stages; NW consumer warps take pages round-robin,
-//    each keeping its own online-softmax state, merged at the end. Every consumer
-//    warp owns its own sub-ring of stages, so consecutive uses of a stage belong
-//    to one warp and a parity wait can never be two phases behind.
+// Work decomposition (bandwidth-bound: every KV byte is read exactly once)
+//  - A unit is one (sequence, kv-head): its pages are read once for all G = Hq/Hkv
+//    query heads of the group.
+//  - Stream-K: the units' pages, laid end to end in (sequence, kv-head, page) order,
+//    are cut into equal ranges, one per CTA of a grid sized to fill the GPU (SMs x
+//    resident CTAs). Each CTA streams its range without a break, so ragged context
+//    lengths cannot unbalance the grid. Units inside a range are finished in place;
+//    a unit cut by range boundaries is finished by whichever of its CTAs arrives
+//    last (an atomic ticket: no CTA waits for another), which merges the partial
+//    results with their LSEs. Only the first and the last unit of a range can be
+//    cut, so each CTA owns two partial slots.
+//  - Warp roles: one producer warp streams pages with TMA (2-D tensor map over the
+//    cache viewed as [num_blocks*Hkv*16 rows][head_dim], 128-byte swizzle) into
+//    mbarrier-guarded stages and stages each unit's G query rows into a double
+//    buffer with a bulk copy; 4 consumer warps take pages round-robin. Each consumer
+//    warp owns its own sub-ring of stages, so consecutive uses of a stage belong to
+//    one warp and a parity wait can never be two phases behind.
 //  - Math per 16-token page on the warp-level tensor path (mma.m16n8k16):
 //      S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8]   (tokens fill M = 16)
 //      online softmax on the S^T fragment (column = query head)
@@ -30,6 +34,8 @@
 //    The head-dimension order inside an MMA is a free permutation (it is the
 //    contraction index for QK^T and a row relabelling for PV), chosen so that each
 //    thread's bytes are contiguous in shared memory.
+//  - Every wait is bounded; a warp whose wait gives up records PGQA_ETIMEOUT, stops
+//    computing, but keeps taking part in every CTA barrier, so nothing can hang.
 #include <cuda_bf16.h>
 #include <float.h>
 
@@ -39,10 +45,9 @@
 namespace pgqa {
 namespace {
 
-constexpr int kNW = 4;              // consumer warps per CTA
+constexpr int kNW = 4;  // consumer warps per CTA
 constexpr int kThreads = (kNW + 1) * 32;
-constexpr int kMinPagesPerSplit = 8;  // never split below 128 tokens
-constexpr int kCtasPerSmTarget = 8;   // aim for this many (split) CTAs per SM
+constexpr int kMinChunk = 8;  // pages per CTA range, at least
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -54,15 +59,14 @@ struct DecodeParams {
   const int32_t* context_lens;
   const float* k_scale;
   const float* v_scale;
-  int* counters;
-  float* ws_lse;
-  float* ws_o;
+  int* counters;    // [B * Hkv] tickets, zero between calls
+  float* part_lse;  // [grid][2][8] base-2 LSE of a partial (+inf = poisoned)
+  float* part_o;    // [grid][2][8][D] normalised partial output
   int* dev_status;
   int max_blocks_per_seq;
-  int num_q_heads, num_kv_heads, group;
+  int num_seqs, num_q_heads, num_kv_heads, group;
   int num_blocks;
   int max_context_len;
-  int pages_per_split, num_splits;
   float scale_log2;  // scale * log2(e)
 };
 
@@ -73,178 +77,327 @@ struct Cfg {
   static constexpr int kSub = kRowBytes / 128;     // 128-byte TMA boxes per row
   static constexpr int kPageBytes = 16 * kRowBytes;
   static constexpr int kStageBytes = 2 * kPageBytes;  // K page + V page
-  static constexpr int kStagesPerWarp = kFp8 ? 3 : 2;  // each consumer warp owns a sub-ring
+  static constexpr int kStagesPerWarp = kFp8 ? 3 : 2;
   static constexpr int kStages = kNW * kStagesPerWarp;
-  static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kNkc = D / 16;              // 16-wide chunks of head_dim
-  static constexpr int kMergeBytes = kNW * 8 * D * 4;
-  static constexpr int kSmem = 1024 + kRingBytes + 2 * kStages * 8 + 16 + kNW * 8 * 2 * 4;
+  static constexpr int kRing = kStages * kStageBytes;
+  static constexpr int kQBuf = 8 * D * 2;          // up to 8 bf16 query rows
+  static constexpr int kMerge = kNW * 8 * D * 4;   // per-warp O of one unit
+  static constexpr int kOffQ = kRing;
+  static constexpr int kOffMerge = kOffQ + 2 * kQBuf;
+  static constexpr int kOffMl = kOffMerge + kMerge;                   // [kNW][8][2] float
+  static constexpr int kOffBar = kOffMl + kNW * 8 * 2 * 4;            // full, empty, q_full, q_empty
+  static constexpr int kOffMeta = kOffBar + (2 * kStages + 4) * 8;    // [S] int
+  static constexpr int kOffMisc = kOffMeta + kStages * 4;             // 32 ints + 8 int64
+  static constexpr int kSmem = 1024 + kOffMisc + 32 * 4 + 8 * 8;
   static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle rows");
-  static_assert(kMergeBytes <= kRingBytes, "merge buffers reuse the ring");
 };
 
-template <int D>
-__device__ __forceinline__ void zero_outputs(const DecodeParams& p, int b, int h) {
-  const int G = p.group;
-  for (int i = threadIdx.x; i < G * D / 8; i += blockDim.x) {
-    const int g = i / (D / 8), c = i % (D / 8);
-    const size_t row = static_cast<size_t>(b) * p.num_q_heads + h * G + g;
-    reinterpret_cast<uint4*>(p.out + row * D)[c] = make_uint4(0, 0, 0, 0);
-    if (c == 0 && p.lse) p.lse[row] = -INFINITY;
+// CTAs of one decode kernel resident per SM (the grid is this times the SM count).
+template <int D, bool kFp8>
+constexpr int ctas_per_sm() {
+  return (227 * 1024) / (Cfg<D, kFp8>::kSmem + 1024) >= 2 ? 2 : 1;
+}
+
+__device__ __forceinline__ int pages_of(const DecodeParams& p, int b, bool* valid = nullptr) {
+  const int L = __ldg(p.context_lens + b);
+  const int n = (L + 15) >> 4;
+  const bool ok = L >= 0 && L <= p.max_context_len && n <= p.max_blocks_per_seq;
+  if (valid) *valid = ok;
+  return ok ? n : 0;
+}
+
+// Sum over the CTA (every thread of the CTA must call it).
+__device__ __forceinline__ long long block_sum(long long v, long long* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  long long t = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) t += scratch[w];
+  return t;
+}
+
+// Inclusive prefix sum over the CTA's threads; *total receives the sum.
+__device__ __forceinline__ long long block_scan(long long v, long long* scratch,
+                                                long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
   }
+  __syncthreads();
+  if (lane == 31) scratch[warp] = v;
+  __syncthreads();
+  long long before = 0, t = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) {
+    if (w < warp) before += scratch[w];
+    t += scratch[w];
+  }
+  *total = t;
+  return v + before;
+}
+
+// A CTA's walk over units: unit (b, h) holds pages [S, S + P) of the global order.
+struct Walk {
+  int b, h, P;
+  long long S;
+  __device__ __forceinline__ void next(const DecodeParams& p) {
+    S += P;
+    if (++h == p.num_kv_heads) {
+      h = 0;
+      do {
+        ++b;
+        P = b < p.num_seqs ? pages_of(p, b) : 0;
+      } while (P == 0 && b < p.num_seqs);
+    }
+  }
+};
+
+__device__ __forceinline__ void bar_consumers() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kNW * 32) : "memory");
 }
 
 template <int D, bool kFp8>
-__global__ void __launch_bounds__(kThreads) paged_decode_kernel(
+__global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_decode_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const DecodeParams p) {
   using C = Cfg<D, kFp8>;
   constexpr int S = C::kStages;
+  constexpr int SPW = C::kStagesPerWarp;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(ring + C::kRingBytes);
+  uint8_t* qbuf = smem + C::kOffQ;
+  float* wo = reinterpret_cast<float*>(smem + C::kOffMerge);  // [kNW][8][D]
+  float* wml = reinterpret_cast<float*>(smem + C::kOffMl);    // [kNW][8][2] (m, l) base 2
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* empty = full + S;
-  int* flags = reinterpret_cast<int*>(empty + S);  // [0] bad block id, [1] timeout, [2] last
-  float* wml = reinterpret_cast<float*>(flags + 4);  // [kNW][8][2] per-warp (m, l), base 2
-  float* wo = reinterpret_cast<float*>(ring);        // [kNW][8][D] per-warp O, after the loop
+  uint64_t* q_full = empty + S;    // [2]
+  uint64_t* q_empty = q_full + 2;  // [2]
+  int* meta = reinterpret_cast<int*>(smem + C::kOffMeta);  // per stage: bad block id seen
+  int* misc = reinterpret_cast<int*>(smem + C::kOffMisc);
+  long long* scratch = reinterpret_cast<long long*>(misc + 32);  // 8 slots
 
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = p.group;
-  const int L = __ldg(p.context_lens + b);
-  const int npages_all = (L + 15) >> 4;
-  const bool len_bad = L < 0 || L > p.max_context_len || npages_all > p.max_blocks_per_seq;
-  if (len_bad || L == 0) {
-    if (split == 0) {
-      if (len_bad && tid == 0) record_status(p.dev_status, PGQA_EINVAL);
-      zero_outputs<D>(p, b, h);
+  const int c = blockIdx.x, ncta = gridDim.x;
+  const int G = p.group, Hkv = p.num_kv_heads, B = p.num_seqs;
+
+  // ---- the global page order holds N pages; this CTA owns [r0, r1)
+  long long local = 0;
+  for (int b = tid; b < B; b += kThreads) local += pages_of(p, b);
+  const long long N = static_cast<long long>(Hkv) * block_sum(local, scratch);
+  long long chunk = N > 0 ? (N + ncta - 1) / ncta : 0;
+  if (chunk > 0 && chunk < kMinChunk) chunk = kMinChunk;
+  const long long r0 = static_cast<long long>(c) * chunk;
+  const long long r1 = r0 + chunk < N ? r0 + chunk : N;
+
+  // ---- sequences with nothing to read (empty or invalid), spread over the CTAs:
+  //      out = 0, lse = -inf
+  for (int b = c; b < B; b += ncta) {
+    bool valid;
+    if (pages_of(p, b, &valid) != 0) continue;
+    if (!valid && tid == 0) record_status(p.dev_status, PGQA_EINVAL);
+    for (int i = tid; i < p.num_q_heads * (D / 8); i += kThreads) {
+      const size_t row = static_cast<size_t>(b) * p.num_q_heads + i / (D / 8);
+      reinterpret_cast<uint4*>(p.out + row * D)[i % (D / 8)] = make_uint4(0, 0, 0, 0);
+      if (i % (D / 8) == 0 && p.lse) p.lse[row] = -INFINITY;
     }
-    return;
   }
-  const int pps = p.pages_per_split;
-  const int p0 = split * pps;
-  if (p0 >= npages_all) return;
-  const int np = min(pps, npages_all - p0);
-  const int nsplit = (npages_all + pps - 1) / pps;
+  if (r0 >= r1) return;
+
+  // ---- find the unit holding r0 (a CTA-wide scan over the sequences)
+  if (tid == 0) misc[0] = -1;
+  long long running = 0;  // pages of the sequences before `base`
+  for (int base = 0; base < B; base += kThreads) {
+    const int b = base + tid;
+    const long long P = b < B ? pages_of(p, b) : 0;
+    long long tot;
+    const long long incl = block_scan(P, scratch, &tot);
+    const long long s0 = static_cast<long long>(Hkv) * (running + incl - P);
+    if (P > 0 && s0 <= r0 && r0 < s0 + Hkv * P) {
+      misc[0] = b;
+      scratch[6] = s0;
+    }
+    running += tot;
+    __syncthreads();
+    if (misc[0] >= 0) break;
+  }
+  Walk w0;
+  w0.b = misc[0];
+  w0.P = pages_of(p, w0.b);
+  w0.h = static_cast<int>((r0 - scratch[6]) / w0.P);
+  w0.S = scratch[6] + static_cast<long long>(w0.h) * w0.P;
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    flags[0] = flags[1] = flags[2] = 0;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], kNW);
+    }
     fence_mbar_init();
   }
   __syncthreads();
 
-  // ------------------------------------------------------------ producer
+  // ================================================================ producer
   if (warp == kNW) {
     if (lane == 0) {
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
     }
-    const int32_t* bt = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq + p0;
-    int issued = 0;
     bool ok = true;
-    for (int base = 0; base < np && ok; base += 32) {
-      const int32_t mine = base + lane < np ? __ldg(bt + base + lane) : 0;
-      const int n = min(32, np - base);
-      for (int k = 0; k < n; ++k) {
-        int32_t pbn = __shfl_sync(0xffffffffu, mine, k);
-        const int i = base + k;
-        if (lane == 0) {
-          const int li = i / kNW;  // index among this consumer warp's pages
-          const int s = (i % kNW) * C::kStagesPerWarp + li % C::kStagesPerWarp;
-          const int use = li / C::kStagesPerWarp;
-          if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
-            record_status(p.dev_status, PGQA_ETIMEOUT);
-            flags[1] = 1;
-            ok = false;
-          } else {
-            if (pbn < 0 || pbn >= p.num_blocks) {
-              flags[0] = 1;
-              pbn = 0;  // load a valid page; the result is discarded
-            }
-            uint8_t* st = ring + s * C::kStageBytes;
-            mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-            const int y = (pbn * p.num_kv_heads + h) * 16;
-#pragma unroll
-            for (int sub = 0; sub < C::kSub; ++sub)
-              tma_load_2d(st + sub * 2048, &kmap, &full[s], sub * (128 / C::kElem), y);
-#pragma unroll
-            for (int sub = 0; sub < C::kSub; ++sub)
-              tma_load_2d(st + C::kPageBytes + sub * 2048, &vmap, &full[s],
-                          sub * (128 / C::kElem), y);
-            ++issued;
-          }
+    int issued = 0, units = 0;
+    for (Walk w = w0; w.S < r1 && ok; w.next(p), ++units) {
+      const int seg0 = static_cast<int>((r0 > w.S ? r0 : w.S) - w.S);
+      const int seg1 = static_cast<int>((r1 < w.S + w.P ? r1 : w.S + w.P) - w.S);
+      // this unit's G query rows -> q buffer (units & 1)
+      if (lane == 0) {
+        const int qs = units & 1;
+        if (units >= 2 && !mbar_wait(&q_empty[qs], ((units >> 1) - 1) & 1)) {
+          record_status(p.dev_status, PGQA_ETIMEOUT);
+          ok = false;
+        } else {
+          const uint32_t bytes = static_cast<uint32_t>(G * D * 2);
+          mbar_arrive_expect_tx(&q_full[qs], bytes);
+          bulk_load(qbuf + qs * C::kQBuf,
+                    p.q + (static_cast<size_t>(w.b) * p.num_q_heads + w.h * G) * D, bytes,
+                    &q_full[qs]);
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      const int32_t* bt = p.block_tables + static_cast<size_t>(w.b) * p.max_blocks_per_seq;
+      for (int base = seg0; base < seg1 && ok; base += 32) {
+        const int32_t mine = base + lane < seg1 ? __ldg(bt + base + lane) : 0;
+        const int n = min(32, seg1 - base);
+        for (int k = 0; k < n; ++k) {
+          int32_t pbn = __shfl_sync(0xffffffffu, mine, k);
+          if (lane == 0) {
+            const int i = issued;  // CTA-local page index
+            const int li = i / kNW;
+            const int s = (i % kNW) * SPW + li % SPW;
+            const int use = li / SPW;
+            if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
+              record_status(p.dev_status, PGQA_ETIMEOUT);
+              ok = false;
+            } else {
+              int bad = 0;
+              if (pbn < 0 || pbn >= p.num_blocks) {
+                bad = 1;
+                pbn = 0;  // load a valid page; the unit's result is discarded
+                record_status(p.dev_status, PGQA_EBADINDEX);
+              }
+              meta[s] = bad;
+              uint8_t* st = ring + s * C::kStageBytes;
+              mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+              const int y = (pbn * Hkv + w.h) * 16;
+#pragma unroll
+              for (int sub = 0; sub < C::kSub; ++sub)
+                tma_load_2d(st + sub * 2048, &kmap, &full[s], sub * (128 / C::kElem), y);
+#pragma unroll
+              for (int sub = 0; sub < C::kSub; ++sub)
+                tma_load_2d(st + C::kPageBytes + sub * 2048, &vmap, &full[s],
+                            sub * (128 / C::kElem), y);
+              ++issued;
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+        }
       }
     }
-    // No TMA write may land after this CTA moves on: wait for the last phase of
-    // every stage used (already complete on the normal path).
+    // No bulk or TMA write may land after this CTA exits: wait for the last fill of
+    // every stage and of both q buffers (complete already on the normal path).
     if (lane == 0) {
       for (int w = 0; w < kNW; ++w) {
-        const int n_w = issued > w ? (issued - w + kNW - 1) / kNW : 0;  // pages issued to w
-        for (int k = 0; k < C::kStagesPerWarp && k < n_w; ++k) {
-          const int last_li = k + ((n_w - 1 - k) / C::kStagesPerWarp) * C::kStagesPerWarp;
-          if (!mbar_wait(&full[w * C::kStagesPerWarp + k], (last_li / C::kStagesPerWarp) & 1))
+        const int n_w = issued > w ? (issued - w + kNW - 1) / kNW : 0;
+        for (int k = 0; k < SPW && k < n_w; ++k) {
+          const int last_li = k + ((n_w - 1 - k) / SPW) * SPW;
+          if (!mbar_wait(&full[w * SPW + k], (last_li / SPW) & 1))
             record_status(p.dev_status, PGQA_ETIMEOUT);
         }
       }
+      for (int qs = 0; qs < 2 && qs < units; ++qs) {
+        const int last = qs + ((units - 1 - qs) / 2) * 2;
+        if (!mbar_wait(&q_full[qs], (last >> 1) & 1)) record_status(p.dev_status, PGQA_ETIMEOUT);
+      }
     }
+    return;
   }
 
-  // ------------------------------------------------------------ consumers
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-  float acc[C::kNkc][4];
-#pragma unroll
-  for (int i = 0; i < C::kNkc; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  // ================================================================ consumers
   const int gid = lane >> 2, tig = lane & 3;
+  const uint32_t rowK = (lane & 7) + (((lane >> 3) & 1) << 3);
+  const uint32_t cK = lane >> 4;
+  const uint32_t rowV = (lane & 7) + ((lane >> 4) << 3);
+  const uint32_t cV = (lane >> 3) & 1;
+  bool alive = true;  // false once one of this warp's waits gave up
+  int i_base = 0;     // CTA-local index of the unit's first page
+  int units = 0;
+  for (Walk w = w0; w.S < r1; w.next(p), ++units) {
+    const int seg0 = static_cast<int>((r0 > w.S ? r0 : w.S) - w.S);
+    const int seg1 = static_cast<int>((r1 < w.S + w.P ? r1 : w.S + w.P) - w.S);
+    const int npg = seg1 - seg0;
+    const int L = __ldg(p.context_lens + w.b);
+    const int qs = units & 1;
 
-  if (warp < kNW) {
-    // Q^T as the B operand: column n = query head gid of the group.
+    // Q^T fragments (B operand, column n = query head gid) from the staged rows
     uint32_t qf[C::kNkc][2];
+    if (alive && !mbar_wait(&q_full[qs], (units >> 1) & 1)) {
+      alive = false;
+      record_status(p.dev_status, PGQA_ETIMEOUT);
+    }
     {
-      const bool live = gid < G;
+      const bool live = gid < G && alive;
       const __nv_bfloat16* qrow =
-          p.q + (static_cast<size_t>(b) * p.num_q_heads + h * G + (live ? gid : 0)) * D;
+          reinterpret_cast<const __nv_bfloat16*>(qbuf + qs * C::kQBuf) + (live ? gid : 0) * D;
 #pragma unroll
       for (int kc = 0; kc < C::kNkc; ++kc) {
         if constexpr (!kFp8) {
           const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow + 16 * kc + 2 * tig);
-          qf[kc][0] = live ? __ldg(q32) : 0u;
-          qf[kc][1] = live ? __ldg(q32 + 4) : 0u;
+          qf[kc][0] = live ? q32[0] : 0u;
+          qf[kc][1] = live ? q32[4] : 0u;
         } else {
           // k index 2tig+{0,1} <-> d = 16kc + 4tig + {0,1}; 2tig+8+{0,1} <-> +{2,3}
-          const uint2 q4 = live ? __ldg(reinterpret_cast<const uint2*>(qrow + 16 * kc + 4 * tig))
-                                : make_uint2(0, 0);
+          const uint2 q4 =
+              live ? *reinterpret_cast<const uint2*>(qrow + 16 * kc + 4 * tig) : make_uint2(0, 0);
           qf[kc][0] = pack_f16(bf16_lo(q4.x), bf16_hi(q4.x));
           qf[kc][1] = pack_f16(bf16_lo(q4.y), bf16_hi(q4.y));
         }
       }
     }
-    const float sl2 = p.scale_log2 * (kFp8 ? __ldg(p.k_scale + h) : 1.f);
-    // lane-invariant parts of the ldmatrix addresses
-    const uint32_t rowK = (lane & 7) + (((lane >> 3) & 1) << 3);
-    const uint32_t cK = lane >> 4;
-    const uint32_t rowV = (lane & 7) + ((lane >> 4) << 3);
-    const uint32_t cV = (lane >> 3) & 1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&q_empty[qs]);
 
-    for (int i = warp; i < np; i += kNW) {
+    const float sl2 = p.scale_log2 * (kFp8 ? __ldg(p.k_scale + w.h) : 1.f);
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    float acc[C::kNkc][4];
+#pragma unroll
+    for (int i = 0; i < C::kNkc; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    int bad = 0;
+
+    // this warp's pages of the unit: CTA-local index i = i_base + j with i % kNW == warp
+    for (int j = (warp - i_base % kNW + kNW) % kNW; j < npg && alive; j += kNW) {
+      const int i = i_base + j;
       const int li = i / kNW;
-      const int s = warp * C::kStagesPerWarp + li % C::kStagesPerWarp;
-      if (!mbar_wait(&full[s], (li / C::kStagesPerWarp) & 1)) {
+      const int s = warp * SPW + li % SPW;
+      if (!mbar_wait(&full[s], (li / SPW) & 1)) {
+        alive = false;
         record_status(p.dev_status, PGQA_ETIMEOUT);
-        flags[1] = 1;
         break;
       }
+      bad |= meta[s];
       const uint32_t stK = smem_u32(ring + s * C::kStageBytes);
       const uint32_t stV = stK + C::kPageBytes;
-      const int nv = min(16, L - (p0 + i) * 16);  // valid tokens in this page
+      const int nv = min(16, L - (seg0 + j) * 16);  // valid tokens in this page
 
       // ---- S^T = K Q^T
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -258,12 +411,12 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(
       } else {
 #pragma unroll
         for (int kc = 0; kc < C::kNkc; kc += 2) {
-          uint32_t r0, r1, r2, r3;
-          ldsm_x4(stK + swz128(rowK, kc + cK), r0, r1, r2, r3);
-          mma_f16(sc, e4m3x2_to_f16x2(r0 & 0xffff), e4m3x2_to_f16x2(r1 & 0xffff),
-                  e4m3x2_to_f16x2(r0 >> 16), e4m3x2_to_f16x2(r1 >> 16), qf[kc][0], qf[kc][1]);
-          mma_f16(sc, e4m3x2_to_f16x2(r2 & 0xffff), e4m3x2_to_f16x2(r3 & 0xffff),
-                  e4m3x2_to_f16x2(r2 >> 16), e4m3x2_to_f16x2(r3 >> 16), qf[kc + 1][0],
+          uint32_t r0v, r1v, r2v, r3v;
+          ldsm_x4(stK + swz128(rowK, kc + cK), r0v, r1v, r2v, r3v);
+          mma_f16(sc, e4m3x2_to_f16x2(r0v & 0xffff), e4m3x2_to_f16x2(r1v & 0xffff),
+                  e4m3x2_to_f16x2(r0v >> 16), e4m3x2_to_f16x2(r1v >> 16), qf[kc][0], qf[kc][1]);
+          mma_f16(sc, e4m3x2_to_f16x2(r2v & 0xffff), e4m3x2_to_f16x2(r3v & 0xffff),
+                  e4m3x2_to_f16x2(r2v >> 16), e4m3x2_to_f16x2(r3v >> 16), qf[kc + 1][0],
                   qf[kc + 1][1]);
         }
       }
@@ -298,7 +451,8 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(
       const uint32_t pb1 = movmatrix_t(kFp8 ? pack_f16(p2v, p3v) : pack_bf16(p2v, p3v));
 
       // ---- O^T += V^T P^T; rows past the context are zeroed (they may hold NaN)
-      const uint32_t m01 = (2 * tig < nv ? 0x0000ffffu : 0u) | (2 * tig + 1 < nv ? 0xffff0000u : 0u);
+      const uint32_t m01 =
+          (2 * tig < nv ? 0x0000ffffu : 0u) | (2 * tig + 1 < nv ? 0xffff0000u : 0u);
       const uint32_t m89 =
           (2 * tig + 8 < nv ? 0x0000ffffu : 0u) | (2 * tig + 9 < nv ? 0xffff0000u : 0u);
       if constexpr (!kFp8) {
@@ -340,17 +494,15 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    // full row sums for this thread's two head columns
+    i_base += npg;
+
+    // ---- this warp's state for the unit -> shared memory
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
       l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], o);
       l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], o);
     }
-  }
-  __syncthreads();  // every page consumed and every TMA landed: the ring is free
-
-  // ---- per-warp state to shared memory
-  if (warp < kNW) {
+    const bool poisoned_w = __any_sync(0xffffffffu, bad != 0) || !__all_sync(0xffffffffu, alive);
 #pragma unroll
     for (int dc = 0; dc < C::kNkc; ++dc) {
       int d0, d1;
@@ -369,104 +521,108 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(
       o1[d1] = acc[dc][3];
     }
     if (gid == 0) {
-      wml[(warp * 8 + 2 * tig) * 2 + 0] = m_run[0];
-      wml[(warp * 8 + 2 * tig) * 2 + 1] = l_run[0];
-      wml[(warp * 8 + 2 * tig + 1) * 2 + 0] = m_run[1];
-      wml[(warp * 8 + 2 * tig + 1) * 2 + 1] = l_run[1];
+      float* ml = wml + (warp * 8 + 2 * tig) * 2;
+      ml[0] = m_run[0];
+      ml[1] = poisoned_w ? NAN : l_run[0];  // NaN l marks a poisoned warp state
+      ml[2] = m_run[1];
+      ml[3] = poisoned_w ? NAN : l_run[1];
     }
-  }
-  __syncthreads();
+    bar_consumers();
 
-  const bool bad = flags[0] != 0 || flags[1] != 0;
-  if (flags[0] != 0 && tid == 0) record_status(p.dev_status, PGQA_EBADINDEX);
-  const int u = b * p.num_kv_heads + h;
-  const float vsc = kFp8 ? __ldg(p.v_scale + h) : 1.f;
-  constexpr int kChunks = D / 8;  // 8 consecutive d per thread item
-
-  // ---- combine the warps: M = max m_w, l = sum l_w 2^(m_w - M), O likewise
-  for (int it = tid; it < G * kChunks; it += blockDim.x) {
-    const int g = it / kChunks, c = it % kChunks;
-    float M = -INFINITY;
+    // ---- combine the warps: M = max m_w, l = sum l_w 2^(m_w - M), O likewise
+    const int u = w.b * Hkv + w.h;
+    const long long c_first = w.S / chunk, c_last = (w.S + w.P - 1) / chunk;
+    const int nseg = static_cast<int>(c_last - c_first + 1);
+    const int slot = (w.S <= r0) ? 0 : 1;  // 0: this unit is the first of this CTA's range
+    const float vsc = kFp8 ? __ldg(p.v_scale + w.h) : 1.f;
+    constexpr int kChunks = D / 8;  // 8 consecutive d per work item
+    for (int it = tid; it < G * kChunks; it += kNW * 32) {
+      const int g = it / kChunks, cc = it % kChunks;
+      float M = -INFINITY;
+      bool poisoned = false;
 #pragma unroll
-    for (int w = 0; w < kNW; ++w) M = fmaxf(M, wml[(w * 8 + g) * 2]);
-    float lsum = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int w = 0; w < kNW; ++w) {
-      const float mw = wml[(w * 8 + g) * 2];
-      const float wt = mw == -INFINITY ? 0.f : ex2(mw - M);
-      lsum += wml[(w * 8 + g) * 2 + 1] * wt;
-      const float4* src = reinterpret_cast<const float4*>(wo + (w * 8 + g) * D + c * 8);
-      const float4 x = src[0], y = src[1];
-      o[0] += x.x * wt; o[1] += x.y * wt; o[2] += x.z * wt; o[3] += x.w * wt;
-      o[4] += y.x * wt; o[5] += y.y * wt; o[6] += y.z * wt; o[7] += y.w * wt;
-    }
-    const float inv = 1.f / lsum;
-    const float lse2 = M + log2f(lsum);
-    const size_t row = static_cast<size_t>(b) * p.num_q_heads + h * G + g;
-    if (nsplit == 1) {
-      uint4 pk;
-      if (bad) {
-        pk = make_uint4(0, 0, 0, 0);
-      } else {
-        const float f = inv * vsc;
-        pk = make_uint4(pack_bf16(o[0] * f, o[1] * f), pack_bf16(o[2] * f, o[3] * f),
-                        pack_bf16(o[4] * f, o[5] * f), pack_bf16(o[6] * f, o[7] * f));
+      for (int ww = 0; ww < kNW; ++ww) {
+        M = fmaxf(M, wml[(ww * 8 + g) * 2]);
+        poisoned |= isnan(wml[(ww * 8 + g) * 2 + 1]);
       }
-      reinterpret_cast<uint4*>(p.out + row * D)[c] = pk;
-      if (c == 0 && p.lse) p.lse[row] = bad ? -INFINITY : lse2 * kLn2;
-    } else {
-      const size_t slot = (static_cast<size_t>(u) * p.num_splits + split) * 8 + g;
-      float4* dst = reinterpret_cast<float4*>(p.ws_o + slot * D + c * 8);
-      dst[0] = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
-      dst[1] = make_float4(o[4] * inv, o[5] * inv, o[6] * inv, o[7] * inv);
-      if (c == 0) p.ws_lse[slot] = bad ? INFINITY : lse2;
-    }
-  }
-  if (nsplit == 1) return;
-
-  // ---- split-K: the last CTA of this (sequence, kv-head) to arrive merges
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    // atomicInc wraps to 0 on the last arrival, leaving the counter ready for the next call
-    const unsigned prev = atomicInc(reinterpret_cast<unsigned*>(p.counters + u),
-                                    static_cast<unsigned>(nsplit - 1));
-    flags[2] = prev == static_cast<unsigned>(nsplit - 1);
-  }
-  __syncthreads();
-  if (!flags[2]) return;
-  __threadfence();
-  for (int it = tid; it < G * kChunks; it += blockDim.x) {
-    const int g = it / kChunks, c = it % kChunks;
-    const size_t base = static_cast<size_t>(u) * p.num_splits * 8 + g;
-    float M = -INFINITY;
-    bool any_bad = false;
-    for (int s = 0; s < nsplit; ++s) {
-      const float ls = __ldcg(p.ws_lse + base + s * 8);
-      any_bad |= ls == INFINITY;
-      M = fmaxf(M, ls);
-    }
-    float lsum = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (!any_bad) {
-      for (int s = 0; s < nsplit; ++s) {
-        const float wt = ex2(__ldcg(p.ws_lse + base + s * 8) - M);
-        lsum += wt;
-        const float4* src =
-            reinterpret_cast<const float4*>(p.ws_o + (base + s * 8) * D + c * 8);
-        const float4 x = __ldcg(src), y = __ldcg(src + 1);
+      float lsum = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ww = 0; ww < kNW; ++ww) {
+        const float mw = wml[(ww * 8 + g) * 2];
+        const float wt = mw == -INFINITY ? 0.f : ex2(mw - M);
+        lsum += wml[(ww * 8 + g) * 2 + 1] * wt;
+        const float4* src = reinterpret_cast<const float4*>(wo + (ww * 8 + g) * D + cc * 8);
+        const float4 x = src[0], y = src[1];
         o[0] += x.x * wt; o[1] += x.y * wt; o[2] += x.z * wt; o[3] += x.w * wt;
         o[4] += y.x * wt; o[5] += y.y * wt; o[6] += y.z * wt; o[7] += y.w * wt;
       }
+      const float inv = 1.f / lsum;
+      const size_t row = static_cast<size_t>(w.b) * p.num_q_heads + w.h * G + g;
+      if (nseg == 1) {
+        uint4 pk = make_uint4(0, 0, 0, 0);
+        if (!poisoned) {
+          const float f = inv * vsc;
+          pk = make_uint4(pack_bf16(o[0] * f, o[1] * f), pack_bf16(o[2] * f, o[3] * f),
+                          pack_bf16(o[4] * f, o[5] * f), pack_bf16(o[6] * f, o[7] * f));
+        }
+        reinterpret_cast<uint4*>(p.out + row * D)[cc] = pk;
+        if (cc == 0 && p.lse) p.lse[row] = poisoned ? -INFINITY : (M + log2f(lsum)) * kLn2;
+      } else {
+        const size_t ps = (static_cast<size_t>(c) * 2 + slot) * 8 + g;
+        float4* dst = reinterpret_cast<float4*>(p.part_o + ps * D + cc * 8);
+        dst[0] = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
+        dst[1] = make_float4(o[4] * inv, o[5] * inv, o[6] * inv, o[7] * inv);
+        if (cc == 0) p.part_lse[ps] = poisoned ? INFINITY : M + log2f(lsum);
+      }
     }
-    const size_t row = static_cast<size_t>(b) * p.num_q_heads + h * G + g;
-    uint4 pk = make_uint4(0, 0, 0, 0);
-    if (!any_bad) {
-      const float f = vsc / lsum;
-      pk = make_uint4(pack_bf16(o[0] * f, o[1] * f), pack_bf16(o[2] * f, o[3] * f),
-                      pack_bf16(o[4] * f, o[5] * f), pack_bf16(o[6] * f, o[7] * f));
+    bar_consumers();  // merge buffers free; this CTA's partial writes are issued
+    if (nseg > 1) {
+      if (tid == 0) {
+        __threadfence();
+        // atomicInc wraps to 0 on the last arrival, leaving the ticket ready for the next call
+        const unsigned prev = atomicInc(reinterpret_cast<unsigned*>(p.counters + u),
+                                        static_cast<unsigned>(nseg - 1));
+        misc[1] = prev == static_cast<unsigned>(nseg - 1);
+      }
+      bar_consumers();
+      if (misc[1]) {
+        __threadfence();
+        for (int it = tid; it < G * kChunks; it += kNW * 32) {
+          const int g = it / kChunks, cc = it % kChunks;
+          float M = -INFINITY;
+          bool any_bad = false;
+          for (long long cta = c_first; cta <= c_last; ++cta) {
+            const int sl = (w.S <= cta * chunk) ? 0 : 1;
+            const float ls = __ldcg(p.part_lse + (cta * 2 + sl) * 8 + g);
+            any_bad |= ls == INFINITY;
+            M = fmaxf(M, ls);
+          }
+          float lsum = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          if (!any_bad) {
+            for (long long cta = c_first; cta <= c_last; ++cta) {
+              const int sl = (w.S <= cta * chunk) ? 0 : 1;
+              const size_t ps = static_cast<size_t>(cta * 2 + sl) * 8 + g;
+              const float wt = ex2(__ldcg(p.part_lse + ps) - M);
+              lsum += wt;
+              const float4* src = reinterpret_cast<const float4*>(p.part_o + ps * D + cc * 8);
+              const float4 x = __ldcg(src), y = __ldcg(src + 1);
+              o[0] += x.x * wt; o[1] += x.y * wt; o[2] += x.z * wt; o[3] += x.w * wt;
+              o[4] += y.x * wt; o[5] += y.y * wt; o[6] += y.z * wt; o[7] += y.w * wt;
+            }
+          }
+          const size_t row = static_cast<size_t>(w.b) * p.num_q_heads + w.h * G + g;
+          uint4 pk = make_uint4(0, 0, 0, 0);
+          if (!any_bad) {
+            const float f = vsc / lsum;
+            pk = make_uint4(pack_bf16(o[0] * f, o[1] * f), pack_bf16(o[2] * f, o[3] * f),
+                            pack_bf16(o[4] * f, o[5] * f), pack_bf16(o[6] * f, o[7] * f));
+          }
+          reinterpret_cast<uint4*>(p.out + row * D)[cc] = pk;
+          if (cc == 0 && p.lse) p.lse[row] = any_bad ? -INFINITY : (M + log2f(lsum)) * kLn2;
+        }
+      }
+      bar_consumers();  // misc[1] is rewritten for the next unit
     }
-    reinterpret_cast<uint4*>(p.out + row * D)[c] = pk;
-    if (c == 0 && p.lse) p.lse[row] = any_bad ? -INFINITY : (M + log2f(lsum)) * kLn2;
   }
 }
 
@@ -493,21 +649,19 @@ pgqa_status_t launch_variant(const DecodeArgs& a, const DecodePlan& plan) {
   p.k_scale = a.k_scale;
   p.v_scale = a.v_scale;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  p.counters = plan.num_splits > 1 ? reinterpret_cast<int*>(ws + plan.counters_off) : nullptr;
-  p.ws_lse = plan.num_splits > 1 ? reinterpret_cast<float*>(ws + plan.lse_off) : nullptr;
-  p.ws_o = plan.num_splits > 1 ? reinterpret_cast<float*>(ws + plan.o_off) : nullptr;
+  p.counters = reinterpret_cast<int*>(ws + plan.counters_off);
+  p.part_lse = reinterpret_cast<float*>(ws + plan.lse_off);
+  p.part_o = reinterpret_cast<float*>(ws + plan.o_off);
   p.dev_status = a.dev_status;
   p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_seqs = a.num_seqs;
   p.num_q_heads = a.num_q_heads;
   p.num_kv_heads = a.num_kv_heads;
   p.group = a.num_q_heads / a.num_kv_heads;
   p.num_blocks = a.num_blocks;
   p.max_context_len = a.max_context_len;
-  p.pages_per_split = plan.pages_per_split;
-  p.num_splits = plan.num_splits;
   p.scale_log2 = a.scale * kLog2e;
-  dim3 grid(plan.num_splits, a.num_kv_heads, a.num_seqs);
-  paged_decode_kernel<D, kFp8><<<grid, kThreads, C::kSmem, a.stream>>>(kmap, vmap, p);
+  paged_decode_kernel<D, kFp8><<<plan.grid, kThreads, C::kSmem, a.stream>>>(kmap, vmap, p);
   return cudaPeekAtLastError() == cudaSuccess ? PGQA_OK : PGQA_ECUDA;
 }
 
@@ -515,30 +669,22 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 }  // namespace
 
-DecodePlan decode_plan(int num_seqs, int num_kv_heads, int head_dim, int max_context_len,
-                       int block_size, int num_sms) {
-  DecodePlan plan{1, 1, 0, 0, 0, 0};
-  const int max_pages = (max_context_len + block_size - 1) / block_size;
-  const long units = static_cast<long>(num_seqs) * num_kv_heads;
-  if (max_pages <= 0 || units <= 0) {
-    plan.pages_per_split = max_pages > 0 ? max_pages : 1;
-    return plan;
-  }
-  const long target = static_cast<long>(num_sms > 0 ? num_sms : 1) * kCtasPerSmTarget;
-  long splits = (target + units - 1) / units;
-  const long max_splits = (max_pages + kMinPagesPerSplit - 1) / kMinPagesPerSplit;
-  if (splits > max_splits) splits = max_splits;
-  if (splits < 1) splits = 1;
-  const int pps = static_cast<int>((max_pages + splits - 1) / splits);
-  plan.pages_per_split = pps;
-  plan.num_splits = (max_pages + pps - 1) / pps;
-  if (plan.num_splits > 1) {
-    const size_t n = static_cast<size_t>(units) * plan.num_splits * 8;
-    plan.counters_off = 0;
-    plan.lse_off = align256(static_cast<size_t>(units) * sizeof(int));
-    plan.o_off = plan.lse_off + align256(n * sizeof(float));
-    plan.bytes = plan.o_off + align256(n * head_dim * sizeof(float));
-  }
+int decode_ctas_per_sm(int head_dim, int cache_dtype) {
+  if (cache_dtype == PGQA_DTYPE_E4M3) return ctas_per_sm<128, true>();
+  return head_dim == 64 ? ctas_per_sm<64, false>() : ctas_per_sm<128, false>();
+}
+
+DecodePlan decode_plan(int num_seqs, int num_kv_heads, int head_dim, int cache_dtype,
+                       int num_sms) {
+  DecodePlan plan{};
+  plan.grid = (num_sms > 0 ? num_sms : 1) * decode_ctas_per_sm(head_dim, cache_dtype);
+  const size_t units = static_cast<size_t>(num_seqs > 0 ? num_seqs : 0) *
+                       static_cast<size_t>(num_kv_heads > 0 ? num_kv_heads : 0);
+  const size_t slots = static_cast<size_t>(plan.grid) * 2 * 8;
+  plan.counters_off = 0;
+  plan.lse_off = align256(units * sizeof(int));
+  plan.o_off = plan.lse_off + align256(slots * sizeof(float));
+  plan.bytes = plan.o_off + align256(slots * static_cast<size_t>(head_dim) * sizeof(float));
   return plan;
 }
 

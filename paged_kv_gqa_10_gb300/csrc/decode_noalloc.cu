@@ -64,13 +64,13 @@ extern "C" pgqa_status_t pgqa_paged_attention_decode_noalloc(
     return PGQA_EINVAL;
   size_t need = 0;
   size_t counter_bytes = 0;
-  if (num_seqs > 0 && max_context_len > 0) {
+  if (num_seqs > 0) {
     const int sms = pgqa::num_sms_current_device();
     if (sms <= 0) return PGQA_ECUDA;
     const pgqa::DecodePlan plan =
-        pgqa::decode_plan(num_seqs, num_kv_heads, head_dim, max_context_len, block_size, sms);
+        pgqa::decode_plan(num_seqs, num_kv_heads, head_dim, cache_dtype, sms);
     need = plan.bytes;
-    counter_bytes = plan.lse_off;  // the counters occupy [0, lse_off)
+    counter_bytes = plan.lse_off;  // the ticket counters occupy [0, lse_off)
   }
   if (need > PGQA_NOALLOC_SCRATCH_BYTES) return PGQA_ENOWORKSPACE;
   void* scratch = nullptr;

@@ -65,14 +65,16 @@ struct DecodeArgs {
   cudaStream_t stream;
 };
 
-// Split plan + workspace layout of paged decode.
+// Grid and workspace layout of paged decode: `grid` CTAs, each owning an equal
+// share of all pages; the workspace holds one ticket counter per (sequence,
+// kv-head) and two partial-result slots per CTA.
 struct DecodePlan {
-  int num_splits;
-  int pages_per_split;
+  int grid;
   size_t counters_off, lse_off, o_off, bytes;
 };
-DecodePlan decode_plan(int num_seqs, int num_kv_heads, int head_dim, int max_context_len,
-                       int block_size, int num_sms);
+int decode_ctas_per_sm(int head_dim, int cache_dtype);
+DecodePlan decode_plan(int num_seqs, int num_kv_heads, int head_dim, int cache_dtype,
+                       int num_sms);
 
 pgqa_status_t launch_paged_decode(const DecodeArgs& a, const DecodePlan& plan);
 

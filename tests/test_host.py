@@ -52,20 +52,17 @@ def test_kv_cache_bytes_matches_printed_figures():
     assert pgqa.kv_cache_bytes(-1, 1, 1, 1) == -1
 
 
-@pytest.mark.parametrize("B,Hkv,ctx", [(64, 8, 1024), (32, 8, 4096), (16, 8, 8192), (2, 2, 50),
-                                       (1, 1, 1), (512, 8, 128), (3, 1, 100000)])
 @pytest.mark.parametrize("sms", [1, 148, 152])
-def test_split_plan_covers_every_page(B, Hkv, ctx, sms):
-    n, pps = pgqa.decode_split_plan(B, Hkv, ctx, sms)
-    pages = -(-ctx // 16)
-    assert n >= 1 and pps >= 1
-    assert n * pps >= pages and (n - 1) * pps < pages       # no empty trailing split
-    assert n == 1 or pps >= 8                                # never below 128 tokens
+@pytest.mark.parametrize("D,dt", [(128, pgqa.BF16), (64, pgqa.BF16), (128, pgqa.E4M3)])
+def test_decode_grid_fills_every_sm(sms, D, dt):
+    g = pgqa.decode_grid_size(sms, D, dt)
+    assert g >= sms and g % sms == 0          # the same number of CTAs on every SM
 
 
-def test_split_plan_rejects_bad_arguments():
-    with pytest.raises(pgqa.PgqaError):
-        pgqa.decode_split_plan(1, 0, 10, 152)
+def test_decode_grid_rejects_bad_arguments():
+    for args in ((0, 128, pgqa.BF16), (152, 96, pgqa.BF16), (152, 128, 9)):
+        with pytest.raises(pgqa.PgqaError):
+            pgqa.decode_grid_size(*args)
 
 
 def _call_decode(**over):

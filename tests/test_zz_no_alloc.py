@@ -61,20 +61,19 @@ def test_noalloc_matches_workspace_entry_point_twice(cache_dtype):
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
-    # grow the batch until the split-K workspace exceeds the fixed array; the
-    # tensors are valid (zeroed cache, in-range block ids) so that even a launch
-    # would be safe, but none must happen
-    ctx, Hq, Hkv, D = 256, 32, 8, 128
-    B = 8
-    while pgqa.decode_workspace_size(B, Hq, Hkv, D, ctx) <= pgqa.NOALLOC_SCRATCH_BYTES:
-        B += 8
-        assert B < 1 << 16
-    nb = ctx // 16
-    kc = torch.zeros((B * nb, Hkv, 16, D), dtype=torch.bfloat16, device="cuda")
-    bt = torch.arange(B * nb, dtype=torch.int32, device="cuda").view(B, nb)
-    inp = workloads.DecodeInputs(q=torch.zeros((B, Hq, D), dtype=torch.bfloat16), k_cache=kc,
-                                 v_cache=kc, block_tables=bt,
-                                 context_lens=torch.full((B,), ctx, dtype=torch.int32),
+    # grow the batch until the workspace (one ticket per (sequence, kv-head) plus the
+    # partial slots) exceeds the fixed array; the inputs are valid -- empty contexts,
+    # so a launch would only write zeros -- but no launch must happen
+    Hq, Hkv, D = 8, 8, 64
+    B = 1 << 14
+    while pgqa.decode_workspace_size(B, Hq, Hkv, D, 16) <= pgqa.NOALLOC_SCRATCH_BYTES:
+        B *= 2
+        assert B < 1 << 22
+    kc = torch.zeros((1, Hkv, 16, D), dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros((B, 1), dtype=torch.int32, device="cuda")
+    inp = workloads.DecodeInputs(q=torch.zeros((B, Hq, D), dtype=torch.bfloat16, device="cuda"),
+                                 k_cache=kc, v_cache=kc, block_tables=bt,
+                                 context_lens=torch.zeros((B,), dtype=torch.int32, device="cuda"),
                                  scale=0.1)
     run = DecodeRun(inp)
     rc, out, _ = _noalloc(run)
