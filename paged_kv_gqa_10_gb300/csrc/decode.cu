@@ -19,10 +19,14 @@
 //    cut, so each CTA owns two partial slots.
 //  - Warp roles: one producer warp streams pages with TMA (2-D tensor map over the
 //    cache viewed as [num_blocks*Hkv*16 rows][head_dim], 128-byte swizzle) into
-//    mbarrier-guarded stages and stages each unit's G query rows into a double
-//    buffer with a bulk copy; 4 consumer warps take pages round-robin. Each consumer
+//    mbarrier-guarded stages; 4 consumer warps take pages round-robin. Each consumer
 //    warp owns its own sub-ring of stages, so consecutive uses of a stage belong to
-//    one warp and a parity wait can never be two phases behind.
+//    one warp and a parity wait can never be two phases behind. The producer reads
+//    the block table up to 256 pages ahead (coalesced, into a shared ring of row
+//    coordinates) and refills each consumer warp's stages as soon as that warp frees
+//    one (non-blocking polls), so a slow warp never holds back the others' loads.
+//    Consumers read each unit's query rows straight from global memory, one unit
+//    ahead.
 //  - Math per 16-token page on the warp-level tensor path (mma.m16n8k16):
 //      S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8]   (tokens fill M = 16)
 //      online softmax on the S^T fragment (column = query head)
@@ -48,6 +52,8 @@ namespace {
 constexpr int kNW = 4;  // consumer warps per CTA
 constexpr int kThreads = (kNW + 1) * 32;
 constexpr int kMinChunk = 8;  // pages per CTA range, at least
+constexpr int kYRing = 256;   // TMA row coordinates fetched ahead of issue
+constexpr int kScanSlots = kThreads / 32 + 1;  // one per warp, then the found unit start
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -81,15 +87,14 @@ struct Cfg {
   static constexpr int kStages = kNW * kStagesPerWarp;
   static constexpr int kNkc = D / 16;              // 16-wide chunks of head_dim
   static constexpr int kRing = kStages * kStageBytes;
-  static constexpr int kQBuf = 8 * D * 2;          // up to 8 bf16 query rows
   static constexpr int kMerge = kNW * 8 * D * 4;   // per-warp O of one unit
-  static constexpr int kOffQ = kRing;
-  static constexpr int kOffMerge = kOffQ + 2 * kQBuf;
+  static constexpr int kOffMerge = kRing;
   static constexpr int kOffMl = kOffMerge + kMerge;                   // [kNW][8][2] float
-  static constexpr int kOffBar = kOffMl + kNW * 8 * 2 * 4;            // full, empty, q_full, q_empty
-  static constexpr int kOffMeta = kOffBar + (2 * kStages + 4) * 8;    // [S] int
-  static constexpr int kOffMisc = kOffMeta + kStages * 4;             // 32 ints + 8 int64
-  static constexpr int kSmem = 1024 + kOffMisc + 32 * 4 + 8 * 8;
+  static constexpr int kOffBar = kOffMl + kNW * 8 * 2 * 4;            // full[S], empty[S]
+  static constexpr int kOffMeta = kOffBar + 2 * kStages * 8;          // [S] int
+  static constexpr int kOffY = kOffMeta + kStages * 4;                // [kYRing] int
+  static constexpr int kOffMisc = kOffY + kYRing * 4;                 // 32 ints, kScanSlots int64
+  static constexpr int kSmem = 1024 + kOffMisc + 32 * 4 + kScanSlots * 8;
   static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle rows");
 };
 
@@ -174,16 +179,14 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* ring = smem;
-  uint8_t* qbuf = smem + C::kOffQ;
   float* wo = reinterpret_cast<float*>(smem + C::kOffMerge);  // [kNW][8][D]
   float* wml = reinterpret_cast<float*>(smem + C::kOffMl);    // [kNW][8][2] (m, l) base 2
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* empty = full + S;
-  uint64_t* q_full = empty + S;    // [2]
-  uint64_t* q_empty = q_full + 2;  // [2]
   int* meta = reinterpret_cast<int*>(smem + C::kOffMeta);  // per stage: bad block id seen
+  int* yring = reinterpret_cast<int*>(smem + C::kOffY);    // row coordinate of page i % kYRing
   int* misc = reinterpret_cast<int*>(smem + C::kOffMisc);
-  long long* scratch = reinterpret_cast<long long*>(misc + 32);  // 8 slots
+  long long* scratch = reinterpret_cast<long long*>(misc + 32);  // kScanSlots slots
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, ncta = gridDim.x;
@@ -223,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
     const long long s0 = static_cast<long long>(Hkv) * (running + incl - P);
     if (P > 0 && s0 <= r0 && r0 < s0 + Hkv * P) {
       misc[0] = b;
-      scratch[6] = s0;
+      scratch[kScanSlots - 1] = s0;
     }
     running += tot;
     __syncthreads();
@@ -232,17 +235,13 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
   Walk w0;
   w0.b = misc[0];
   w0.P = pages_of(p, w0.b);
-  w0.h = static_cast<int>((r0 - scratch[6]) / w0.P);
-  w0.S = scratch[6] + static_cast<long long>(w0.h) * w0.P;
+  w0.h = static_cast<int>((r0 - scratch[kScanSlots - 1]) / w0.P);
+  w0.S = scratch[kScanSlots - 1] + static_cast<long long>(w0.h) * w0.P;
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&q_full[s], 1);
-      mbar_init(&q_empty[s], kNW);
     }
     fence_mbar_init();
   }
@@ -254,80 +253,80 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
     }
-    bool ok = true;
-    int issued = 0, units = 0;
-    for (Walk w = w0; w.S < r1 && ok; w.next(p), ++units) {
-      const int seg0 = static_cast<int>((r0 > w.S ? r0 : w.S) - w.S);
-      const int seg1 = static_cast<int>((r1 < w.S + w.P ? r1 : w.S + w.P) - w.S);
-      // this unit's G query rows -> q buffer (units & 1)
-      if (lane == 0) {
-        const int qs = units & 1;
-        if (units >= 2 && !mbar_wait(&q_empty[qs], ((units >> 1) - 1) & 1)) {
-          record_status(p.dev_status, PGQA_ETIMEOUT);
-          ok = false;
-        } else {
-          const uint32_t bytes = static_cast<uint32_t>(G * D * 2);
-          mbar_arrive_expect_tx(&q_full[qs], bytes);
-          bulk_load(qbuf + qs * C::kQBuf,
-                    p.q + (static_cast<size_t>(w.b) * p.num_q_heads + w.h * G) * D, bytes,
-                    &q_full[qs]);
+    const int n = static_cast<int>(r1 - r0);  // pages of this CTA, CTA-local index 0..n-1
+    Walk fw = w0;                             // fetch cursor: unit and page within it
+    int fpg = static_cast<int>(r0 - w0.S);
+    int fetched = 0;  // pages whose row coordinate is in yring
+    // lane w < kNW serves consumer warp w: its pages are w, w + kNW, ...
+    const int nw_pages = lane < kNW && n > lane ? (n - lane + kNW - 1) / kNW : 0;
+    int next_li = 0;  // next local index of that warp to issue
+    uint64_t idle_since = 0;
+    for (;;) {
+      const int pend = __reduce_min_sync(
+          0xffffffffu, lane < kNW && next_li < nw_pages ? lane + kNW * next_li : INT_MAX);
+      if (pend == INT_MAX) break;  // every page issued
+      bool progress = false;
+      // fetch up to 32 row coordinates of the current unit, never overwriting an
+      // entry that is still to be issued
+      if (fetched < n && fetched < pend + kYRing - 32) {
+        const int cnt = min(32, min(fw.P - fpg, n - fetched));
+        if (lane < cnt) {
+          const int32_t pbn =
+              __ldg(p.block_tables + static_cast<size_t>(fw.b) * p.max_blocks_per_seq + fpg + lane);
+          yring[(fetched + lane) % kYRing] =
+              (pbn < 0 || pbn >= p.num_blocks) ? -1 : (pbn * Hkv + fw.h) * 16;
+        }
+        fetched += cnt;
+        fpg += cnt;
+        if (fpg == fw.P) {
+          fw.next(p);
+          fpg = 0;
+        }
+        __syncwarp();
+        progress = true;
+      }
+      // refill consumer warp `lane`'s next stage if it is free
+      if (lane < kNW && next_li < nw_pages) {
+        const int i = lane + kNW * next_li;
+        const int s = lane * SPW + next_li % SPW, use = next_li / SPW;
+        if (i < fetched && (use == 0 || mbar_try_wait(&empty[s], (use - 1) & 1))) {
+          int y = yring[i % kYRing];
+          int bad = 0;
+          if (y < 0) {
+            bad = 1;
+            y = 0;  // load a valid page; the unit's result is discarded
+            record_status(p.dev_status, PGQA_EBADINDEX);
+          }
+          meta[s] = bad;
+          uint8_t* st = ring + s * C::kStageBytes;
+          mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+#pragma unroll
+          for (int sub = 0; sub < C::kSub; ++sub)
+            tma_load_2d(st + sub * 2048, &kmap, &full[s], sub * (128 / C::kElem), y);
+#pragma unroll
+          for (int sub = 0; sub < C::kSub; ++sub)
+            tma_load_2d(st + C::kPageBytes + sub * 2048, &vmap, &full[s],
+                        sub * (128 / C::kElem), y);
+          ++next_li;
+          progress = true;
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      const int32_t* bt = p.block_tables + static_cast<size_t>(w.b) * p.max_blocks_per_seq;
-      for (int base = seg0; base < seg1 && ok; base += 32) {
-        const int32_t mine = base + lane < seg1 ? __ldg(bt + base + lane) : 0;
-        const int n = min(32, seg1 - base);
-        for (int k = 0; k < n; ++k) {
-          int32_t pbn = __shfl_sync(0xffffffffu, mine, k);
-          if (lane == 0) {
-            const int i = issued;  // CTA-local page index
-            const int li = i / kNW;
-            const int s = (i % kNW) * SPW + li % SPW;
-            const int use = li / SPW;
-            if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
-              record_status(p.dev_status, PGQA_ETIMEOUT);
-              ok = false;
-            } else {
-              int bad = 0;
-              if (pbn < 0 || pbn >= p.num_blocks) {
-                bad = 1;
-                pbn = 0;  // load a valid page; the unit's result is discarded
-                record_status(p.dev_status, PGQA_EBADINDEX);
-              }
-              meta[s] = bad;
-              uint8_t* st = ring + s * C::kStageBytes;
-              mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-              const int y = (pbn * Hkv + w.h) * 16;
-#pragma unroll
-              for (int sub = 0; sub < C::kSub; ++sub)
-                tma_load_2d(st + sub * 2048, &kmap, &full[s], sub * (128 / C::kElem), y);
-#pragma unroll
-              for (int sub = 0; sub < C::kSub; ++sub)
-                tma_load_2d(st + C::kPageBytes + sub * 2048, &vmap, &full[s],
-                            sub * (128 / C::kElem), y);
-              ++issued;
-            }
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-        }
+      if (__any_sync(0xffffffffu, progress)) {
+        idle_since = 0;
+      } else if (idle_since == 0) {
+        idle_since = globaltimer_ns();
+      } else if (globaltimer_ns() - idle_since > kWaitLimitNs) {
+        if (lane == 0) record_status(p.dev_status, PGQA_ETIMEOUT);
+        break;
       }
     }
-    // No bulk or TMA write may land after this CTA exits: wait for the last fill of
-    // every stage and of both q buffers (complete already on the normal path).
-    if (lane == 0) {
-      for (int w = 0; w < kNW; ++w) {
-        const int n_w = issued > w ? (issued - w + kNW - 1) / kNW : 0;
-        for (int k = 0; k < SPW && k < n_w; ++k) {
-          const int last_li = k + ((n_w - 1 - k) / SPW) * SPW;
-          if (!mbar_wait(&full[w * SPW + k], (last_li / SPW) & 1))
-            record_status(p.dev_status, PGQA_ETIMEOUT);
-        }
-      }
-      for (int qs = 0; qs < 2 && qs < units; ++qs) {
-        const int last = qs + ((units - 1 - qs) / 2) * 2;
-        if (!mbar_wait(&q_full[qs], (last >> 1) & 1)) record_status(p.dev_status, PGQA_ETIMEOUT);
+    // No TMA write may land after this CTA exits: wait for the last fill of each
+    // stage (complete already on the normal path).
+    if (lane < kNW) {
+      for (int k = 0; k < SPW && k < next_li; ++k) {
+        const int last_li = k + ((next_li - 1 - k) / SPW) * SPW;
+        if (!mbar_wait(&full[lane * SPW + k], (last_li / SPW) & 1))
+          record_status(p.dev_status, PGQA_ETIMEOUT);
       }
     }
     return;
@@ -341,41 +340,52 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
   const uint32_t cV = (lane >> 3) & 1;
   bool alive = true;  // false once one of this warp's waits gave up
   int i_base = 0;     // CTA-local index of the unit's first page
-  int units = 0;
-  for (Walk w = w0; w.S < r1; w.next(p), ++units) {
+  // raw query words of a unit, column n = query head gid of the group:
+  //   bf16: the two B-fragment registers per 16-wide chunk as stored;
+  //   E4M3: k index 2tig+{0,1} <-> d = 16kc + 4tig + {0,1}; 2tig+8+{0,1} <-> +{2,3}
+  uint32_t qraw[C::kNkc][2];
+  auto load_q = [&](const Walk& u) {
+    const bool live = gid < G;
+    const __nv_bfloat16* qrow =
+        p.q + (static_cast<size_t>(u.b) * p.num_q_heads + u.h * G + (live ? gid : 0)) * D;
+#pragma unroll
+    for (int kc = 0; kc < C::kNkc; ++kc) {
+      if constexpr (!kFp8) {
+        const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow + 16 * kc + 2 * tig);
+        qraw[kc][0] = live ? __ldg(q32) : 0u;
+        qraw[kc][1] = live ? __ldg(q32 + 4) : 0u;
+      } else {
+        const uint2 q4 = live ? __ldg(reinterpret_cast<const uint2*>(qrow + 16 * kc + 4 * tig))
+                              : make_uint2(0, 0);
+        qraw[kc][0] = q4.x;
+        qraw[kc][1] = q4.y;
+      }
+    }
+  };
+  load_q(w0);
+  for (Walk w = w0; w.S < r1; w.next(p)) {
     const int seg0 = static_cast<int>((r0 > w.S ? r0 : w.S) - w.S);
     const int seg1 = static_cast<int>((r1 < w.S + w.P ? r1 : w.S + w.P) - w.S);
     const int npg = seg1 - seg0;
     const int L = __ldg(p.context_lens + w.b);
-    const int qs = units & 1;
 
-    // Q^T fragments (B operand, column n = query head gid) from the staged rows
+    // Q^T fragments (B operand) of this unit, then start loading the next unit's
     uint32_t qf[C::kNkc][2];
-    if (alive && !mbar_wait(&q_full[qs], (units >> 1) & 1)) {
-      alive = false;
-      record_status(p.dev_status, PGQA_ETIMEOUT);
-    }
-    {
-      const bool live = gid < G && alive;
-      const __nv_bfloat16* qrow =
-          reinterpret_cast<const __nv_bfloat16*>(qbuf + qs * C::kQBuf) + (live ? gid : 0) * D;
 #pragma unroll
-      for (int kc = 0; kc < C::kNkc; ++kc) {
-        if constexpr (!kFp8) {
-          const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow + 16 * kc + 2 * tig);
-          qf[kc][0] = live ? q32[0] : 0u;
-          qf[kc][1] = live ? q32[4] : 0u;
-        } else {
-          // k index 2tig+{0,1} <-> d = 16kc + 4tig + {0,1}; 2tig+8+{0,1} <-> +{2,3}
-          const uint2 q4 =
-              live ? *reinterpret_cast<const uint2*>(qrow + 16 * kc + 4 * tig) : make_uint2(0, 0);
-          qf[kc][0] = pack_f16(bf16_lo(q4.x), bf16_hi(q4.x));
-          qf[kc][1] = pack_f16(bf16_lo(q4.y), bf16_hi(q4.y));
-        }
+    for (int kc = 0; kc < C::kNkc; ++kc) {
+      if constexpr (!kFp8) {
+        qf[kc][0] = qraw[kc][0];
+        qf[kc][1] = qraw[kc][1];
+      } else {
+        qf[kc][0] = pack_f16(bf16_lo(qraw[kc][0]), bf16_hi(qraw[kc][0]));
+        qf[kc][1] = pack_f16(bf16_lo(qraw[kc][1]), bf16_hi(qraw[kc][1]));
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&q_empty[qs]);
+    {
+      Walk wn = w;
+      wn.next(p);
+      if (wn.S < r1) load_q(wn);
+    }
 
     const float sl2 = p.scale_log2 * (kFp8 ? __ldg(p.k_scale + w.h) : 1.f);
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
