@@ -367,6 +367,8 @@ def measure_prefill(args, dev):
     out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.zeros(pgqa.prefill_workspace_size(inp.num_seqs, Hq, inp.max_seqlen),
+                     dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def write():
@@ -374,7 +376,7 @@ def measure_prefill(args, dev):
 
     def prefill():
         pgqa.paged_prefill_varlen(out, lse, q, kc, vc, bt, cu, inp.max_seqlen, inp.scale,
-                                  dev_status=status)
+                                  workspace=ws, dev_status=status)
 
     for _ in range(args.warmup):
         write()

@@ -222,7 +222,8 @@ pgqa_status_t pgqa_paged_attention_decode_noalloc(void* out, float* lse, const v
                                                   const float* v_scale, int max_context_len,
                                                   int* dev_status, void* stream);
 
-/* Workspace bytes pgqa_paged_prefill_varlen needs (currently 0). */
+/* Workspace bytes pgqa_paged_prefill_varlen needs (256: the ticket counters the
+ * CTAs take work items with). */
 size_t pgqa_prefill_workspace_size(int num_seqs, int num_q_heads, int max_seqlen);
 
 /*
@@ -238,9 +239,14 @@ size_t pgqa_prefill_workspace_size(int num_seqs, int num_q_heads, int max_seqlen
  *   cu_seqlens    [num_seqs + 1] int32, read: sequence i owns tokens
  *                 cu_seqlens[i] .. cu_seqlens[i+1]-1; the token at position p
  *                 of sequence i attends to keys 0..p of sequence i.
- *   max_seqlen    an upper bound on the sequence lengths (sizes the grid).
+ *   max_seqlen    an upper bound on the sequence lengths (at most 524288).
  *   block_tables  [num_seqs][max_blocks_per_seq] int32, read.
- *   workspace     may be NULL while pgqa_prefill_workspace_size() is 0.
+ *   num_seqs      at most 4096.
+ *   scale         must be > 0.
+ *   workspace     device scratch of at least pgqa_prefill_workspace_size()
+ *                 bytes, 16-byte aligned, ZERO-FILLED before its first use; every
+ *                 call that completes leaves it zero. Calls sharing a workspace
+ *                 must not overlap in time.
  * bf16 cache only; q/out/k_cache/v_cache 16-byte aligned. Inconsistent
  * cu_seqlens (negative lengths, a length above max_seqlen or beyond the block
  * table, a last entry other than num_tokens) are a device error (PGQA_EINVAL in

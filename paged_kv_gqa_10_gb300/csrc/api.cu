@@ -332,7 +332,7 @@ size_t pgqa_prefill_workspace_size(int num_seqs, int num_q_heads, int max_seqlen
   (void)num_seqs;
   (void)num_q_heads;
   (void)max_seqlen;
-  return 0;
+  return pgqa::kPrefillWorkspaceBytes;
 }
 
 pgqa_status_t pgqa_paged_prefill_varlen(void* out, float* lse, const void* q, int num_tokens,
@@ -343,18 +343,20 @@ pgqa_status_t pgqa_paged_prefill_varlen(void* out, float* lse, const void* q, in
                                         int num_blocks, int block_size, float scale,
                                         void* workspace, size_t workspace_bytes,
                                         int* dev_status, void* stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   if (num_seqs < 0 || max_seqlen < 0 || num_tokens < 0 || num_q_heads <= 0 ||
       num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || block_size <= 0 ||
-      max_blocks_per_seq < 0 || !isfinite(scale))
+      max_blocks_per_seq < 0 || !isfinite(scale) || !(scale > 0.f))
     return PGQA_EINVAL;
   if (num_q_heads % num_kv_heads != 0) return PGQA_EINVAL;
   if (head_dim != 128 && head_dim != 64) return PGQA_EUNSUPPORTED;
   if (block_size != 16) return PGQA_EUNSUPPORTED;
   if (static_cast<int64_t>(num_blocks) * num_kv_heads * 16 > INT32_MAX) return PGQA_EUNSUPPORTED;
+  if (num_seqs > pgqa::prefill_max_seqs() || max_seqlen > pgqa::prefill_max_seqlen())
+    return PGQA_EUNSUPPORTED;
   if (num_seqs == 0 || max_seqlen == 0 || num_tokens == 0) return PGQA_OK;
-  if (num_seqs > 65535 * 64 || (max_seqlen + 127) / 128 > 65535) return PGQA_EUNSUPPORTED;
+  if (workspace == nullptr || workspace_bytes < pgqa::kPrefillWorkspaceBytes)
+    return PGQA_ENOWORKSPACE;
+  if (!aligned(workspace, 16)) return PGQA_EINVAL;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !cu_seqlens) return PGQA_EINVAL;
   if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
     return PGQA_EINVAL;
@@ -367,6 +369,7 @@ pgqa_status_t pgqa_paged_prefill_varlen(void* out, float* lse, const void* q, in
   a.block_tables = block_tables;
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.cu_seqlens = cu_seqlens;
+  a.workspace = workspace;
   a.num_tokens = num_tokens;
   a.num_seqs = num_seqs;
   a.max_seqlen = max_seqlen;

@@ -87,6 +87,7 @@ struct PrefillArgs {
   const int32_t* block_tables;
   int max_blocks_per_seq;
   const int32_t* cu_seqlens;
+  void* workspace;  // >= prefill_workspace_bytes(), zero before first use
   int num_tokens;
   int num_seqs, max_seqlen, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size;
   float scale;
@@ -95,5 +96,8 @@ struct PrefillArgs {
 };
 
 pgqa_status_t launch_paged_prefill(const PrefillArgs& a);
+constexpr size_t kPrefillWorkspaceBytes = 256;  // two ticket counters
+int prefill_max_seqs();    // sequences per prefill call
+int prefill_max_seqlen();  // tokens of the longest sequence
 
 }  // namespace pgqa

@@ -30,6 +30,8 @@ class PrefillRun:
         self.out = torch.full((T, Hq, D), 5.0, dtype=torch.bfloat16, device="cuda")
         self.lse = torch.full((T, Hq), 5.0, dtype=torch.float32, device="cuda")
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.ws = torch.zeros(pgqa.prefill_workspace_size(inp.num_seqs, Hq, inp.max_seqlen),
+                              dtype=torch.uint8, device="cuda")
         self.max_seqlen = max_seqlen if max_seqlen is not None else inp.max_seqlen
 
     def write(self):
@@ -38,7 +40,8 @@ class PrefillRun:
 
     def prefill(self):
         pgqa.paged_prefill_varlen(self.out, self.lse, self.q, self.kc, self.vc, self.bt, self.cu,
-                                  self.max_seqlen, self.inp.scale, dev_status=self.status)
+                                  self.max_seqlen, self.inp.scale, workspace=self.ws,
+                                  dev_status=self.status)
 
     def status_code(self):
         torch.cuda.synchronize()
@@ -143,6 +146,23 @@ def test_ragged_lengths_full_compare(G, D):
 def test_one_long_sequence_full_compare():
     run, ref_out, ref_lse = _full_case([1000], 4, 1, 128, seed=50)
     assert_attention_close(run.out, run.lse, ref_out, ref_lse)
+
+
+def test_repeat_calls_reuse_the_workspace():
+    """The ticket counters are left zero: a second call on the same workspace gives
+    the same bits, and the workspace ends zero."""
+    lens = [700, 3, 129, 400, 256]
+    inp = workloads.make_prefill(lens, 8, 2, 128, 128, seed=65)
+    run = PrefillRun(inp)
+    run.write()
+    run.prefill()
+    assert run.status_code() == 0
+    out1, lse1 = run.out.clone(), run.lse.clone()
+    run.out.fill_(7.0)
+    run.prefill()
+    assert run.status_code() == 0
+    assert torch.equal(run.out, out1) and torch.equal(run.lse, lse1)
+    assert not torch.any(run.ws)
 
 
 def test_max_seqlen_upper_bound_is_enough():

@@ -112,3 +112,8 @@ def test_prefill_argument_validation():
     assert f(*args[:11], 7, *args[12:]) == pgqa.EINVAL
     assert f(*args[:9], 0, *args[10:]) == pgqa.OK
     assert f(*args[:3], -1, *args[4:]) == pgqa.EINVAL
+    assert f(*args[:16], -0.1, *args[17:]) == pgqa.EINVAL          # scale must be > 0
+    assert f(*args[:9], 5000, *args[10:]) == pgqa.EUNSUPPORTED     # more than 4096 sequences
+    assert f(*args) == pgqa.ENOWORKSPACE                           # no workspace given
+    assert f(*args[:10], 600000, *args[11:]) == pgqa.EUNSUPPORTED  # longer than 524288 tokens
+    assert pgqa.prefill_workspace_size(2, 8, 64) == 256
