@@ -222,8 +222,8 @@ pgqa_status_t pgqa_paged_attention_decode_noalloc(void* out, float* lse, const v
                                                   const float* v_scale, int max_context_len,
                                                   int* dev_status, void* stream);
 
-/* Workspace bytes pgqa_paged_prefill_varlen needs (256: the ticket counters the
- * CTAs take work items with). */
+/* Workspace bytes pgqa_paged_prefill_varlen needs (33024: the ticket counters the
+ * CTAs take work items with, and the longest-first item tables each call rebuilds). */
 size_t pgqa_prefill_workspace_size(int num_seqs, int num_q_heads, int max_seqlen);
 
 /*
@@ -244,9 +244,9 @@ size_t pgqa_prefill_workspace_size(int num_seqs, int num_q_heads, int max_seqlen
  *   num_seqs      at most 4096.
  *   scale         must be > 0.
  *   workspace     device scratch of at least pgqa_prefill_workspace_size()
- *                 bytes, 16-byte aligned, ZERO-FILLED before its first use; every
- *                 call that completes leaves it zero. Calls sharing a workspace
- *                 must not overlap in time.
+ *                 bytes, 16-byte aligned; its first 256 bytes ZERO-FILLED before
+ *                 its first use (every call that completes leaves them zero).
+ *                 Calls sharing a workspace must not overlap in time.
  * bf16 cache only; q/out/k_cache/v_cache 16-byte aligned. Inconsistent
  * cu_seqlens (negative lengths, a length above max_seqlen or beyond the block
  * table, a last entry other than num_tokens) are a device error (PGQA_EINVAL in

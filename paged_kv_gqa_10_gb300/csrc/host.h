@@ -96,7 +96,9 @@ struct PrefillArgs {
 };
 
 pgqa_status_t launch_paged_prefill(const PrefillArgs& a);
-constexpr size_t kPrefillWorkspaceBytes = 256;  // two ticket counters
+// ticket counters (256 B) + the item tables (sorted sequences, per-level counts
+// and offsets) of up to 4096 sequences and 2048 tile pairs
+constexpr size_t kPrefillWorkspaceBytes = 256 + (4096 + 2 * 2048) * 4;
 int prefill_max_seqs();    // sequences per prefill call
 int prefill_max_seqlen();  // tokens of the longest sequence
 

@@ -16,23 +16,28 @@
 //  - Every CTA builds the same dense list of the batch's items, longest first:
 //    items of pair index m (descending), then sequences ordered by their number of
 //    tile pairs (a stable counting sort in shared memory), then heads (so the heads
-//    sharing a kv-head run side by side and share K/V in L2). A persistent grid (one
-//    CTA per SM) takes items from this list with an atomic ticket counter, so the
-//    load balances itself whatever the length mix; the last CTA to finish resets the
+//    sharing a kv-head run side by side and share K/V in L2). The tables go to the
+//    workspace (every CTA writes the same values). A persistent grid (one CTA per
+//    SM) takes items from the list with an atomic ticket counter, so the load
+//    balances itself whatever the length mix; the last CTA to finish resets the
 //    counter for the next call.
-// Warp roles
-//  - warp 8 (TMA): takes tickets (one ahead), checks the item's block ids, loads
-//    Q_A and Q_B once, then for each key tile K and V (one stage each), each gathered
-//    as 8 pages of 16 rows with 2-D tensor-map loads (128-byte swizzle). Pages past
-//    the sequence end are loaded from past the end of the cache view, which TMA
-//    fills with zeros.
+// Warp roles (12 warps; warps 10-11 only wait: at 384 threads the register
+// allocator fits the softmax in 167 registers without spilling)
+//  - warp 8 (TMA): publishes each item with its Q_A and Q_B, then streams K_0, K_1,
+//    V_0, K_2, V_1, ... (K one tile ahead, the order the MMA needs them) through a
+//    3-stage ring, each tile gathered as 8 pages of 16 rows with 2-D tensor-map loads
+//    (128-byte swizzle). Block ids are read 32 pages at a time, one chunk ahead, and
+//    the next item (ticket, decode, block-id check, first pages) is planned while the
+//    ring is full, so no load waits on a table read. Pages past the sequence end are
+//    loaded from past the end of the cache view, which TMA fills with zeros.
 //  - warp 9 (MMA, one thread): tcgen05.mma, M = N = 128, f32 accumulators in TMEM:
-//    S_X = Q_X K^T for X = A, B and O_X += P_X V (V MN-major). The tile pair
-//    ping-pongs: while one tile's softmax runs, the tensor core computes the other
-//    tile's S and PV.
-//  - warps 0-3 / 4-7 (softmax of tile A / B; thread = query row = TMEM lane): two
-//    passes over the row's scores in TMEM (max, then exp2; 64 columns per load), the
-//    causal mask applied on the diagonal tile only, P = 2^(s - m) as bf16 into
+//    S_X = Q_X K^T for X = A, B and O_X += P_X V (V MN-major). S_X of the next key
+//    tile is computed as soon as the softmax has read S_X into registers, so it runs
+//    under that softmax; the tile pair ping-pongs, the tensor core working on one
+//    tile while the other's softmax runs.
+//  - warps 0-3 / 4-7 (softmax of tile A / B; thread = query row = TMEM lane): one
+//    load of the row's 128 scores from TMEM, the causal mask on the diagonal tile
+//    only, the row max and sum over independent chains, P = 2^(s - m) as bf16 into
 //    shared memory in the MMA's swizzled layout, O rescaled in TMEM only when the
 //    running max grows by more than 2^8 (exact either way: P and l use the same
 //    reference max); at the end O / l -> bf16 out and lse.
@@ -48,29 +53,35 @@ namespace {
 
 constexpr int kBlockM = 128;  // query rows per tile
 constexpr int kBlockN = 128;  // keys per tile
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kStages = 3;           // K/V ring
 constexpr uint32_t kTmemCols = 512;  // S_A 0, S_B 128, O_A 256, O_B 384
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 constexpr int kMaxSeqs = 4096;            // sequences per call
 constexpr int kMaxLevels = 2048;          // tile pairs of the longest sequence
+static_assert(256 + (kMaxSeqs + 2 * kMaxLevels) * 4 == kPrefillWorkspaceBytes,
+              "workspace layout");
 
 template <int D>
 struct PCfg {
   static constexpr int kSub = D / 64;        // 128-byte (64-element) column blocks
   static constexpr int kTile = 128 * D * 2;  // [128 rows][D] bf16
   static constexpr int kQ = 0;               // Q_A, Q_B
-  static constexpr int kK = 2 * kTile;       // K
-  static constexpr int kV = 3 * kTile;       // V
-  static constexpr int kP = 4 * kTile;       // P_A, P_B: [128 rows][128 keys] bf16 each
-  static constexpr int kSeq = kP + 2 * 128 * 128 * 2;       // int [kMaxSeqs]: sorted sequences
-  static constexpr int kLvlCnt = kSeq + kMaxSeqs * 4;       // int [kMaxLevels]: seqs with > m pairs
-  static constexpr int kLvlOff = kLvlCnt + kMaxLevels * 4;  // int [kMaxLevels]: items before m
-  static constexpr int kBar = kLvlOff + kMaxLevels * 4;
+  static constexpr int kRing = 2 * kTile;    // kStages K/V tiles, in load order
+  static constexpr int kP = kRing + kStages * kTile;  // P_A, P_B: [128][128] bf16 each
+  static constexpr int kBar = kP + 2 * 128 * 128 * 2;
   static constexpr int kSmem = 1024 + kBar + 256;
 };
+
+// Scratch in the P area while the tables are built (before any P is written).
+constexpr int kScrHist = 0;                            // int [kMaxLevels]
+constexpr int kScrSorted = kScrHist + kMaxLevels * 4;  // int [kMaxSeqs]
+constexpr int kScrCnt = kScrSorted + kMaxSeqs * 4;     // int [kMaxLevels]
+constexpr int kScrOff = kScrCnt + kMaxLevels * 4;      // int [kMaxLevels]
+static_assert(kScrOff + kMaxLevels * 4 <= 2 * 128 * 128 * 2, "table scratch");
 
 struct PrefillParams {
   __nv_bfloat16* out;
@@ -78,7 +89,8 @@ struct PrefillParams {
   const int32_t* cu_seqlens;
   const int32_t* block_tables;
   int* dev_status;
-  int* ticket;  // [2] workspace: next ticket, finished CTAs (zero between calls)
+  int* ticket;  // workspace: [0] next ticket, [1] finished CTAs (zero between calls)
+  int* tables;  // workspace + 256 B: sorted [kMaxSeqs], lvl_cnt, lvl_off [kMaxLevels]
   int max_blocks_per_seq;
   int num_seqs, num_tokens, max_seqlen;
   int num_q_heads, num_kv_heads, group;
@@ -103,19 +115,22 @@ __device__ __forceinline__ int pairs_of(const PrefillParams& p, int s) {
   return ((L + kBlockM - 1) / kBlockM + 1) / 2;
 }
 
-// One work item: a pair of query tiles of one (sequence, head).
+// One work item: a pair of query tiles of one (sequence, head), as the TMA warp
+// publishes it to the other roles (8 ints per slot). ticket < 0: end of the list.
 struct Item {
-  int seq, hq, m, start, L, nkt;
-  bool active_b;
+  int ticket, seq, hq, m, start, L, active_b, bad;
+  __device__ int nkt() const { return active_b ? 2 * m + 2 : 2 * m + 1; }
 };
 
 // Maps ticket t of the dense item list to its item. `lvl` is the caller's level
 // cursor (the tickets a CTA receives only grow, so it only moves down).
-__device__ __forceinline__ Item item_of(const PrefillParams& p, const int* sorted,
-                                        const int* lvl_cnt, const int* lvl_off, int t,
-                                        int& lvl) {
+__device__ __forceinline__ Item item_of(const PrefillParams& p, int t, int& lvl) {
+  const int* sorted = p.tables;
+  const int* lvl_cnt = p.tables + kMaxSeqs;
+  const int* lvl_off = lvl_cnt + kMaxLevels;
   while (lvl > 0 && t >= lvl_off[lvl] + lvl_cnt[lvl] * p.num_q_heads) --lvl;
   Item w;
+  w.ticket = t;
   w.m = lvl;
   const int j = t - lvl_off[lvl];
   w.seq = sorted[j / p.num_q_heads];
@@ -125,7 +140,7 @@ __device__ __forceinline__ Item item_of(const PrefillParams& p, const int* sorte
   w.start = st;
   w.L = L;
   w.active_b = (2 * w.m + 1) * kBlockM < L;
-  w.nkt = w.active_b ? 2 * w.m + 2 : 2 * w.m + 1;
+  w.bad = 0;
   return w;
 }
 
@@ -143,52 +158,50 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
-    const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
-  using C = PCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  int* sorted = reinterpret_cast<int*>(smem + C::kSeq);
-  int* lvl_cnt = reinterpret_cast<int*>(smem + C::kLvlCnt);
-  int* lvl_off = reinterpret_cast<int*>(smem + C::kLvlOff);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
-  uint64_t* q_full = bars + 0;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;
-  uint64_t* k_empty = bars + 3;
-  uint64_t* v_full = bars + 4;
-  uint64_t* v_empty = bars + 5;
-  uint64_t* s_full = bars + 6;   // [2] per tile
-  uint64_t* p_full = bars + 8;   // [2]
-  uint64_t* o_full = bars + 10;  // [2]
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 12);
-  int* slot = reinterpret_cast<int*>(bars + 13);  // [2] ticket, [2] bad flag, by item parity
-  int* misc = slot + 4;                           // [0] total items
+__device__ __forceinline__ void publish(int* slot, const Item& w) {
+  slot[0] = w.ticket;
+  slot[1] = w.seq;
+  slot[2] = w.hq;
+  slot[3] = w.m;
+  slot[4] = w.start;
+  slot[5] = w.L;
+  slot[6] = w.active_b;
+  slot[7] = w.bad;
+}
+__device__ __forceinline__ Item read_slot(const int* slot) {
+  Item w;
+  w.ticket = slot[0];
+  w.seq = slot[1];
+  w.hq = slot[2];
+  w.m = slot[3];
+  w.start = slot[4];
+  w.L = slot[5];
+  w.active_b = slot[6];
+  w.bad = slot[7];
+  return w;
+}
 
+// Builds the longest-first item tables in shared scratch, copies them to the
+// workspace and leaves the number of items in misc[0].
+__device__ __forceinline__ void build_tables(const PrefillParams& p, uint8_t* scratch,
+                                             int* misc) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c = blockIdx.x, ncta = gridDim.x;
   const int S = p.num_seqs, NL = p.n_levels;
-
-  // length errors: reported once per sequence, by CTA 0
-  if (c == 0) {
-    for (int s = tid; s < S; s += kThreads) {
-      int st, L;
-      const bool ok = seq_ok(p, s, &st, &L) || L == 0;
-      if (!ok || (s == S - 1 && st + L != p.num_tokens)) record_status(p.dev_status, PGQA_EINVAL);
-    }
-  }
-
-  // ---- the dense item list: histogram of tile pairs per sequence (P area as scratch)
-  int* hist = reinterpret_cast<int*>(smem + C::kP);
+  int* hist = reinterpret_cast<int*>(scratch + kScrHist);
+  int* sorted = reinterpret_cast<int*>(scratch + kScrSorted);
+  int* lvl_cnt = reinterpret_cast<int*>(scratch + kScrCnt);
+  int* lvl_off = reinterpret_cast<int*>(scratch + kScrOff);
   for (int i = tid; i < NL; i += kThreads) hist[i] = 0;
   __syncthreads();
   for (int s = tid; s < S; s += kThreads) {
@@ -240,18 +253,62 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       misc[0] = off;
     }
   }
+  __syncthreads();
+  const int n_sorted = NL > 0 ? lvl_cnt[0] : 0;
+  for (int i = tid; i < n_sorted; i += kThreads) p.tables[i] = sorted[i];
+  for (int i = tid; i < NL; i += kThreads) {
+    p.tables[kMaxSeqs + i] = lvl_cnt[i];
+    p.tables[kMaxSeqs + kMaxLevels + i] = lvl_off[i];
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
+    const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+  using C = PCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* full = bars + 2;     // [kStages] ring
+  uint64_t* empty = bars + 5;    // [kStages]
+  uint64_t* s_full = bars + 8;   // [2] per tile: S_X computed
+  uint64_t* s_free = bars + 10;  // [2] S_X read into registers: its columns may be rewritten
+  uint64_t* p_full = bars + 12;  // [2] P_X written (and O_X rescaled)
+  uint64_t* o_full = bars + 14;  // [2] P_X V accumulated
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
+  int* slots = reinterpret_cast<int*>(bars + 17);  // [2][8]: the item, by item parity
+  int* misc = slots + 16;                          // [0] total items
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x, ncta = gridDim.x;
+
+  // length errors: reported once per sequence, by CTA 0
+  if (c == 0) {
+    for (int s = tid; s < p.num_seqs; s += kThreads) {
+      int st, L;
+      const bool ok = seq_ok(p, s, &st, &L) || L == 0;
+      if (!ok || (s == p.num_seqs - 1 && st + L != p.num_tokens))
+        record_status(p.dev_status, PGQA_EINVAL);
+    }
+  }
+  build_tables(p, smem + C::kP, misc);
   if (tid == 0) {
     mbar_init(q_full, 1);
     // Q buffers are reused once the item's last S MMAs are done (one commit) and all
     // 8 softmax warps have taken the item (one arrival each), so q_full can never
     // run two phases ahead of a softmax warp's wait
     mbar_init(q_empty, 1 + 8);
-    mbar_init(k_full, 1);
-    mbar_init(k_empty, 1);
-    mbar_init(v_full, 1);
-    mbar_init(v_empty, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], 4);
       mbar_init(&p_full[s], 4 * 32);
       mbar_init(&o_full[s], 1);
     }
@@ -262,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  __syncthreads();  // also orders the table writes before the TMA warp reads them
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const int total = misc[0];
@@ -274,34 +331,74 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
     }
-    int it = 0, gk = 0, gv = 0, lvl = NL - 1;
+    int it = 0, g = 0, lvl = p.n_levels - 1;
     bool ok = true;
-    int t = 0;
-    if (lane == 0) t = atomicAdd(p.ticket, 1);
-    t = __shfl_sync(0xffffffffu, t, 0);
-    for (;;) {
-      const bool last = t >= total;
-      int t_next = 0;
-      if (lane == 0 && !last) t_next = atomicAdd(p.ticket, 1);  // one ahead
+    // cache row of page 32 * ch + lane of item w (past the end: the zero-fill row)
+    auto chunk_rows = [&](const Item& w, int ch) {
+      int y = p.oob_row;
+      const int lp = ch * 32 + lane;
+      if (w.ticket >= 0 && lp * 16 < w.L) {
+        const int32_t pbn =
+            __ldg(p.block_tables + static_cast<size_t>(w.seq) * p.max_blocks_per_seq + lp);
+        if (pbn >= 0 && pbn < p.num_blocks) y = (pbn * p.num_kv_heads + w.hq / p.group) * 16;
+      }
+      return y;
+    };
+    // the next item: a ticket, its decode, its block-id check, its first 64 pages
+    struct Plan {
       Item w;
-      bool bad = false;
-      if (!last) {
-        w = item_of(p, sorted, lvl_cnt, lvl_off, t, lvl);
-        const int32_t* bt = p.block_tables + static_cast<size_t>(w.seq) * p.max_blocks_per_seq;
-        const int npages = (min(w.L, w.nkt * kBlockN) + 15) / 16;
+      int ch0, ch1;
+    };
+    auto plan_next = [&]() {
+      int t = 0;
+      if (lane == 0) t = atomicAdd(p.ticket, 1);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      Plan pl;
+      pl.w = Item{-1, 0, 0, 0, 0, 0, 0, 0};  // the end-of-list marker unless a ticket is left
+      if (t < total) {
+        pl.w = item_of(p, t, lvl);
+        const int32_t* bt = p.block_tables + static_cast<size_t>(pl.w.seq) * p.max_blocks_per_seq;
+        const int npages = (min(pl.w.L, pl.w.nkt() * kBlockN) + 15) / 16;
+        bool bad = false;
         for (int pg = lane; pg < npages; pg += 32) {  // block ids checked before Q is out
           const int32_t pbn = __ldg(bt + pg);
           bad |= pbn < 0 || pbn >= p.num_blocks;
         }
-        bad = __any_sync(0xffffffffu, bad);
+        pl.w.bad = __any_sync(0xffffffffu, bad);
       }
+      pl.ch0 = chunk_rows(pl.w, 0);
+      pl.ch1 = chunk_rows(pl.w, 1);
+      return pl;
+    };
+    // one ring load: K or V tile (g), rows y of this lane's page (lanes 0-7)
+    auto load_tile = [&](const CUtensorMap* map, int y) {
+      const int s = g % kStages;
+      if (lane == 0) {
+        if (g >= kStages && !mbar_wait(&empty[s], ((g / kStages) - 1) & 1))
+          ok = false;
+        else
+          mbar_arrive_expect_tx(&full[s], C::kTile);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) return;
+      if (lane < 8) {
+        uint8_t* dst = smem + C::kRing + s * C::kTile + lane * 2048;
+#pragma unroll
+        for (int sub = 0; sub < C::kSub; ++sub)
+          tma_load_2d(dst + sub * 16384, map, &full[s], sub * 64, y);
+      }
+      ++g;
+    };
+    Plan cur = plan_next();
+    for (;;) {
+      const Item& w = cur.w;
+      const bool last = w.ticket < 0;
       if (lane == 0) {
         if (it > 0 && !mbar_wait(q_empty, (it - 1) & 1)) {
           ok = false;
         } else {
-          slot[it & 1] = last ? -1 : t;
-          slot[2 + (it & 1)] = bad;
-          if (bad) record_status(p.dev_status, PGQA_EBADINDEX);
+          publish(slots + (it & 1) * 8, w);
+          if (w.bad) record_status(p.dev_status, PGQA_EBADINDEX);
           if (last) {
             mbar_arrive(q_full);  // publishes the end of the list
           } else {
@@ -320,55 +417,54 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       ok = __shfl_sync(0xffffffffu, ok, 0);
       ++it;
       if (last || !ok) break;
-      const int h = w.hq / p.group;
-      const int32_t* bt = p.block_tables + static_cast<size_t>(w.seq) * p.max_blocks_per_seq;
-      for (int j = 0; j < w.nkt && ok; ++j) {
-        int y = p.oob_row;
-        if (lane < 8) {
-          const int lp = j * 8 + lane;  // logical page
-          if (lp * 16 < w.L) {
-            const int32_t pbn = __ldg(bt + lp);
-            if (pbn >= 0 && pbn < p.num_blocks) y = (pbn * p.num_kv_heads + h) * 16;
-          }
+      const int nkt = w.nkt();
+      // rows of key tile j for lanes 0-7, from the chunk registers (chunk j / 4)
+      int ch_a = cur.ch0, ch_b = cur.ch1, ch_i = 0;
+      auto tile_row = [&](int j) {
+        if ((j >> 2) != ch_i) {  // j / 4 moves up by one at a time
+          ch_i = j >> 2;
+          ch_a = ch_b;
+          ch_b = chunk_rows(w, ch_i + 1);  // one chunk ahead
         }
-        if (lane == 0) {  // K tile j (its previous tile's S MMAs are done)
-          if (gk >= 1 && !mbar_wait(k_empty, (gk - 1) & 1))
-            ok = false;
-          else
-            mbar_arrive_expect_tx(k_full, C::kTile);
+        return __shfl_sync(0xffffffffu, ch_a, ((j & 3) << 3) | (lane & 7));
+      };
+      Plan nxt;
+      int n_loads = 0;
+      bool planned = false;
+      // once the ring is full, the warp plans the next item instead of waiting
+      auto after_load = [&]() {
+        if (++n_loads == kStages) {
+          nxt = plan_next();
+          planned = true;
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
+      };
+      // K runs one tile ahead of V: K_0, K_1, V_0, K_2, V_1, ..., V_{n-1}
+      int y_next = tile_row(0);
+      load_tile(&kmap, y_next);
+      after_load();
+      for (int j = 0; j < nkt && ok; ++j) {
+        const int y = y_next;
+        if (j + 1 < nkt) {
+          y_next = tile_row(j + 1);
+          load_tile(&kmap, y_next);
+          if (!ok) break;
+          after_load();
+        }
+        load_tile(&vmap, y);
         if (!ok) break;
-        if (lane < 8) {
-#pragma unroll
-          for (int sub = 0; sub < C::kSub; ++sub)
-            tma_load_2d(smem + C::kK + sub * 16384 + lane * 2048, &kmap, k_full, sub * 64, y);
-        }
-        ++gk;
-        if (lane == 0) {  // V tile j (its previous tile's PV MMAs are done)
-          if (gv >= 1 && !mbar_wait(v_empty, (gv - 1) & 1))
-            ok = false;
-          else
-            mbar_arrive_expect_tx(v_full, C::kTile);
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        if (lane < 8) {
-#pragma unroll
-          for (int sub = 0; sub < C::kSub; ++sub)
-            tma_load_2d(smem + C::kV + sub * 16384 + lane * 2048, &vmap, v_full, sub * 64, y);
-        }
-        ++gv;
+        after_load();
         __syncwarp();
       }
-      t = __shfl_sync(0xffffffffu, t_next, 0);
+      if (!ok) break;
+      if (!planned) nxt = plan_next();
+      cur = nxt;
     }
     if (lane == 0) {
       if (!ok) record_status(p.dev_status, PGQA_ETIMEOUT);
       // no TMA write may land after the CTA exits: wait for the last fill of each buffer
       bool done = mbar_wait(q_full, (it - 1) & 1);
-      if (gk > 0) done &= mbar_wait(k_full, (gk - 1) & 1);
-      if (gv > 0) done &= mbar_wait(v_full, (gv - 1) & 1);
+      for (int i = max(0, g - kStages); i < g; ++i)
+        done &= mbar_wait(&full[i % kStages], (i / kStages) & 1);
       if (!done) record_status(p.dev_status, PGQA_ETIMEOUT);
     }
   } else if (warp == kWarpMma) {
@@ -376,134 +472,140 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(128, kBlockN, false);
       const uint32_t id_o = idesc_bf16_f32(128, D, true);
-      const uint32_t q_addr = smem_u32(smem + C::kQ), k_addr = smem_u32(smem + C::kK);
-      const uint32_t v_addr = smem_u32(smem + C::kV), p_addr = smem_u32(smem + C::kP);
-      int it = 0, gk = 0, gv = 0, np[2] = {0, 0}, lvl = NL - 1;
+      const uint32_t q_addr = smem_u32(smem + C::kQ), ring = smem_u32(smem + C::kRing);
+      const uint32_t p_addr = smem_u32(smem + C::kP);
+      int it = 0, g = 0, np[2] = {0, 0}, s_issued[2] = {0, 0};
       bool ok = true;
-      // S_X = Q_X K^T
-      auto issue_s = [&](int X) {
-        const uint32_t qx = q_addr + X * C::kTile;
+      // S_X = Q_X K^T, K in ring stage ks, once the softmax has read the previous S_X
+      auto issue_s = [&](int X, int ks) {
+        if (s_issued[X] > 0) {
+          if (!(ok = mbar_wait(&s_free[X], (s_issued[X] - 1) & 1))) return false;
+          tc_fence_after();
+        }
+        ++s_issued[X];
+        const uint32_t qx = q_addr + X * C::kTile, kx = ring + ks * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           umma_f16_ss(tmem + X * 128, smem_desc_sw128(qx + off, 16, 1024),
-                      smem_desc_sw128(k_addr + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+                      smem_desc_sw128(kx + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[X]);
+        return true;
       };
-      // O_X (+)= P_X V
-      auto issue_pv = [&](int X, bool accumulate) {
-        const uint32_t px = p_addr + X * (128 * 128 * 2);
+      // O_X (+)= P_X V, V in ring stage vs, once the softmax has written P_X
+      auto issue_pv = [&](int X, int vs, bool accumulate) {
+        if (!(ok = mbar_wait(&p_full[X], np[X] & 1))) return false;
+        ++np[X];
+        tc_fence_after();
+        const uint32_t px = p_addr + X * (128 * 128 * 2), vx = ring + vs * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk) {
           const uint32_t poff = (kk >> 2) * 16384 + (kk & 3) * 32;
           umma_f16_ss(tmem + 256 + X * 128, smem_desc_sw128(px + poff, 16, 1024),
-                      smem_desc_sw128(v_addr + kk * 2048, 16384, 1024), id_o,
+                      smem_desc_sw128(vx + kk * 2048, 16384, 1024), id_o,
                       (accumulate || kk > 0) ? 1u : 0u);
         }
         umma_commit(&o_full[X]);
+        return true;
       };
+      // waits for ring load gi to land; returns its stage in st
+      auto take = [&](int gi, int& st) {
+        st = gi % kStages;
+        if (!(ok = mbar_wait(&full[st], (gi / kStages) & 1))) return false;
+        tc_fence_after();
+        return true;
+      };
+      // Per key tile j: S_A(j+1) as soon as the A softmax has read S_A(j) (it runs
+      // under that softmax), P_A V_j, S_B(j+1), P_B V_j.
       for (;;) {
         if (!(ok = mbar_wait(q_full, it & 1))) break;
-        const int t = slot[it & 1];
+        const Item w = read_slot(slots + (it & 1) * 8);
         ++it;
-        if (t < 0) break;
+        if (w.ticket < 0) break;
         tc_fence_after();
-        const Item w = item_of(p, sorted, lvl_cnt, lvl_off, t, lvl);
-        const int nkt_a = 2 * w.m + 1;
-        if (!(ok = mbar_wait(k_full, gk & 1))) break;
-        tc_fence_after();
-        issue_s(0);
-        if (w.active_b) issue_s(1);
-        umma_commit(k_empty);
-        ++gk;
-        if (w.nkt == 1) umma_commit(q_empty);
-        for (int j = 0; j < w.nkt; ++j) {
-          const bool more = j + 1 < w.nkt;
-          if (!(ok = mbar_wait(v_full, gv & 1))) break;
-          tc_fence_after();
-          if (j < nkt_a) {
-            if (!(ok = mbar_wait(&p_full[0], np[0] & 1))) break;
-            ++np[0];
-            tc_fence_after();
-            issue_pv(0, j > 0);
-          }
+        const int nkt = w.nkt(), nkt_a = 2 * w.m + 1;
+        int ks, vs;
+        if (!take(g++, ks)) break;  // K_0
+        if (!issue_s(0, ks)) break;
+        if (w.active_b && !issue_s(1, ks)) break;
+        umma_commit(&empty[ks]);
+        if (nkt == 1) umma_commit(q_empty);
+        for (int j = 0; j < nkt; ++j) {
+          const bool more = j + 1 < nkt;
           if (more) {
-            if (!(ok = mbar_wait(k_full, gk & 1))) break;
-            tc_fence_after();
-            if (j + 1 < nkt_a) issue_s(0);
+            if (!take(g++, ks)) break;  // K_{j+1}
+            if (j + 1 < nkt_a && !issue_s(0, ks)) break;
           }
-          if (w.active_b) {
-            if (!(ok = mbar_wait(&p_full[1], np[1] & 1))) break;
-            ++np[1];
-            tc_fence_after();
-            issue_pv(1, j > 0);
-          }
-          umma_commit(v_empty);
-          ++gv;
+          if (!take(g++, vs)) break;  // V_j
+          if (j < nkt_a && !issue_pv(0, vs, j > 0)) break;
           if (more) {
-            if (w.active_b) issue_s(1);
-            umma_commit(k_empty);
-            ++gk;
-            if (j + 1 == w.nkt - 1) umma_commit(q_empty);
+            if (w.active_b && !issue_s(1, ks)) break;
+            umma_commit(&empty[ks]);
+            if (j + 1 == nkt - 1) umma_commit(q_empty);
           }
+          if (w.active_b && !issue_pv(1, vs, j > 0)) break;
+          umma_commit(&empty[vs]);
         }
         if (!ok) break;
       }
       if (!ok) record_status(p.dev_status, PGQA_ETIMEOUT);
     }
-  } else {
+  } else if (warp < kWarpTma) {
     // ================================================================ softmax rows
-    const int X = warp >> 2;                      // 0: tile A, 1: tile B
-    const int wq = warp & 3;                      // TMEM lane quadrant
-    const int r = wq * 32 + lane;                 // query row in the tile = TMEM lane
+    const int X = warp >> 2;       // 0: tile A, 1: tile B
+    const int wq = warp & 3;       // TMEM lane quadrant
+    const int r = wq * 32 + lane;  // query row in the tile = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t s_col = X * 128, o_col = 256 + X * 128;
     uint8_t* sP = smem + C::kP + X * (128 * 128 * 2);
     const float sc = p.scale_log2;  // > 0 (checked on the host)
     const uint64_t sc2 = f2(sc, sc);
-    int it = 0, gv = 0, tcnt = 0, lvl = NL - 1;
+    int it = 0, gl = 0, tcnt = 0;
     bool ok = true;
     for (;;) {
-      // the item's ticket and bad-block flag were published with its Q; every softmax
-      // warp takes every item, including the warps of tile B when B does not exist
+      // every softmax warp takes every item, including the warps of tile B when B
+      // does not exist
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(q_full, it & 1)))) break;
-      const int t = slot[it & 1];
-      const bool bad = slot[2 + (it & 1)] != 0;
+      const Item w = read_slot(slots + (it & 1) * 8);
       ++it;
-      if (t < 0) break;
+      if (w.ticket < 0) break;
       __syncwarp();
       if (lane == 0) mbar_arrive(q_empty);
-      const Item w = item_of(p, sorted, lvl_cnt, lvl_off, t, lvl);
-      const int gv0 = gv;
-      gv += w.nkt;
+      const int gl0 = gl;  // ring index of this item's K_0 (then K_1, V_0, K_2, V_1, ...)
+      gl += 2 * w.nkt();
       if (X == 1 && !w.active_b) continue;
-      const int tq = 2 * w.m + X;                 // this tile's index in the sequence
-      const int qpos = tq * kBlockM + r;          // this row's position in the sequence
-      const int lim = min(qpos, w.L - 1);         // last key this row attends
+      const int tq = 2 * w.m + X;          // this tile's index in the sequence
+      const int qpos = tq * kBlockM + r;   // this row's position in the sequence
+      const int lim = min(qpos, w.L - 1);  // last key this row attends
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j <= tq; ++j) {
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(&s_full[X], tcnt & 1)))) break;
         tc_fence_after();
         const int kbase = j * kBlockN;
-        const bool diag = j == tq;  // the only tile with masked keys
-        // pass 1: the row's max (of the raw scores; scale > 0)
-        float mx = -INFINITY;
+        uint32_t sr[128];
+        tmem_ld128(lane_base + s_col, sr);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[X]);  // S_X(j+1) may now be computed
+        if (j == tq) {  // the diagonal tile: the only one with masked keys
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t sr[64];
-          tmem_ld64(lane_base + s_col + half * 64, sr);
-          if (!diag) {
-#pragma unroll
-            for (int q = 0; q < 64; q += 2)
-              mx = max3(mx, __uint_as_float(sr[q]), __uint_as_float(sr[q + 1]));
-          } else {
-#pragma unroll
-            for (int q = 0; q < 64; ++q)
-              mx = fmaxf(mx, kbase + half * 64 + q <= lim ? __uint_as_float(sr[q]) : -INFINITY);
-          }
+          for (int q = 0; q < 128; ++q)
+            if (kbase + q > lim) sr[q] = __float_as_uint(-INFINITY);
         }
-        mx *= sc;
+        // the row max of the raw scores over 8 independent chains (scale > 0)
+        float mc[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          mc[u] = fmaxf(__uint_as_float(sr[u]), __uint_as_float(sr[8 + u]));
+#pragma unroll
+        for (int q = 16; q < 128; q += 16) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            mc[u] = max3(mc[u], __uint_as_float(sr[q + u]), __uint_as_float(sr[q + 8 + u]));
+        }
+        const float mx =
+            max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])) * sc;
         if (j > 0) {  // P_X V of the previous tile done: O_X stable and P_X free
           if (!(ok = __all_sync(0xffffffffu, mbar_wait(&o_full[X], (tcnt - 1) & 1)))) break;
           tc_fence_after();
@@ -514,47 +616,43 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
           l *= alpha;
           m_ref = mx;
         }
-        // pass 2: P = 2^(s * scale - m_ref) as bf16 into row r of the K-major,
-        // 128-byte-swizzled A operand (masked keys give exactly 0)
+        // P = 2^(s * scale - m_ref) as bf16 into row r of the K-major, 128-byte-swizzled
+        // A operand (masked keys: 2^-inf = 0); the row sum over 8 independent chains
         const uint64_t neg_m2 = f2(-m_ref, -m_ref);
-        float sum0 = 0.f, sum1 = 0.f;
+        uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t sr[64];
-          tmem_ld64(lane_base + s_col + half * 64, sr);
+        for (int c16 = 0; c16 < 16; ++c16) {  // 16-byte chunk of the 256-byte row
+          uint32_t pk[4];
 #pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int i0 = c8 * 8 + 2 * q;
-              float a0, a1;
-              unf2(fma2(f2(__uint_as_float(sr[i0]), __uint_as_float(sr[i0 + 1])), sc2, neg_m2),
-                   a0, a1);
-              float e0 = ex2(a0), e1 = ex2(a1);
-              if (diag) {
-                if (kbase + half * 64 + i0 > lim) e0 = 0.f;
-                if (kbase + half * 64 + i0 + 1 > lim) e1 = 0.f;
-              }
-              sum0 += e0;
-              sum1 += e1;
-              pk[q] = pack_bf16(e0, e1);
-            }
-            const int c16 = half * 8 + c8;  // 16-byte chunk of the 256-byte row
-            *reinterpret_cast<uint4*>(sP + (c16 >> 3) * 16384 + swz128(r, c16 & 7)) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          for (int q = 0; q < 4; ++q) {
+            const int i0 = c16 * 8 + 2 * q;
+            float a0, a1;
+            unf2(fma2(f2(__uint_as_float(sr[i0]), __uint_as_float(sr[i0 + 1])), sc2, neg_m2), a0,
+                 a1);
+            const float e0 = ex2(a0), e1 = ex2(a1);
+            acc[q] = add2(acc[q], f2(e0, e1));
+            pk[q] = pack_bf16(e0, e1);
           }
+          *reinterpret_cast<uint4*>(sP + (c16 >> 3) * 16384 + swz128(r, c16 & 7)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
-        l += sum0 + sum1;
+        {
+          float s0, s1, s2, s3, s4, s5, s6, s7;
+          unf2(acc[0], s0, s1);
+          unf2(acc[1], s2, s3);
+          unf2(acc[2], s4, s5);
+          unf2(acc[3], s6, s7);
+          l += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+        }
         // rescale O_X when some row's max grew (warp-collective TMEM access)
         if (j > 0 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t o[32];
-            tmem_ld32(lane_base + o_col + cc * 32, o);
+          for (int cc = 0; cc < D / 64; ++cc) {
+            uint32_t o[64];
+            tmem_ld64(lane_base + o_col + cc * 64, o);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
-            tmem_st32(lane_base + o_col + cc * 32, o);
+            for (int q = 0; q < 64; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
+            tmem_st64(lane_base + o_col + cc * 64, o);
           }
           tmem_wait_st();
         }
@@ -562,11 +660,13 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         // that P = 0 there contributes exactly nothing. Only the last key tile of the
         // item reaches past the end, and only this tile's softmax uses it.
         if (kbase + kBlockN > w.L) {
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(v_full, (gv0 + j) & 1)))) break;
+          const int gi = gl0 + (j + 1 < w.nkt() ? 2 * j + 2 : 2 * j + 1), vs = gi % kStages;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full[vs], (gi / kStages) & 1)))) break;
           if (kbase + r >= w.L) {
+            uint8_t* vrow = smem + C::kRing + vs * C::kTile + r * 128;
 #pragma unroll
             for (int sub = 0; sub < C::kSub; ++sub) {
-              uint4* row = reinterpret_cast<uint4*>(smem + C::kV + sub * 16384 + r * 128);
+              uint4* row = reinterpret_cast<uint4*>(vrow + sub * 16384);
 #pragma unroll
               for (int q = 0; q < 8; ++q) row[q] = make_uint4(0, 0, 0, 0);
             }
@@ -593,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           uint4 v = make_uint4(0, 0, 0, 0);
-          if (!bad) {
+          if (!w.bad) {
             const float* f = reinterpret_cast<const float*>(o) + q * 8;
             v = make_uint4(pack_bf16(f[0] * inv, f[1] * inv), pack_bf16(f[2] * inv, f[3] * inv),
                            pack_bf16(f[4] * inv, f[5] * inv), pack_bf16(f[6] * inv, f[7] * inv));
@@ -601,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
           if (store) dst[half * 8 + q] = v;
         }
       }
-      if (store && p.lse) p.lse[orow] = bad ? -INFINITY : (m_ref + log2f(l)) * kLn2;
+      if (store && p.lse) p.lse[orow] = w.bad ? -INFINITY : (m_ref + log2f(l)) * kLn2;
       tc_fence_before();
     }
     if (!ok && lane == 0) record_status(p.dev_status, PGQA_ETIMEOUT);
@@ -644,6 +744,7 @@ pgqa_status_t launch_prefill_variant(const PrefillArgs& a) {
   p.block_tables = a.block_tables;
   p.dev_status = a.dev_status;
   p.ticket = static_cast<int*>(a.workspace);
+  p.tables = reinterpret_cast<int*>(static_cast<uint8_t*>(a.workspace) + 256);
   p.max_blocks_per_seq = a.max_blocks_per_seq;
   p.num_seqs = a.num_seqs;
   p.num_tokens = a.num_tokens;

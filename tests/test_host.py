@@ -116,4 +116,4 @@ def test_prefill_argument_validation():
     assert f(*args[:9], 5000, *args[10:]) == pgqa.EUNSUPPORTED     # more than 4096 sequences
     assert f(*args) == pgqa.ENOWORKSPACE                           # no workspace given
     assert f(*args[:10], 600000, *args[11:]) == pgqa.EUNSUPPORTED  # longer than 524288 tokens
-    assert pgqa.prefill_workspace_size(2, 8, 64) == 256
+    assert pgqa.prefill_workspace_size(2, 8, 64) == 256 + (4096 + 2 * 2048) * 4
