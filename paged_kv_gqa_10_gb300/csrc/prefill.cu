@@ -23,24 +23,24 @@
 //    counter for the next call.
 // Warp roles (12 warps; warps 10-11 only wait: at 384 threads the register
 // allocator fits the softmax in 167 registers without spilling)
-//  - warp 8 (TMA): publishes each item with its Q_A and Q_B, then streams K_0, K_1,
-//    V_0, K_2, V_1, ... (K one tile ahead, the order the MMA needs them) through a
-//    3-stage ring, each tile gathered as 8 pages of 16 rows with 2-D tensor-map loads
-//    (128-byte swizzle). Block ids are read 32 pages at a time, one chunk ahead, and
+//  - warp 8 (TMA): publishes each item with its Q_A and Q_B, then streams K_0, V_0,
+//    K_1, V_1, ... through a ring of 5 tiles (8 for head_dim 64), each tile gathered
+//    as 8 pages of 16 rows with 2-D tensor-map loads (128-byte swizzle). Block ids are read 32 pages at a time, one chunk ahead, and
 //    the next item (ticket, decode, block-id check, first pages) is planned while the
 //    ring is full, so no load waits on a table read. Pages past the sequence end are
 //    loaded from past the end of the cache view, which TMA fills with zeros.
 //  - warp 9 (MMA, one thread): tcgen05.mma, M = N = 128, f32 accumulators in TMEM:
-//    S_X = Q_X K^T for X = A, B and O_X += P_X V (V MN-major). S_X of the next key
-//    tile is computed as soon as the softmax has read S_X into registers, so it runs
-//    under that softmax; the tile pair ping-pongs, the tensor core working on one
-//    tile while the other's softmax runs.
+//    S_X = Q_X K^T for X = A, B (both operands in shared memory) and O_X += P_X V with
+//    P_X read from tensor memory (V MN-major in shared memory). Issue order per key
+//    tile j: P_A V_j, S_A(j+1), P_B V_j, S_B(j+1), so the tensor core works on one
+//    tile while the other's softmax runs; S_X(j+1) overwrites the columns P_X(j) was
+//    in, so it waits for P_X V_j to complete (the other tile's MMAs fill the pipe).
 //  - warps 0-3 / 4-7 (softmax of tile A / B; thread = query row = TMEM lane): one
 //    load of the row's 128 scores from TMEM, the causal mask on the diagonal tile
 //    only, the row max and sum over independent chains, P = 2^(s - m) as bf16 into
-//    shared memory in the MMA's swizzled layout, O rescaled in TMEM only when the
-//    running max grows by more than 2^8 (exact either way: P and l use the same
-//    reference max); at the end O / l -> bf16 out and lse.
+//    the first 64 columns of S_X, O rescaled in TMEM only when the running max grows
+//    by more than 2^8 (exact either way: P and l use the same reference max); at the
+//    end O / l -> bf16 out and lse.
 // All waits are bounded (a wait that gives up records PGQA_ETIMEOUT).
 #include <cuda_bf16.h>
 
@@ -55,8 +55,7 @@ constexpr int kBlockM = 128;  // query rows per tile
 constexpr int kBlockN = 128;  // keys per tile
 constexpr int kThreads = 384;
 constexpr int kWarpTma = 8, kWarpMma = 9;
-constexpr int kStages = 3;           // K/V ring
-constexpr uint32_t kTmemCols = 512;  // S_A 0, S_B 128, O_A 256, O_B 384
+constexpr uint32_t kTmemCols = 512;  // S_A 0, S_B 128 (P_X over the first 64), O_A 256, O_B 384
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
@@ -69,19 +68,19 @@ template <int D>
 struct PCfg {
   static constexpr int kSub = D / 64;        // 128-byte (64-element) column blocks
   static constexpr int kTile = 128 * D * 2;  // [128 rows][D] bf16
+  static constexpr int kStages = D == 128 ? 5 : 8;  // K/V ring: 160 KB / 128 KB
   static constexpr int kQ = 0;               // Q_A, Q_B
   static constexpr int kRing = 2 * kTile;    // kStages K/V tiles, in load order
-  static constexpr int kP = kRing + kStages * kTile;  // P_A, P_B: [128][128] bf16 each
-  static constexpr int kBar = kP + 2 * 128 * 128 * 2;
-  static constexpr int kSmem = 1024 + kBar + 256;
+  static constexpr int kBar = kRing + kStages * kTile;
+  static constexpr int kSmem = 1024 + kBar + 512;
 };
 
-// Scratch in the P area while the tables are built (before any P is written).
+// Scratch in the ring while the tables are built (before any tile is loaded).
 constexpr int kScrHist = 0;                            // int [kMaxLevels]
 constexpr int kScrSorted = kScrHist + kMaxLevels * 4;  // int [kMaxSeqs]
 constexpr int kScrCnt = kScrSorted + kMaxSeqs * 4;     // int [kMaxLevels]
 constexpr int kScrOff = kScrCnt + kMaxLevels * 4;      // int [kMaxLevels]
-static_assert(kScrOff + kMaxLevels * 4 <= 2 * 128 * 128 * 2, "table scratch");
+static_assert(kScrOff + kMaxLevels * 4 <= 5 * 128 * 64 * 2, "table scratch");
 
 struct PrefillParams {
   __nv_bfloat16* out;
@@ -267,20 +266,20 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
     const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
   using C = PCfg<D>;
+  constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* full = bars + 2;     // [kStages] ring
-  uint64_t* empty = bars + 5;    // [kStages]
-  uint64_t* s_full = bars + 8;   // [2] per tile: S_X computed
-  uint64_t* s_free = bars + 10;  // [2] S_X read into registers: its columns may be rewritten
-  uint64_t* p_full = bars + 12;  // [2] P_X written (and O_X rescaled)
-  uint64_t* o_full = bars + 14;  // [2] P_X V accumulated
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
-  int* slots = reinterpret_cast<int*>(bars + 17);  // [2][8]: the item, by item parity
+  uint64_t* full = bars + 2;                 // [kStages] ring
+  uint64_t* empty = full + kStages;          // [kStages]
+  uint64_t* s_full = empty + kStages;        // [2] per tile: S_X computed
+  uint64_t* p_full = s_full + 2;             // [2] P_X written (and O_X rescaled)
+  uint64_t* o_full = p_full + 2;             // [2] P_X V accumulated
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(o_full + 2);
+  int* slots = reinterpret_cast<int*>(o_full + 3);  // [2][8]: the item, by item parity
   int* misc = slots + 16;                          // [0] total items
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -295,7 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         record_status(p.dev_status, PGQA_EINVAL);
     }
   }
-  build_tables(p, smem + C::kP, misc);
+  static_assert((2 + 2 * kStages + 6 + 1) * 8 + 16 * 4 + 16 <= 512, "barrier area");
+  build_tables(p, smem + C::kRing, misc);
   if (tid == 0) {
     mbar_init(q_full, 1);
     // Q buffers are reused once the item's last S MMAs are done (one commit) and all
@@ -308,7 +308,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], 4);
       mbar_init(&p_full[s], 4 * 32);
       mbar_init(&o_full[s], 1);
     }
@@ -438,18 +437,12 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
           planned = true;
         }
       };
-      // K runs one tile ahead of V: K_0, K_1, V_0, K_2, V_1, ..., V_{n-1}
-      int y_next = tile_row(0);
-      load_tile(&kmap, y_next);
-      after_load();
+      // K_0, V_0, K_1, V_1, ...
       for (int j = 0; j < nkt && ok; ++j) {
-        const int y = y_next;
-        if (j + 1 < nkt) {
-          y_next = tile_row(j + 1);
-          load_tile(&kmap, y_next);
-          if (!ok) break;
-          after_load();
-        }
+        const int y = tile_row(j);
+        load_tile(&kmap, y);
+        if (!ok) break;
+        after_load();
         load_tile(&vmap, y);
         if (!ok) break;
         after_load();
@@ -473,16 +466,15 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       const uint32_t id_s = idesc_bf16_f32(128, kBlockN, false);
       const uint32_t id_o = idesc_bf16_f32(128, D, true);
       const uint32_t q_addr = smem_u32(smem + C::kQ), ring = smem_u32(smem + C::kRing);
-      const uint32_t p_addr = smem_u32(smem + C::kP);
-      int it = 0, g = 0, np[2] = {0, 0}, s_issued[2] = {0, 0};
+      int it = 0, g = 0, np[2] = {0, 0}, pv_issued[2] = {0, 0};
       bool ok = true;
-      // S_X = Q_X K^T, K in ring stage ks, once the softmax has read the previous S_X
+      // S_X = Q_X K^T, K in ring stage ks. Its columns held P_X of the previous tile:
+      // wait for that P_X V to complete first.
       auto issue_s = [&](int X, int ks) {
-        if (s_issued[X] > 0) {
-          if (!(ok = mbar_wait(&s_free[X], (s_issued[X] - 1) & 1))) return false;
+        if (pv_issued[X] > 0) {
+          if (!(ok = mbar_wait(&o_full[X], (pv_issued[X] - 1) & 1))) return false;
           tc_fence_after();
         }
-        ++s_issued[X];
         const uint32_t qx = q_addr + X * C::kTile, kx = ring + ks * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -493,20 +485,19 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         umma_commit(&s_full[X]);
         return true;
       };
-      // O_X (+)= P_X V, V in ring stage vs, once the softmax has written P_X
+      // O_X (+)= P_X V: P_X from TMEM (8 columns per 16 keys), V in ring stage vs
       auto issue_pv = [&](int X, int vs, bool accumulate) {
         if (!(ok = mbar_wait(&p_full[X], np[X] & 1))) return false;
         ++np[X];
         tc_fence_after();
-        const uint32_t px = p_addr + X * (128 * 128 * 2), vx = ring + vs * C::kTile;
+        const uint32_t vx = ring + vs * C::kTile;
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          const uint32_t poff = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_f16_ss(tmem + 256 + X * 128, smem_desc_sw128(px + poff, 16, 1024),
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          umma_f16_ts(tmem + 256 + X * 128, tmem + X * 128 + kk * 8,
                       smem_desc_sw128(vx + kk * 2048, 16384, 1024), id_o,
                       (accumulate || kk > 0) ? 1u : 0u);
-        }
         umma_commit(&o_full[X]);
+        ++pv_issued[X];
         return true;
       };
       // waits for ring load gi to land; returns its stage in st
@@ -516,8 +507,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         tc_fence_after();
         return true;
       };
-      // Per key tile j: S_A(j+1) as soon as the A softmax has read S_A(j) (it runs
-      // under that softmax), P_A V_j, S_B(j+1), P_B V_j.
       for (;;) {
         if (!(ok = mbar_wait(q_full, it & 1))) break;
         const Item w = read_slot(slots + (it & 1) * 8);
@@ -533,19 +522,19 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         if (nkt == 1) umma_commit(q_empty);
         for (int j = 0; j < nkt; ++j) {
           const bool more = j + 1 < nkt;
+          if (!take(g++, vs)) break;  // V_j
+          if (j < nkt_a && !issue_pv(0, vs, j > 0)) break;
           if (more) {
             if (!take(g++, ks)) break;  // K_{j+1}
             if (j + 1 < nkt_a && !issue_s(0, ks)) break;
           }
-          if (!take(g++, vs)) break;  // V_j
-          if (j < nkt_a && !issue_pv(0, vs, j > 0)) break;
+          if (w.active_b && !issue_pv(1, vs, j > 0)) break;
+          umma_commit(&empty[vs]);
           if (more) {
             if (w.active_b && !issue_s(1, ks)) break;
             umma_commit(&empty[ks]);
             if (j + 1 == nkt - 1) umma_commit(q_empty);
           }
-          if (w.active_b && !issue_pv(1, vs, j > 0)) break;
-          umma_commit(&empty[vs]);
         }
         if (!ok) break;
       }
@@ -558,7 +547,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     const int r = wq * 32 + lane;  // query row in the tile = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t s_col = X * 128, o_col = 256 + X * 128;
-    uint8_t* sP = smem + C::kP + X * (128 * 128 * 2);
     const float sc = p.scale_log2;  // > 0 (checked on the host)
     const uint64_t sc2 = f2(sc, sc);
     int it = 0, gl = 0, tcnt = 0;
@@ -572,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       if (w.ticket < 0) break;
       __syncwarp();
       if (lane == 0) mbar_arrive(q_empty);
-      const int gl0 = gl;  // ring index of this item's K_0 (then K_1, V_0, K_2, V_1, ...)
+      const int gl0 = gl;  // ring index of this item's K_0 (then V_0, K_1, V_1, ...)
       gl += 2 * w.nkt();
       if (X == 1 && !w.active_b) continue;
       const int tq = 2 * w.m + X;          // this tile's index in the sequence
@@ -585,9 +573,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         const int kbase = j * kBlockN;
         uint32_t sr[128];
         tmem_ld128(lane_base + s_col, sr);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[X]);  // S_X(j+1) may now be computed
         if (j == tq) {  // the diagonal tile: the only one with masked keys
 #pragma unroll
           for (int q = 0; q < 128; ++q)
@@ -606,36 +591,28 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         }
         const float mx =
             max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])) * sc;
-        if (j > 0) {  // P_X V of the previous tile done: O_X stable and P_X free
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&o_full[X], (tcnt - 1) & 1)))) break;
-          tc_fence_after();
-        }
+        // (S_X(j) was issued after P_X V_{j-1} completed: O_X is stable here)
         const bool grow = mx > m_ref + kRescaleThreshold;
         const float alpha = grow ? ex2(m_ref - mx) : 1.f;  // 0 while m_ref = -inf
         if (grow) {
           l *= alpha;
           m_ref = mx;
         }
-        // P = 2^(s * scale - m_ref) as bf16 into row r of the K-major, 128-byte-swizzled
-        // A operand (masked keys: 2^-inf = 0); the row sum over 8 independent chains
+        // P = 2^(s * scale - m_ref) as bf16, two keys per TMEM column over the first
+        // 64 columns of S_X (masked keys: 2^-inf = 0); the row sum over 8 chains
         const uint64_t neg_m2 = f2(-m_ref, -m_ref);
         uint64_t acc[4] = {0, 0, 0, 0};
+        uint32_t pk[64];
 #pragma unroll
-        for (int c16 = 0; c16 < 16; ++c16) {  // 16-byte chunk of the 256-byte row
-          uint32_t pk[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int i0 = c16 * 8 + 2 * q;
-            float a0, a1;
-            unf2(fma2(f2(__uint_as_float(sr[i0]), __uint_as_float(sr[i0 + 1])), sc2, neg_m2), a0,
-                 a1);
-            const float e0 = ex2(a0), e1 = ex2(a1);
-            acc[q] = add2(acc[q], f2(e0, e1));
-            pk[q] = pack_bf16(e0, e1);
-          }
-          *reinterpret_cast<uint4*>(sP + (c16 >> 3) * 16384 + swz128(r, c16 & 7)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        for (int c = 0; c < 64; ++c) {
+          float a0, a1;
+          unf2(fma2(f2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc2, neg_m2),
+               a0, a1);
+          const float e0 = ex2(a0), e1 = ex2(a1);
+          acc[c & 3] = add2(acc[c & 3], f2(e0, e1));
+          pk[c] = pack_bf16(e0, e1);
         }
+        tmem_st64(lane_base + s_col, pk);
         {
           float s0, s1, s2, s3, s4, s5, s6, s7;
           unf2(acc[0], s0, s1);
@@ -654,13 +631,13 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
             for (int q = 0; q < 64; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
             tmem_st64(lane_base + o_col + cc * 64, o);
           }
-          tmem_wait_st();
         }
+        tmem_wait_st();
         // V rows past the sequence end may hold anything (NaN included): zero them so
         // that P = 0 there contributes exactly nothing. Only the last key tile of the
         // item reaches past the end, and only this tile's softmax uses it.
         if (kbase + kBlockN > w.L) {
-          const int gi = gl0 + (j + 1 < w.nkt() ? 2 * j + 2 : 2 * j + 1), vs = gi % kStages;
+          const int gi = gl0 + 2 * j + 1, vs = gi % kStages;
           if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full[vs], (gi / kStages) & 1)))) break;
           if (kbase + r >= w.L) {
             uint8_t* vrow = smem + C::kRing + vs * C::kTile + r * 128;
