@@ -21,14 +21,17 @@
 //    SM) takes items from the list with an atomic ticket counter, so the load
 //    balances itself whatever the length mix; the last CTA to finish resets the
 //    counter for the next call.
-// Warp roles (12 warps; warps 10-11 only wait: at 384 threads the register
-// allocator fits the softmax in 167 registers without spilling)
+// Warp roles (12 warps; warp 11 only waits: at 384 threads the register allocator
+// fits the softmax in 167 registers without spilling)
+//  - warp 10 (planner): takes tickets, decodes the items and checks their block ids,
+//    up to two items ahead of the TMA warp (a two-entry queue in shared memory).
 //  - warp 8 (TMA): publishes each item with its Q_A and Q_B, then streams K_0, V_0,
 //    K_1, V_1, ... through a ring of 5 tiles (8 for head_dim 64), each tile gathered
-//    as 8 pages of 16 rows with 2-D tensor-map loads (128-byte swizzle). Block ids are read 32 pages at a time, one chunk ahead, and
-//    the next item (ticket, decode, block-id check, first pages) is planned while the
-//    ring is full, so no load waits on a table read. Pages past the sequence end are
-//    loaded from past the end of the cache view, which TMA fills with zeros.
+//    as 8 pages of 16 rows with 2-D tensor-map loads (128-byte swizzle). Block ids are
+//    read 32 pages at a time, one chunk ahead, and the next item's first pages are
+//    requested while the ring is full, so no load waits on a table read. Pages past
+//    the sequence end are loaded from past the end of the cache view, which TMA
+//    fills with zeros.
 //  - warp 9 (MMA, one thread): tcgen05.mma, M = N = 128, f32 accumulators in TMEM:
 //    S_X = Q_X K^T for X = A, B (both operands in shared memory) and O_X += P_X V with
 //    P_X read from tensor memory (V MN-major in shared memory). Issue order per key
@@ -54,7 +57,7 @@ namespace {
 constexpr int kBlockM = 128;  // query rows per tile
 constexpr int kBlockN = 128;  // keys per tile
 constexpr int kThreads = 384;
-constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kWarpTma = 8, kWarpMma = 9, kWarpPlan = 10;
 constexpr uint32_t kTmemCols = 512;  // S_A 0, S_B 128 (P_X over the first 64), O_A 256, O_B 384
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -278,9 +281,12 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
   uint64_t* s_full = empty + kStages;        // [2] per tile: S_X computed
   uint64_t* p_full = s_full + 2;             // [2] P_X written (and O_X rescaled)
   uint64_t* o_full = p_full + 2;             // [2] P_X V accumulated
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(o_full + 2);
-  int* slots = reinterpret_cast<int*>(o_full + 3);  // [2][8]: the item, by item parity
-  int* misc = slots + 16;                          // [0] total items
+  uint64_t* plan_full = o_full + 2;          // [2] planner -> TMA warp item queue
+  uint64_t* plan_empty = plan_full + 2;      // [2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(plan_empty + 2);
+  int* slots = reinterpret_cast<int*>(plan_empty + 3);  // [2][8]: the item, by item parity
+  int* plans = slots + 16;                              // [2][8]: the planner's queue
+  int* misc = plans + 16;                               // [0] total items
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, ncta = gridDim.x;
@@ -294,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         record_status(p.dev_status, PGQA_EINVAL);
     }
   }
-  static_assert((2 + 2 * kStages + 6 + 1) * 8 + 16 * 4 + 16 <= 512, "barrier area");
+  static_assert((2 + 2 * kStages + 10 + 1) * 8 + 32 * 4 + 16 <= 512, "barrier area");
   build_tables(p, smem + C::kRing, misc);
   if (tid == 0) {
     mbar_init(q_full, 1);
@@ -310,6 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       mbar_init(&s_full[s], 1);
       mbar_init(&p_full[s], 4 * 32);
       mbar_init(&o_full[s], 1);
+      mbar_init(&plan_full[s], 1);
+      mbar_init(&plan_empty[s], 1);
     }
     fence_mbar_init();
   }
@@ -330,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
     }
-    int it = 0, g = 0, lvl = p.n_levels - 1;
+    int it = 0, g = 0;
     bool ok = true;
     // cache row of page 32 * ch + lane of item w (past the end: the zero-fill row)
     auto chunk_rows = [&](const Item& w, int ch) {
@@ -343,34 +351,32 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       }
       return y;
     };
-    // the next item: a ticket, its decode, its block-id check, its first 64 pages
+    // the next item from the planner's queue (decoded, block ids checked) and the
+    // cache rows of its first 64 pages
     struct Plan {
       Item w;
       int ch0, ch1;
     };
+    int n_plans = 0;
     auto plan_next = [&]() {
-      int t = 0;
-      if (lane == 0) t = atomicAdd(p.ticket, 1);
-      t = __shfl_sync(0xffffffffu, t, 0);
       Plan pl;
-      pl.w = Item{-1, 0, 0, 0, 0, 0, 0, 0};  // the end-of-list marker unless a ticket is left
-      if (t < total) {
-        pl.w = item_of(p, t, lvl);
-        const int32_t* bt = p.block_tables + static_cast<size_t>(pl.w.seq) * p.max_blocks_per_seq;
-        const int npages = (min(pl.w.L, pl.w.nkt() * kBlockN) + 15) / 16;
-        bool bad = false;
-        for (int pg = lane; pg < npages; pg += 32) {  // block ids checked before Q is out
-          const int32_t pbn = __ldg(bt + pg);
-          bad |= pbn < 0 || pbn >= p.num_blocks;
-        }
-        pl.w.bad = __any_sync(0xffffffffu, bad);
+      pl.w = Item{-1, 0, 0, 0, 0, 0, 0, 0};
+      const int q = n_plans & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&plan_full[q], (n_plans >> 1) & 1))) {
+        ok = false;  // the end marker stands in for the item
+      } else {
+        pl.w = read_slot(plans + q * 8);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&plan_empty[q]);
       }
+      ++n_plans;
       pl.ch0 = chunk_rows(pl.w, 0);
       pl.ch1 = chunk_rows(pl.w, 1);
       return pl;
     };
     // one ring load: K or V tile (g), rows y of this lane's page (lanes 0-7)
     auto load_tile = [&](const CUtensorMap* map, int y) {
+      if (!ok) return;
       const int s = g % kStages;
       if (lane == 0) {
         if (g >= kStages && !mbar_wait(&empty[s], ((g / kStages) - 1) & 1))
@@ -390,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     };
     Plan cur = plan_next();
     for (;;) {
+      if (!ok) break;
       const Item& w = cur.w;
       const bool last = w.ticket < 0;
       if (lane == 0) {
@@ -460,6 +467,40 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         done &= mbar_wait(&full[i % kStages], (i / kStages) & 1);
       if (!done) record_status(p.dev_status, PGQA_ETIMEOUT);
     }
+  } else if (warp == kWarpPlan) {
+    // ================================================================ planner
+    // Takes tickets, decodes them and checks the items' block ids, two items ahead
+    // of the TMA warp, so no table read sits on the load path.
+    int lvl = p.n_levels - 1;
+    bool ok = true;
+    for (int k = 0;; ++k) {
+      const int q = k & 1;
+      if (k >= 2 && !__all_sync(0xffffffffu, mbar_wait(&plan_empty[q], ((k >> 1) - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      int t = 0;
+      if (lane == 0) t = atomicAdd(p.ticket, 1);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      Item w{-1, 0, 0, 0, 0, 0, 0, 0};  // the end-of-list marker unless a ticket is left
+      if (t < total) {
+        w = item_of(p, t, lvl);
+        const int32_t* bt = p.block_tables + static_cast<size_t>(w.seq) * p.max_blocks_per_seq;
+        const int npages = (min(w.L, w.nkt() * kBlockN) + 15) / 16;
+        bool bad = false;
+        for (int pg = lane; pg < npages; pg += 32) {  // block ids checked before Q is out
+          const int32_t pbn = __ldg(bt + pg);
+          bad |= pbn < 0 || pbn >= p.num_blocks;
+        }
+        w.bad = __any_sync(0xffffffffu, bad);
+      }
+      if (lane == 0) {
+        publish(plans + q * 8, w);
+        mbar_arrive(&plan_full[q]);
+      }
+      if (w.ticket < 0) break;
+    }
+    if (!ok && lane == 0) record_status(p.dev_status, PGQA_ETIMEOUT);
   } else if (warp == kWarpMma) {
     // ================================================================ MMA issuer
     if (lane == 0) {
