@@ -239,7 +239,7 @@ size_t pgqa_prefill_workspace_size(int num_seqs, int num_q_heads, int max_seqlen
  *   cu_seqlens    [num_seqs + 1] int32, read: sequence i owns tokens
  *                 cu_seqlens[i] .. cu_seqlens[i+1]-1; the token at position p
  *                 of sequence i attends to keys 0..p of sequence i.
- *   max_seqlen    an upper bound on the sequence lengths (at most 524288).
+ *   max_seqlen    an upper bound on the sequence lengths (at most 262144).
  *   block_tables  [num_seqs][max_blocks_per_seq] int32, read.
  *   num_seqs      at most 4096.
  *   scale         must be > 0.

@@ -10,12 +10,13 @@
 // online softmax over 128-key tiles; the full score matrix is never formed.
 //
 // Work and scheduling
-//  - A work item is a pair of consecutive 128-query tiles (A = 2m, B = 2m + 1) of
-//    one query head; tile t visits key tiles 0..t (causal tile skipping) and B
-//    exists only if the sequence reaches it.
+//  - A work item is one 128-query tile t of a sequence for a pair of query heads of
+//    one kv-head group (A = head h, B = head h + 1; B absent for the last head of an
+//    odd-sized group). Both tiles visit key tiles 0..t (causal tile skipping) over the
+//    same K/V, in lockstep.
 //  - Every CTA builds the same dense list of the batch's items, longest first:
-//    items of pair index m (descending), then sequences ordered by their number of
-//    tile pairs (a stable counting sort in shared memory), then heads (so the heads
+//    items of tile index t (descending), then sequences ordered by their number of
+//    tiles (a stable counting sort in shared memory), then head pairs (so the heads
 //    sharing a kv-head run side by side and share K/V in L2). The tables go to the
 //    workspace (every CTA writes the same values). A persistent grid (one CTA per
 //    SM) takes items from the list with an atomic ticket counter, so the load
@@ -63,7 +64,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 constexpr int kMaxSeqs = 4096;            // sequences per call
-constexpr int kMaxLevels = 2048;          // tile pairs of the longest sequence
+constexpr int kMaxLevels = 2048;          // query tiles of the longest sequence
 static_assert(256 + (kMaxSeqs + 2 * kMaxLevels) * 4 == kPrefillWorkspaceBytes,
               "workspace layout");
 
@@ -97,7 +98,8 @@ struct PrefillParams {
   int num_seqs, num_tokens, max_seqlen;
   int num_q_heads, num_kv_heads, group;
   int num_blocks;
-  int n_levels;  // tile pairs of the longest allowed sequence
+  int n_levels;  // query tiles of the longest allowed sequence
+  int pairs;     // head pairs per (sequence, tile): num_kv_heads * ceil(group / 2)
   int oob_row;   // a row index past the end of the cache view (TMA fills zeros)
   float scale_log2;
 };
@@ -110,18 +112,19 @@ __device__ __forceinline__ bool seq_ok(const PrefillParams& p, int s, int* start
          st + L <= p.num_tokens;
 }
 
-// Tile pairs of sequence s (0 for an empty or invalid one).
-__device__ __forceinline__ int pairs_of(const PrefillParams& p, int s) {
+// Query tiles of sequence s (0 for an empty or invalid one).
+__device__ __forceinline__ int tiles_of(const PrefillParams& p, int s) {
   int st, L;
   if (!seq_ok(p, s, &st, &L)) return 0;
-  return ((L + kBlockM - 1) / kBlockM + 1) / 2;
+  return (L + kBlockM - 1) / kBlockM;
 }
 
-// One work item: a pair of query tiles of one (sequence, head), as the TMA warp
-// publishes it to the other roles (8 ints per slot). ticket < 0: end of the list.
+// One work item: query tile t of one sequence for heads hq (A) and hq + 1 (B, if
+// active_b), as the TMA warp publishes it to the other roles (8 ints per slot).
+// ticket < 0: end of the list.
 struct Item {
-  int ticket, seq, hq, m, start, L, active_b, bad;
-  __device__ int nkt() const { return active_b ? 2 * m + 2 : 2 * m + 1; }
+  int ticket, seq, hq, t, start, L, active_b, bad;
+  __device__ int nkt() const { return t + 1; }
 };
 
 // Maps ticket t of the dense item list to its item. `lvl` is the caller's level
@@ -130,18 +133,20 @@ __device__ __forceinline__ Item item_of(const PrefillParams& p, int t, int& lvl)
   const int* sorted = p.tables;
   const int* lvl_cnt = p.tables + kMaxSeqs;
   const int* lvl_off = lvl_cnt + kMaxLevels;
-  while (lvl > 0 && t >= lvl_off[lvl] + lvl_cnt[lvl] * p.num_q_heads) --lvl;
+  while (lvl > 0 && t >= lvl_off[lvl] + lvl_cnt[lvl] * p.pairs) --lvl;
   Item w;
   w.ticket = t;
-  w.m = lvl;
+  w.t = lvl;
   const int j = t - lvl_off[lvl];
-  w.seq = sorted[j / p.num_q_heads];
-  w.hq = j % p.num_q_heads;
+  w.seq = sorted[j / p.pairs];
+  const int per_group = (p.group + 1) / 2, pi = j % p.pairs;
+  const int kv = pi / per_group;
+  w.hq = kv * p.group + 2 * (pi % per_group);
+  w.active_b = w.hq + 1 < (kv + 1) * p.group;
   int st, L;
   seq_ok(p, w.seq, &st, &L);
   w.start = st;
   w.L = L;
-  w.active_b = (2 * w.m + 1) * kBlockM < L;
   w.bad = 0;
   return w;
 }
@@ -175,7 +180,7 @@ __device__ __forceinline__ void publish(int* slot, const Item& w) {
   slot[0] = w.ticket;
   slot[1] = w.seq;
   slot[2] = w.hq;
-  slot[3] = w.m;
+  slot[3] = w.t;
   slot[4] = w.start;
   slot[5] = w.L;
   slot[6] = w.active_b;
@@ -186,7 +191,7 @@ __device__ __forceinline__ Item read_slot(const int* slot) {
   w.ticket = slot[0];
   w.seq = slot[1];
   w.hq = slot[2];
-  w.m = slot[3];
+  w.t = slot[3];
   w.start = slot[4];
   w.L = slot[5];
   w.active_b = slot[6];
@@ -207,12 +212,12 @@ __device__ __forceinline__ void build_tables(const PrefillParams& p, uint8_t* sc
   for (int i = tid; i < NL; i += kThreads) hist[i] = 0;
   __syncthreads();
   for (int s = tid; s < S; s += kThreads) {
-    const int np = pairs_of(p, s);
+    const int np = tiles_of(p, s);
     if (np > 0) atomicAdd(&hist[np - 1], 1);
   }
   __syncthreads();
   if (warp == 0) {
-    // lvl_cnt[m] = sequences with more than m pairs (a suffix sum over the histogram)
+    // lvl_cnt[m] = sequences with more than m tiles (a suffix sum over the histogram)
     int carry = 0;
     for (int base = ((NL - 1) / 32) * 32; base >= 0; base -= 32) {
       const int m = base + 31 - lane;  // descending within the chunk
@@ -226,14 +231,14 @@ __device__ __forceinline__ void build_tables(const PrefillParams& p, uint8_t* sc
       carry += __shfl_sync(0xffffffffu, v, 31);
     }
     __syncwarp();
-    // scatter cursor of pair count v: after the sequences with more than v pairs
+    // scatter cursor of tile count v: after the sequences with more than v tiles
     int* cursor = hist;
     for (int v = 1 + lane; v <= NL; v += 32) cursor[v - 1] = v < NL ? lvl_cnt[v] : 0;
     __syncwarp();
-    // stable scatter: sequence index order within equal pair counts
+    // stable scatter: sequence index order within equal tile counts
     for (int base = 0; base < S; base += 32) {
       const int s = base + lane;
-      const int v = s < S ? pairs_of(p, s) : 0;
+      const int v = s < S ? tiles_of(p, s) : 0;
       const unsigned grp = __match_any_sync(0xffffffffu, v);
       const int rank = __popc(grp & ((1u << lane) - 1));
       int pos = 0;
@@ -250,7 +255,7 @@ __device__ __forceinline__ void build_tables(const PrefillParams& p, uint8_t* sc
       int off = 0;
       for (int m = NL - 1; m >= 0; --m) {
         lvl_off[m] = off;
-        off += lvl_cnt[m] * p.num_q_heads;
+        off += lvl_cnt[m] * p.pairs;
       }
       misc[0] = off;
     }
@@ -412,10 +417,10 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
 #pragma unroll
             for (int sub = 0; sub < C::kSub; ++sub) {
               tma_load_3d(smem + C::kQ + sub * 16384, &qmap, q_full, sub * 64, w.hq,
-                          w.start + 2 * w.m * kBlockM);
+                          w.start + w.t * kBlockM);
               if (w.active_b)
                 tma_load_3d(smem + C::kQ + C::kTile + sub * 16384, &qmap, q_full, sub * 64,
-                            w.hq, w.start + (2 * w.m + 1) * kBlockM);
+                            w.hq + 1, w.start + w.t * kBlockM);
             }
           }
         }
@@ -554,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         ++it;
         if (w.ticket < 0) break;
         tc_fence_after();
-        const int nkt = w.nkt(), nkt_a = 2 * w.m + 1;
+        const int nkt = w.nkt(), nkt_a = nkt;  // both tiles visit key tiles 0..t
         int ks, vs;
         if (!take(g++, ks)) break;  // K_0
         if (!issue_s(0, ks)) break;
@@ -604,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       const int gl0 = gl;  // ring index of this item's K_0 (then V_0, K_1, V_1, ...)
       gl += 2 * w.nkt();
       if (X == 1 && !w.active_b) continue;
-      const int tq = 2 * w.m + X;          // this tile's index in the sequence
+      const int tq = w.t;                  // this tile's index in the sequence
       const int qpos = tq * kBlockM + r;   // this row's position in the sequence
       const int lim = min(qpos, w.L - 1);  // last key this row attends
       float m_ref = -INFINITY, l = 0.f;
@@ -676,8 +681,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         tmem_wait_st();
         // V rows past the sequence end may hold anything (NaN included): zero them so
         // that P = 0 there contributes exactly nothing. Only the last key tile of the
-        // item reaches past the end, and only this tile's softmax uses it.
-        if (kbase + kBlockN > w.L) {
+        // item reaches past the end; tile A's softmax zeroes it (P_B V is issued after
+        // P_A V, which waits for this).
+        if (X == 0 && kbase + kBlockN > w.L) {
           const int gi = gl0 + 2 * j + 1, vs = gi % kStages;
           if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full[vs], (gi / kStages) & 1)))) break;
           if (kbase + r >= w.L) {
@@ -701,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       tc_fence_after();
       const bool store = qpos < w.L;
       const size_t orow =
-          static_cast<size_t>(w.start + (store ? qpos : 0)) * p.num_q_heads + w.hq;
+          static_cast<size_t>(w.start + (store ? qpos : 0)) * p.num_q_heads + w.hq + X;
       uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D);
       const float inv = 1.f / l;
 #pragma unroll
@@ -771,10 +777,11 @@ pgqa_status_t launch_prefill_variant(const PrefillArgs& a) {
   p.num_kv_heads = a.num_kv_heads;
   p.group = a.num_q_heads / a.num_kv_heads;
   p.num_blocks = a.num_blocks;
-  p.n_levels = ((a.max_seqlen + kBlockM - 1) / kBlockM + 1) / 2;
+  p.n_levels = (a.max_seqlen + kBlockM - 1) / kBlockM;
+  p.pairs = a.num_kv_heads * ((p.group + 1) / 2);
   p.oob_row = static_cast<int>(rows);
   p.scale_log2 = a.scale * kLog2e;
-  const long long items = static_cast<long long>(p.n_levels) * a.num_seqs * a.num_q_heads;
+  const long long items = static_cast<long long>(p.n_levels) * a.num_seqs * p.pairs;
   const int grid = static_cast<int>(items < sms ? items : sms);
   paged_prefill_kernel<D><<<grid, kThreads, C::kSmem, a.stream>>>(qmap, kmap, vmap, p);
   return cudaPeekAtLastError() == cudaSuccess ? PGQA_OK : PGQA_ECUDA;
@@ -783,7 +790,7 @@ pgqa_status_t launch_prefill_variant(const PrefillArgs& a) {
 }  // namespace
 
 int prefill_max_seqs() { return kMaxSeqs; }
-int prefill_max_seqlen() { return kMaxLevels * 2 * kBlockM; }
+int prefill_max_seqlen() { return kMaxLevels * kBlockM; }
 
 pgqa_status_t launch_paged_prefill(const PrefillArgs& a) {
   if (a.head_dim == 128) return launch_prefill_variant<128>(a);
