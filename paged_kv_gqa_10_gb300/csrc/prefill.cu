@@ -553,36 +553,52 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         tc_fence_after();
         return true;
       };
-      for (;;) {
-        if (!(ok = mbar_wait(q_full, it & 1))) break;
-        const Item w = read_slot(slots + (it & 1) * 8);
+      // Items run back to back: the next item's S_X(0) takes the place of S_X(t+1)
+      // in the last key tile, so the tensor pipe does not drain between items.
+      Item w;
+      int ks, vs;
+      // the first item's S_A(0), S_B(0)
+      auto start_item = [&](Item& nw) {
+        if (!(ok = mbar_wait(q_full, it & 1))) return false;
+        nw = read_slot(slots + (it & 1) * 8);
         ++it;
-        if (w.ticket < 0) break;
         tc_fence_after();
-        const int nkt = w.nkt(), nkt_a = nkt;  // both tiles visit key tiles 0..t
-        int ks, vs;
-        if (!take(g++, ks)) break;  // K_0
-        if (!issue_s(0, ks)) break;
-        if (w.active_b && !issue_s(1, ks)) break;
+        return nw.ticket >= 0;
+      };
+      if (start_item(w) && take(g++, ks) && issue_s(0, ks) && (!w.active_b || issue_s(1, ks))) {
         umma_commit(&empty[ks]);
-        if (nkt == 1) umma_commit(q_empty);
-        for (int j = 0; j < nkt; ++j) {
-          const bool more = j + 1 < nkt;
-          if (!take(g++, vs)) break;  // V_j
-          if (j < nkt_a && !issue_pv(0, vs, j > 0)) break;
-          if (more) {
-            if (!take(g++, ks)) break;  // K_{j+1}
-            if (j + 1 < nkt_a && !issue_s(0, ks)) break;
+        if (w.nkt() == 1) umma_commit(q_empty);
+        for (;;) {
+          const int nkt = w.nkt();  // both tiles visit key tiles 0..t
+          Item nx;
+          bool nx_valid = false;
+          for (int j = 0; j < nkt; ++j) {
+            const bool more = j + 1 < nkt;
+            if (!take(g++, vs)) break;  // V_j
+            if (!issue_pv(0, vs, j > 0)) break;
+            if (more) {
+              if (!take(g++, ks)) break;  // K_{j+1}
+              if (!issue_s(0, ks)) break;
+            } else {  // the next item (its Q is out once this item's S are done)
+              nx_valid = start_item(nx);
+              if (!ok) break;
+              if (nx_valid && (!take(g++, ks) || !issue_s(0, ks))) break;
+            }
+            if (w.active_b && !issue_pv(1, vs, j > 0)) break;
+            if (more) {
+              if (w.active_b && !issue_s(1, ks)) break;
+              umma_commit(&empty[ks]);
+              if (j + 1 == nkt - 1) umma_commit(q_empty);
+            } else if (nx_valid) {
+              if (nx.active_b && !issue_s(1, ks)) break;
+              umma_commit(&empty[ks]);
+              if (nx.nkt() == 1) umma_commit(q_empty);
+            }
+            umma_commit(&empty[vs]);
           }
-          if (w.active_b && !issue_pv(1, vs, j > 0)) break;
-          umma_commit(&empty[vs]);
-          if (more) {
-            if (w.active_b && !issue_s(1, ks)) break;
-            umma_commit(&empty[ks]);
-            if (j + 1 == nkt - 1) umma_commit(q_empty);
-          }
+          if (!ok || !nx_valid) break;
+          w = nx;
         }
-        if (!ok) break;
       }
       if (!ok) record_status(p.dev_status, PGQA_ETIMEOUT);
     }
