@@ -50,7 +50,8 @@ namespace pgqa {
 namespace {
 
 constexpr int kNW = 4;  // consumer warps per CTA
-constexpr int kThreads = (kNW + 1) * 32;
+constexpr int kWarpProd = kNW, kWarpMerge = kNW + 1;
+constexpr int kThreads = (kNW + 2) * 32;
 constexpr int kMinChunk = 8;  // pages per CTA range, at least
 constexpr int kYRing = 256;   // TMA row coordinates fetched ahead of issue
 constexpr int kScanSlots = kThreads / 32 + 1;  // one per warp, then the found unit start
@@ -88,10 +89,11 @@ struct Cfg {
   static constexpr int kNkc = D / 16;              // 16-wide chunks of head_dim
   static constexpr int kRing = kStages * kStageBytes;
   static constexpr int kMerge = kNW * 8 * D * 4;   // per-warp O of one unit
-  static constexpr int kOffMerge = kRing;
-  static constexpr int kOffMl = kOffMerge + kMerge;                   // [kNW][8][2] float
-  static constexpr int kOffBar = kOffMl + kNW * 8 * 2 * 4;            // full[S], empty[S]
-  static constexpr int kOffMeta = kOffBar + 2 * kStages * 8;          // [S] int
+  static constexpr int kOffMerge = kRing;          // [2] by unit parity
+  static constexpr int kOffMl = kOffMerge + 2 * kMerge;               // [2][kNW][8][2] float
+  static constexpr int kOffBar = kOffMl + 2 * kNW * 8 * 2 * 4;        // full[S], empty[S],
+                                                                      // unit_done[2], merge_free[2]
+  static constexpr int kOffMeta = kOffBar + (2 * kStages + 4) * 8;    // [S] int
   static constexpr int kOffY = kOffMeta + kStages * 4;                // [kYRing] int
   static constexpr int kOffMisc = kOffY + kYRing * 4;                 // 32 ints, kScanSlots int64
   static constexpr int kSmem = 1024 + kOffMisc + 32 * 4 + kScanSlots * 8;
@@ -168,6 +170,149 @@ __device__ __forceinline__ void bar_consumers() {
   asm volatile("bar.sync 1, %0;" ::"n"(kNW * 32) : "memory");
 }
 
+// Unit epilogue, run by nt threads (t = this thread's index among them).
+// combine_unit: the consumer warps' states of unit w from the merge buffer (M = max m_w,
+// l = sum l_w 2^(m_w - M), O likewise) -> the output, or, for a unit cut by range
+// boundaries (nseg > 1), this CTA's partial.
+template <int D, bool kFp8>
+__device__ __forceinline__ void combine_unit(const DecodeParams& p, const Walk& w, int nseg,
+                                             int slot, const float* wob, const float* wmlb,
+                                             int t, int nt) {
+  const int G = p.group;
+  constexpr int kChunks = D / 8;  // 8 consecutive d per work item
+  const float vsc = kFp8 ? __ldg(p.v_scale + w.h) : 1.f;
+  for (int it = t; it < G * kChunks; it += nt) {
+    const int g = it / kChunks, cc = it % kChunks;
+    float M = -INFINITY;
+    bool poisoned = false;
+#pragma unroll
+    for (int ww = 0; ww < kNW; ++ww) {
+      M = fmaxf(M, wmlb[(ww * 8 + g) * 2]);
+      poisoned |= isnan(wmlb[(ww * 8 + g) * 2 + 1]);
+    }
+    float lsum = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ww = 0; ww < kNW; ++ww) {
+      const float mw = wmlb[(ww * 8 + g) * 2];
+      const float wt = mw == -INFINITY ? 0.f : ex2(mw - M);
+      lsum += wmlb[(ww * 8 + g) * 2 + 1] * wt;
+      const float4* src = reinterpret_cast<const float4*>(wob + (ww * 8 + g) * D + cc * 8);
+      const float4 x = src[0], y = src[1];
+      o[0] += x.x * wt; o[1] += x.y * wt; o[2] += x.z * wt; o[3] += x.w * wt;
+      o[4] += y.x * wt; o[5] += y.y * wt; o[6] += y.z * wt; o[7] += y.w * wt;
+    }
+    const float inv = 1.f / lsum;
+    const size_t row = static_cast<size_t>(w.b) * p.num_q_heads + w.h * G + g;
+    if (nseg == 1) {
+      uint4 pk = make_uint4(0, 0, 0, 0);
+      if (!poisoned) {
+        const float f = inv * vsc;
+        pk = make_uint4(pack_bf16(o[0] * f, o[1] * f), pack_bf16(o[2] * f, o[3] * f),
+                        pack_bf16(o[4] * f, o[5] * f), pack_bf16(o[6] * f, o[7] * f));
+      }
+      reinterpret_cast<uint4*>(p.out + row * D)[cc] = pk;
+      if (cc == 0 && p.lse) p.lse[row] = poisoned ? -INFINITY : (M + log2f(lsum)) * kLn2;
+    } else {
+      const size_t ps = (static_cast<size_t>(blockIdx.x) * 2 + slot) * 8 + g;
+      float4* dst = reinterpret_cast<float4*>(p.part_o + ps * D + cc * 8);
+      dst[0] = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
+      dst[1] = make_float4(o[4] * inv, o[5] * inv, o[6] * inv, o[7] * inv);
+      if (cc == 0) p.part_lse[ps] = poisoned ? INFINITY : M + log2f(lsum);
+    }
+  }
+}
+
+// merge_partials: the last of the unit's CTAs to arrive merges their partials.
+template <int D, bool kFp8>
+__device__ __forceinline__ void merge_partials(const DecodeParams& p, const Walk& w,
+                                               long long chunk, int t, int nt) {
+  const int G = p.group;
+  constexpr int kChunks = D / 8;
+  const float vsc = kFp8 ? __ldg(p.v_scale + w.h) : 1.f;
+  const long long c_first = w.S / chunk, c_last = (w.S + w.P - 1) / chunk;
+  for (int it = t; it < G * kChunks; it += nt) {
+    const int g = it / kChunks, cc = it % kChunks;
+    float M = -INFINITY;
+    bool any_bad = false;
+    for (long long cta = c_first; cta <= c_last; ++cta) {
+      const int sl = (w.S <= cta * chunk) ? 0 : 1;
+      const float ls = __ldcg(p.part_lse + (cta * 2 + sl) * 8 + g);
+      any_bad |= ls == INFINITY;
+      M = fmaxf(M, ls);
+    }
+    float lsum = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (!any_bad) {
+      for (long long cta = c_first; cta <= c_last; ++cta) {
+        const int sl = (w.S <= cta * chunk) ? 0 : 1;
+        const size_t ps = static_cast<size_t>(cta * 2 + sl) * 8 + g;
+        const float wt = ex2(__ldcg(p.part_lse + ps) - M);
+        lsum += wt;
+        const float4* src = reinterpret_cast<const float4*>(p.part_o + ps * D + cc * 8);
+        const float4 x = __ldcg(src), y = __ldcg(src + 1);
+        o[0] += x.x * wt; o[1] += x.y * wt; o[2] += x.z * wt; o[3] += x.w * wt;
+        o[4] += y.x * wt; o[5] += y.y * wt; o[6] += y.z * wt; o[7] += y.w * wt;
+      }
+    }
+    const size_t row = static_cast<size_t>(w.b) * p.num_q_heads + w.h * G + g;
+    uint4 pk = make_uint4(0, 0, 0, 0);
+    if (!any_bad) {
+      const float f = vsc / lsum;
+      pk = make_uint4(pack_bf16(o[0] * f, o[1] * f), pack_bf16(o[2] * f, o[3] * f),
+                      pack_bf16(o[4] * f, o[5] * f), pack_bf16(o[6] * f, o[7] * f));
+    }
+    reinterpret_cast<uint4*>(p.out + row * D)[cc] = pk;
+    if (cc == 0 && p.lse) p.lse[row] = any_bad ? -INFINITY : (M + log2f(lsum)) * kLn2;
+  }
+}
+
+// Segments of unit w over the CTA ranges, and which partial slot this CTA uses.
+__device__ __forceinline__ int unit_segments(const Walk& w, long long chunk) {
+  return static_cast<int>((w.S + w.P - 1) / chunk - w.S / chunk + 1);
+}
+
+// The merge warp: the epilogue of every unit of this CTA's range but the last (the
+// consumer warps, which have nothing left to stream then, do that one with 128
+// threads), so the consumers hand a unit over and go straight on to the next.
+template <int D, bool kFp8>
+__device__ __forceinline__ void merge_units(const DecodeParams& p, const Walk& w0, long long r0,
+                                            long long r1, long long chunk, const float* wo,
+                                            const float* wml, uint64_t* unit_done,
+                                            uint64_t* merge_free) {
+  const int lane = threadIdx.x & 31;
+  int cu = 0;
+  for (Walk w = w0;; ++cu) {
+    Walk wn = w;
+    wn.next(p);
+    if (!(wn.S < r1)) return;  // w is the range's last unit
+    const int mb = cu & 1;
+    if (!__all_sync(0xffffffffu, mbar_wait(&unit_done[mb], (cu >> 1) & 1))) {
+      if (lane == 0) record_status(p.dev_status, PGQA_ETIMEOUT);
+      return;
+    }
+    const int nseg = unit_segments(w, chunk);
+    combine_unit<D, kFp8>(p, w, nseg, w.S <= r0 ? 0 : 1, wo + mb * (kNW * 8 * D),
+                          wml + mb * (kNW * 8 * 2), lane, 32);
+    __syncwarp();  // every lane has read the buffer and issued its writes
+    if (lane == 0) mbar_arrive(&merge_free[mb]);
+    if (nseg > 1) {
+      unsigned last = 0;
+      if (lane == 0) {
+        __threadfence();
+        // atomicInc wraps to 0 on the last arrival, leaving the ticket ready for the next call
+        const unsigned prev = atomicInc(
+            reinterpret_cast<unsigned*>(p.counters + w.b * p.num_kv_heads + w.h),
+            static_cast<unsigned>(nseg - 1));
+        last = prev == static_cast<unsigned>(nseg - 1);
+      }
+      if (__shfl_sync(0xffffffffu, last, 0)) {
+        __threadfence();
+        merge_partials<D, kFp8>(p, w, chunk, lane, 32);
+      }
+    }
+    w = wn;
+  }
+}
+
 template <int D, bool kFp8>
 __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_decode_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -180,9 +325,11 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* ring = smem;
   float* wo = reinterpret_cast<float*>(smem + C::kOffMerge);  // [kNW][8][D]
-  float* wml = reinterpret_cast<float*>(smem + C::kOffMl);    // [kNW][8][2] (m, l) base 2
+  float* wml = reinterpret_cast<float*>(smem + C::kOffMl);    // [2][kNW][8][2] (m, l) base 2
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* empty = full + S;
+  uint64_t* unit_done = empty + S;       // [2] the consumer warps' states of a unit are in
+  uint64_t* merge_free = unit_done + 2;  // [2] the merge warp has read them
   int* meta = reinterpret_cast<int*>(smem + C::kOffMeta);  // per stage: bad block id seen
   int* yring = reinterpret_cast<int*>(smem + C::kOffY);    // row coordinate of page i % kYRing
   int* misc = reinterpret_cast<int*>(smem + C::kOffMisc);
@@ -243,12 +390,16 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&unit_done[s], kNW);
+      mbar_init(&merge_free[s], 1);
+    }
     fence_mbar_init();
   }
   __syncthreads();
 
   // ================================================================ producer
-  if (warp == kNW) {
+  if (warp == kWarpProd) {
     if (lane == 0) {
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
@@ -332,6 +483,12 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
     return;
   }
 
+  // ================================================================ merge warp
+  if (warp == kWarpMerge) {
+    merge_units<D, kFp8>(p, w0, r0, r1, chunk, wo, wml, unit_done, merge_free);
+    return;
+  }
+
   // ================================================================ consumers
   const int gid = lane >> 2, tig = lane & 3;
   const uint32_t rowK = (lane & 7) + (((lane >> 3) & 1) << 3);
@@ -340,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
   const uint32_t cV = (lane >> 3) & 1;
   bool alive = true;  // false once one of this warp's waits gave up
   int i_base = 0;     // CTA-local index of the unit's first page
+  int cu = 0;         // units of this CTA done so far
   // raw query words of a unit, column n = query head gid of the group:
   //   bf16: the two B-fragment registers per 16-wide chunk as stored;
   //   E4M3: k index 2tig+{0,1} <-> d = 16kc + 4tig + {0,1}; 2tig+8+{0,1} <-> +{2,3}
@@ -506,13 +664,21 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
     }
     i_base += npg;
 
-    // ---- this warp's state for the unit -> shared memory
+    // ---- this warp's state for the unit -> the merge buffer of the unit's parity;
+    //      the merge warp takes it from there and this warp goes on to the next unit
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
       l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], o);
       l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], o);
     }
     const bool poisoned_w = __any_sync(0xffffffffu, bad != 0) || !__all_sync(0xffffffffu, alive);
+    const int mb = cu & 1;
+    if (cu >= 2 && !__all_sync(0xffffffffu, mbar_wait(&merge_free[mb], ((cu >> 1) - 1) & 1))) {
+      alive = false;
+      if (lane == 0) record_status(p.dev_status, PGQA_ETIMEOUT);
+    }
+    float* wob = wo + mb * (kNW * 8 * D);
+    float* wmlb = wml + mb * (kNW * 8 * 2);
 #pragma unroll
     for (int dc = 0; dc < C::kNkc; ++dc) {
       int d0, d1;
@@ -523,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
         d0 = 16 * gid + 2 * dc;
         d1 = d0 + 1;
       }
-      float* o0 = wo + (warp * 8 + 2 * tig) * D;
+      float* o0 = wob + (warp * 8 + 2 * tig) * D;
       float* o1 = o0 + D;
       o0[d0] = acc[dc][0];
       o1[d0] = acc[dc][1];
@@ -531,108 +697,40 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
       o1[d1] = acc[dc][3];
     }
     if (gid == 0) {
-      float* ml = wml + (warp * 8 + 2 * tig) * 2;
+      float* ml = wmlb + (warp * 8 + 2 * tig) * 2;
       ml[0] = m_run[0];
       ml[1] = poisoned_w ? NAN : l_run[0];  // NaN l marks a poisoned warp state
       ml[2] = m_run[1];
       ml[3] = poisoned_w ? NAN : l_run[1];
     }
-    bar_consumers();
-
-    // ---- combine the warps: M = max m_w, l = sum l_w 2^(m_w - M), O likewise
-    const int u = w.b * Hkv + w.h;
-    const long long c_first = w.S / chunk, c_last = (w.S + w.P - 1) / chunk;
-    const int nseg = static_cast<int>(c_last - c_first + 1);
-    const int slot = (w.S <= r0) ? 0 : 1;  // 0: this unit is the first of this CTA's range
-    const float vsc = kFp8 ? __ldg(p.v_scale + w.h) : 1.f;
-    constexpr int kChunks = D / 8;  // 8 consecutive d per work item
-    for (int it = tid; it < G * kChunks; it += kNW * 32) {
-      const int g = it / kChunks, cc = it % kChunks;
-      float M = -INFINITY;
-      bool poisoned = false;
-#pragma unroll
-      for (int ww = 0; ww < kNW; ++ww) {
-        M = fmaxf(M, wml[(ww * 8 + g) * 2]);
-        poisoned |= isnan(wml[(ww * 8 + g) * 2 + 1]);
-      }
-      float lsum = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int ww = 0; ww < kNW; ++ww) {
-        const float mw = wml[(ww * 8 + g) * 2];
-        const float wt = mw == -INFINITY ? 0.f : ex2(mw - M);
-        lsum += wml[(ww * 8 + g) * 2 + 1] * wt;
-        const float4* src = reinterpret_cast<const float4*>(wo + (ww * 8 + g) * D + cc * 8);
-        const float4 x = src[0], y = src[1];
-        o[0] += x.x * wt; o[1] += x.y * wt; o[2] += x.z * wt; o[3] += x.w * wt;
-        o[4] += y.x * wt; o[5] += y.y * wt; o[6] += y.z * wt; o[7] += y.w * wt;
-      }
-      const float inv = 1.f / lsum;
-      const size_t row = static_cast<size_t>(w.b) * p.num_q_heads + w.h * G + g;
-      if (nseg == 1) {
-        uint4 pk = make_uint4(0, 0, 0, 0);
-        if (!poisoned) {
-          const float f = inv * vsc;
-          pk = make_uint4(pack_bf16(o[0] * f, o[1] * f), pack_bf16(o[2] * f, o[3] * f),
-                          pack_bf16(o[4] * f, o[5] * f), pack_bf16(o[6] * f, o[7] * f));
-        }
-        reinterpret_cast<uint4*>(p.out + row * D)[cc] = pk;
-        if (cc == 0 && p.lse) p.lse[row] = poisoned ? -INFINITY : (M + log2f(lsum)) * kLn2;
-      } else {
-        const size_t ps = (static_cast<size_t>(c) * 2 + slot) * 8 + g;
-        float4* dst = reinterpret_cast<float4*>(p.part_o + ps * D + cc * 8);
-        dst[0] = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
-        dst[1] = make_float4(o[4] * inv, o[5] * inv, o[6] * inv, o[7] * inv);
-        if (cc == 0) p.part_lse[ps] = poisoned ? INFINITY : M + log2f(lsum);
-      }
+    __syncwarp();
+    Walk wn = w;
+    wn.next(p);
+    if (wn.S < r1) {  // the merge warp takes the unit
+      if (lane == 0) mbar_arrive(&unit_done[mb]);
+      ++cu;
+      continue;
     }
-    bar_consumers();  // merge buffers free; this CTA's partial writes are issued
+    // the range's last unit: nothing left to stream, so the consumer warps finish it
+    const int nseg = unit_segments(w, chunk);
+    bar_consumers();
+    combine_unit<D, kFp8>(p, w, nseg, w.S <= r0 ? 0 : 1, wob, wmlb, tid, kNW * 32);
     if (nseg > 1) {
+      bar_consumers();  // this CTA's partial writes are issued
       if (tid == 0) {
         __threadfence();
         // atomicInc wraps to 0 on the last arrival, leaving the ticket ready for the next call
-        const unsigned prev = atomicInc(reinterpret_cast<unsigned*>(p.counters + u),
+        const unsigned prev = atomicInc(reinterpret_cast<unsigned*>(p.counters + w.b * Hkv + w.h),
                                         static_cast<unsigned>(nseg - 1));
         misc[1] = prev == static_cast<unsigned>(nseg - 1);
       }
       bar_consumers();
       if (misc[1]) {
         __threadfence();
-        for (int it = tid; it < G * kChunks; it += kNW * 32) {
-          const int g = it / kChunks, cc = it % kChunks;
-          float M = -INFINITY;
-          bool any_bad = false;
-          for (long long cta = c_first; cta <= c_last; ++cta) {
-            const int sl = (w.S <= cta * chunk) ? 0 : 1;
-            const float ls = __ldcg(p.part_lse + (cta * 2 + sl) * 8 + g);
-            any_bad |= ls == INFINITY;
-            M = fmaxf(M, ls);
-          }
-          float lsum = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          if (!any_bad) {
-            for (long long cta = c_first; cta <= c_last; ++cta) {
-              const int sl = (w.S <= cta * chunk) ? 0 : 1;
-              const size_t ps = static_cast<size_t>(cta * 2 + sl) * 8 + g;
-              const float wt = ex2(__ldcg(p.part_lse + ps) - M);
-              lsum += wt;
-              const float4* src = reinterpret_cast<const float4*>(p.part_o + ps * D + cc * 8);
-              const float4 x = __ldcg(src), y = __ldcg(src + 1);
-              o[0] += x.x * wt; o[1] += x.y * wt; o[2] += x.z * wt; o[3] += x.w * wt;
-              o[4] += y.x * wt; o[5] += y.y * wt; o[6] += y.z * wt; o[7] += y.w * wt;
-            }
-          }
-          const size_t row = static_cast<size_t>(w.b) * p.num_q_heads + w.h * G + g;
-          uint4 pk = make_uint4(0, 0, 0, 0);
-          if (!any_bad) {
-            const float f = vsc / lsum;
-            pk = make_uint4(pack_bf16(o[0] * f, o[1] * f), pack_bf16(o[2] * f, o[3] * f),
-                            pack_bf16(o[4] * f, o[5] * f), pack_bf16(o[6] * f, o[7] * f));
-          }
-          reinterpret_cast<uint4*>(p.out + row * D)[cc] = pk;
-          if (cc == 0 && p.lse) p.lse[row] = any_bad ? -INFINITY : (M + log2f(lsum)) * kLn2;
-        }
+        merge_partials<D, kFp8>(p, w, chunk, tid, kNW * 32);
       }
-      bar_consumers();  // misc[1] is rewritten for the next unit
     }
+    ++cu;
   }
 }
 
