@@ -338,6 +338,11 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, ncta = gridDim.x;
   const int G = p.group, Hkv = p.num_kv_heads, B = p.num_seqs;
+  if (warp == kWarpProd && lane == 0) {
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+  }
+  grid_dependency_wait();  // the stream's previous kernel (e.g. the KV append) is done
 
   // ---- the global page order holds N pages; this CTA owns [r0, r1)
   long long local = 0;
@@ -400,10 +405,6 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
 
   // ================================================================ producer
   if (warp == kWarpProd) {
-    if (lane == 0) {
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-    }
     const int n = static_cast<int>(r1 - r0);  // pages of this CTA, CTA-local index 0..n-1
     Walk fw = w0;                             // fetch cursor: unit and page within it
     int fpg = static_cast<int>(r0 - w0.S);
@@ -769,7 +770,9 @@ pgqa_status_t launch_variant(const DecodeArgs& a, const DecodePlan& plan) {
   p.num_blocks = a.num_blocks;
   p.max_context_len = a.max_context_len;
   p.scale_log2 = a.scale * kLog2e;
-  paged_decode_kernel<D, kFp8><<<plan.grid, kThreads, C::kSmem, a.stream>>>(kmap, vmap, p);
+  if (launch_after_previous(paged_decode_kernel<D, kFp8>, dim3(plan.grid), dim3(kThreads),
+                            C::kSmem, a.stream, kmap, vmap, p) != cudaSuccess)
+    return PGQA_ECUDA;
   return cudaPeekAtLastError() == cudaSuccess ? PGQA_OK : PGQA_ECUDA;
 }
 

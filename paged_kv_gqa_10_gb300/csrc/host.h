@@ -30,6 +30,24 @@ int num_sms_current_device();
 // (once per device and kernel). Returns false if the runtime refuses.
 bool smem_attr_ready(const void* kernel, int bytes);
 
+// Launches `kernel` with programmatic stream serialization: it may be scheduled while
+// the stream's previous kernel runs, and waits for it in grid_dependency_wait().
+template <typename... Params, typename... Args>
+cudaError_t launch_after_previous(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                                  cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ----------------------------------------------------------- launchers
 
 pgqa_status_t launch_kv_cache_write(const void* key, const void* value,

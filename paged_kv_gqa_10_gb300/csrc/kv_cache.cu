@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(256) kv_cache_write_kernel(
     const int64_t* __restrict__ slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
     void* __restrict__ k_cache, void* __restrict__ v_cache, int num_blocks, int block_size,
     const float* __restrict__ k_scale, const float* __restrict__ v_scale, int* dev_status) {
+  grid_launch_dependents();  // a following attention kernel may get its CTAs in place now
   const int vecs = head_dim / 8;  // 16-byte input vectors per (token, head) row
   const int64_t total = static_cast<int64_t>(num_tokens) * num_kv_heads * vecs;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;

@@ -295,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, ncta = gridDim.x;
+  grid_dependency_wait();  // the stream's previous kernel (e.g. the KV scatter) is done
 
   // length errors: reported once per sequence, by CTA 0
   if (c == 0) {
@@ -799,7 +800,9 @@ pgqa_status_t launch_prefill_variant(const PrefillArgs& a) {
   p.scale_log2 = a.scale * kLog2e;
   const long long items = static_cast<long long>(p.n_levels) * a.num_seqs * p.pairs;
   const int grid = static_cast<int>(items < sms ? items : sms);
-  paged_prefill_kernel<D><<<grid, kThreads, C::kSmem, a.stream>>>(qmap, kmap, vmap, p);
+  if (launch_after_previous(paged_prefill_kernel<D>, dim3(grid), dim3(kThreads), C::kSmem,
+                            a.stream, qmap, kmap, vmap, p) != cudaSuccess)
+    return PGQA_ECUDA;
   return cudaPeekAtLastError() == cudaSuccess ? PGQA_OK : PGQA_ECUDA;
 }
 

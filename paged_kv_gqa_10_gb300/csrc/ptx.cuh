@@ -29,6 +29,19 @@ __device__ __forceinline__ void record_status(int* dev_status, int code) {
   if (dev_status != nullptr) atomicCAS(dev_status, 0, code);
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while the
+// previous kernel of the stream is still running; it must not touch global memory
+// before grid_dependency_wait(), which returns once that kernel has finished and its
+// writes are visible (at once when there is no such kernel).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel of the stream (if launched as above) start now.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
