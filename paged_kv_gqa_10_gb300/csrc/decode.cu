@@ -84,7 +84,8 @@ struct Cfg {
   static constexpr int kSub = kRowBytes / 128;     // 128-byte TMA boxes per row
   static constexpr int kPageBytes = 16 * kRowBytes;
   static constexpr int kStageBytes = 2 * kPageBytes;  // K page + V page
-  static constexpr int kStagesPerWarp = kFp8 ? 3 : 2;
+  // about 16 KB of pages in flight per consumer warp
+  static constexpr int kStagesPerWarp = kStageBytes >= 8192 ? 2 : 16384 / kStageBytes;
   static constexpr int kStages = kNW * kStagesPerWarp;
   static constexpr int kNkc = D / 16;              // 16-wide chunks of head_dim
   static constexpr int kRing = kStages * kStageBytes;
