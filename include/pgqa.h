@@ -261,6 +261,35 @@ pgqa_status_t pgqa_paged_prefill_varlen(void* out, float* lse, const void* q, in
                                         void* workspace, size_t workspace_bytes,
                                         int* dev_status, void* stream);
 
+/*
+ * Chunked prefill over a cached prefix: the varlen call of the rkmt.cn article,
+ * sec. 2.4, with separate query and key lengths (its cu_seqlens_q / cu_seqlens_k),
+ * keys read through the block tables of sec. 3.1. Sequence i's new tokens (its
+ * chunk, cu_seqlens_q[i] .. cu_seqlens_q[i+1]-1, Lq of them) are the last Lq of the
+ * Lk = seq_lens_k[i] tokens in its cache, so chunk position p attends to keys
+ * 0 .. Lk-Lq+p (bottom-right causal alignment; Lk = Lq is
+ * pgqa_paged_prefill_varlen). The chunk's own K/V must already be in the cache
+ * (pgqa_kv_cache_write). Speculative verification (a few draft tokens per
+ * sequence) is the case Lq = 2..6.
+ *
+ *   cu_seqlens_q  [num_seqs + 1] int32, read: the chunks in q / out / lse.
+ *   seq_lens_k    [num_seqs] int32, read: Lk per sequence, Lq <= Lk <= max_seqlen_k.
+ *   max_seqlen_q  an upper bound on the chunk lengths (at most 262144).
+ *   max_seqlen_k  an upper bound on Lk (at most 2^26).
+ * Every other argument, the workspace and the error behaviour are as for
+ * pgqa_paged_prefill_varlen; a sequence with Lk < Lq, Lk above max_seqlen_k or
+ * beyond its block table is a device error (PGQA_EINVAL).
+ */
+pgqa_status_t pgqa_paged_prefill_varlen_kv(void* out, float* lse, const void* q, int num_tokens,
+                                           const void* k_cache, const void* v_cache,
+                                           const int32_t* block_tables, int max_blocks_per_seq,
+                                           const int32_t* cu_seqlens_q, const int32_t* seq_lens_k,
+                                           int num_seqs, int max_seqlen_q, int max_seqlen_k,
+                                           int num_q_heads, int num_kv_heads, int head_dim,
+                                           int num_blocks, int block_size, float scale,
+                                           void* workspace, size_t workspace_bytes,
+                                           int* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

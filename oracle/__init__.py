@@ -43,6 +43,9 @@ def _bind(path):
     lib.oracle_paged_prefill.argtypes = [P, P, P, I, P, P, P, I, P, I, I, I, I, I, I, D, P, I64,
                                          P, P, I]
     lib.oracle_paged_prefill.restype = I
+    lib.oracle_paged_prefill_kv.argtypes = [P, P, P, I, P, P, P, I, P, P, I, I, I, I, I, I, D, P,
+                                            I64, P, P, I]
+    lib.oracle_paged_prefill_kv.restype = I
     lib.oracle_dense_row.argtypes = [P, P, P, I, I, D, P, P]
     lib.oracle_dense_row.restype = None
     lib.oracle_has_openmp.argtypes = []
@@ -198,6 +201,33 @@ def paged_prefill(q, k_cache, v_cache, block_tables, cu_seqlens, scale, rows=Non
                                       bs, float(scale), _ptr(r), n_rows, _ptr(out), _ptr(lse),
                                       threads or default_threads())
     _check(rc, "paged_prefill")
+    return out, lse
+
+
+def paged_prefill_kv(q, k_cache, v_cache, block_tables, cu_seqlens_q, seq_lens_k, scale,
+                     rows=None, dtype=BF16, k_scale=None, v_scale=None, threads=None):
+    """Chunked prefill over a cached prefix: sequence i's chunk (cu_seqlens_q) is the
+    last Lq of its seq_lens_k[i] cached tokens; query i of a chunk sees keys
+    0..Lk-Lq+i. rows: optional int array [n, 2] of (token, q_head).
+    Returns (out [T, Hq, D], lse [T, Hq]) float64; rows not computed stay NaN."""
+    q = _np(q, np.uint16)
+    elem = np.uint16 if dtype == BF16 else np.uint8
+    kc, vc = _np(k_cache, elem), _np(v_cache, elem)
+    bt, cu = _np(block_tables, np.int32), _np(cu_seqlens_q, np.int32)
+    lk = _np(seq_lens_k, np.int32)
+    ks = None if k_scale is None else _np(k_scale, np.float32)
+    vs = None if v_scale is None else _np(v_scale, np.float32)
+    T, Hq, D = q.shape
+    NB, Hkv, bs, _ = kc.shape
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, np.int32).reshape(-1, 2))
+    n_rows = 0 if r is None else r.shape[0]
+    out = np.full((T, Hq, D), np.nan, np.float64)
+    lse = np.full((T, Hq), np.nan, np.float64)
+    rc = _load().oracle_paged_prefill_kv(_ptr(q), _ptr(kc), _ptr(vc), dtype, _ptr(ks), _ptr(vs),
+                                         _ptr(bt), bt.shape[1], _ptr(cu), _ptr(lk), len(cu) - 1,
+                                         Hq, Hkv, D, NB, bs, float(scale), _ptr(r), n_rows,
+                                         _ptr(out), _ptr(lse), threads or default_threads())
+    _check(rc, "paged_prefill_kv")
     return out, lse
 
 

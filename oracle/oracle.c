@@ -37,6 +37,11 @@
  *    (and the fp8 K scale); an empty context gives out = 0, lse = -inf.
  *  - Causal prefill without a cached prefix: query position p of a sequence
  *    sees keys 0..p of the same sequence.
+ *  - Prefill over a cached prefix ([P1] sec. 2.4 passes separate cumulative
+ *    lengths for queries and keys): a chunk of Lq new tokens of a sequence whose
+ *    cache holds Lk >= Lq tokens (the chunk's own tokens last) sits at the end of
+ *    the sequence, so query i of the chunk (0-based) sees keys 0..Lk-Lq+i
+ *    (bottom-right causal alignment); Lk = Lq is the prefill above.
  *  - FP8 cache: stored code = E4M3_rne_satfinite(float(x) / float(scale_h)),
  *    the division done in binary32 (the precision the GPU kernel decides the
  *    code in); dequantised value = E4M3 value * scale_h.
@@ -309,6 +314,72 @@ int oracle_paged_prefill(const uint16_t* q, const void* k_cache, const void* v_c
         while (cu_seqlens[i + 1] <= t) ++i; /* the sequence that owns token t */
         p = (int)(t - cu_seqlens[i]);        /* its position in that sequence */
         L = p + 1;                           /* causal: keys 0..p */
+        h = hq / G;
+        K = (double*)malloc(sizeof(double) * (size_t)L * D);
+        V = (double*)malloc(sizeof(double) * (size_t)L * D);
+        qd = (double*)malloc(sizeof(double) * D);
+        scores = (double*)malloc(sizeof(double) * (size_t)L);
+        rc = oracle_gather_kv(k_cache, v_cache, dtype, k_scale, v_scale,
+                              block_tables + (size_t)i * max_blocks_per_seq, max_blocks_per_seq, L,
+                              h, Hkv, D, num_blocks, block_size, K, V);
+        if (rc != ORACLE_OK) {
+#pragma omp critical
+            status = rc;
+        } else {
+            const uint16_t* qrow = q + ((size_t)t * Hq + hq) * D;
+            for (int d = 0; d < D; ++d) qd[d] = oracle_bf16_to_f64(qrow[d]);
+            attend_row(qd, K, V, L, D, scale, scores, out + ((size_t)t * Hq + hq) * D,
+                       lse + (size_t)t * Hq + hq);
+        }
+        free(K);
+        free(V);
+        free(qd);
+        free(scores);
+    }
+    return status;
+}
+
+/* Chunked prefill over a cached prefix: as oracle_paged_prefill, with seq_lens_k[i]
+ * (>= the chunk's length Lq) the number of tokens sequence i has in the cache,
+ * the chunk's tokens last; query i of the chunk sees keys 0..Lk-Lq+i ([P1] sec. 2.4,
+ * the varlen call with separate query and key lengths; bottom-right alignment). */
+int oracle_paged_prefill_kv(const uint16_t* q, const void* k_cache, const void* v_cache,
+                            int dtype, const float* k_scale, const float* v_scale,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* cu_seqlens_q, const int32_t* seq_lens_k, int num_seqs,
+                            int Hq, int Hkv, int D, int num_blocks, int block_size, double scale,
+                            const int32_t* rows, int64_t n_rows, double* out, double* lse,
+                            int nthreads) {
+    int G, status = ORACLE_OK;
+    int64_t T, n_items;
+    if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || block_size <= 0)
+        return ORACLE_EINVAL;
+    if (dtype == ORACLE_E4M3 && (!k_scale || !v_scale)) return ORACLE_EINVAL;
+    if (num_seqs > 0 && cu_seqlens_q[0] != 0) return ORACLE_EINVAL;
+    for (int i = 0; i < num_seqs; ++i)
+        if (cu_seqlens_q[i + 1] < cu_seqlens_q[i] ||
+            seq_lens_k[i] < cu_seqlens_q[i + 1] - cu_seqlens_q[i])
+            return ORACLE_EINVAL;
+    G = Hq / Hkv;
+    T = num_seqs > 0 ? cu_seqlens_q[num_seqs] : 0;
+    n_items = rows ? n_rows : T * Hq;
+    (void)nthreads;
+#pragma omp parallel for schedule(dynamic, 4) num_threads(nthreads > 0 ? nthreads : 1)
+    for (int64_t it = 0; it < n_items; ++it) {
+        int64_t t = rows ? rows[2 * it] : it / Hq;
+        int hq = rows ? rows[2 * it + 1] : (int)(it % Hq);
+        int i = 0, p, L, h, rc, Lq, Lk;
+        double *K, *V, *qd, *scores;
+        if (t < 0 || t >= T || hq < 0 || hq >= Hq) {
+#pragma omp critical
+            status = ORACLE_EINVAL;
+            continue;
+        }
+        while (cu_seqlens_q[i + 1] <= t) ++i; /* the sequence that owns token t */
+        p = (int)(t - cu_seqlens_q[i]);        /* its position in the chunk */
+        Lq = cu_seqlens_q[i + 1] - cu_seqlens_q[i];
+        Lk = seq_lens_k[i];
+        L = Lk - Lq + p + 1; /* keys 0..Lk-Lq+p */
         h = hq / G;
         K = (double*)malloc(sizeof(double) * (size_t)L * D);
         V = (double*)malloc(sizeof(double) * (size_t)L * D);

@@ -67,6 +67,8 @@ def _load():
         "pgqa_prefill_workspace_size": ([I, I, I], SZ),
         "pgqa_paged_prefill_varlen": ([P, P, P, I, P, P, P, I, P, I, I, I, I, I, I, I, F, P,
                                        SZ, P, P], I),
+        "pgqa_paged_prefill_varlen_kv": ([P, P, P, I, P, P, P, I, P, P, I, I, I, I, I, I, I, I,
+                                          F, P, SZ, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -280,3 +282,31 @@ def paged_prefill_varlen(out, lse, q, k_cache, v_cache, block_tables, cu_seqlens
         block_tables.shape[1], _ptr(cu_seqlens), S, int(max_seqlen), Hq, Hkv, D, NB, bs,
         float(scale), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
     _check(rc, "paged_prefill_varlen")
+
+
+def paged_prefill_varlen_kv(out, lse, q, k_cache, v_cache, block_tables, cu_seqlens_q, seq_lens_k,
+                            max_seqlen_q, max_seqlen_k, scale, workspace=None, dev_status=None,
+                            stream=None):
+    """Prefill over a cached prefix: each sequence's chunk (cu_seqlens_q) is the last
+    Lq of its seq_lens_k cached tokens. out [T, Hq, D] bf16 and lse [T, Hq] fp32 (or
+    None) are written."""
+    _dev(out, "out", torch.bfloat16)
+    _dev(lse, "lse", torch.float32)
+    _dev(q, "q", torch.bfloat16)
+    _dev(k_cache, "k_cache", torch.bfloat16)
+    _dev(v_cache, "v_cache", torch.bfloat16)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    _dev(seq_lens_k, "seq_lens_k", torch.int32)
+    _dev(workspace, "workspace")
+    _dev(dev_status, "dev_status", torch.int32)
+    T, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    S = cu_seqlens_q.shape[0] - 1
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = _handle().pgqa_paged_prefill_varlen_kv(
+        _ptr(out), _ptr(lse), _ptr(q), T, _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(cu_seqlens_q), _ptr(seq_lens_k), S, int(max_seqlen_q),
+        int(max_seqlen_k), Hq, Hkv, D, NB, bs, float(scale), _ptr(workspace), ws_bytes,
+        _ptr(dev_status), _stream(stream))
+    _check(rc, "paged_prefill_varlen_kv")

@@ -335,15 +335,16 @@ size_t pgqa_prefill_workspace_size(int num_seqs, int num_q_heads, int max_seqlen
   return pgqa::kPrefillWorkspaceBytes;
 }
 
-pgqa_status_t pgqa_paged_prefill_varlen(void* out, float* lse, const void* q, int num_tokens,
-                                        const void* k_cache, const void* v_cache,
-                                        const int32_t* block_tables, int max_blocks_per_seq,
-                                        const int32_t* cu_seqlens, int num_seqs, int max_seqlen,
-                                        int num_q_heads, int num_kv_heads, int head_dim,
-                                        int num_blocks, int block_size, float scale,
-                                        void* workspace, size_t workspace_bytes,
-                                        int* dev_status, void* stream) {
-  if (num_seqs < 0 || max_seqlen < 0 || num_tokens < 0 || num_q_heads <= 0 ||
+// Shared by both prefill entry points (seq_lens_k null: no cached prefix).
+static pgqa_status_t prefill_call(void* out, float* lse, const void* q, int num_tokens,
+                                  const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, int max_blocks_per_seq,
+                                  const int32_t* cu_seqlens, const int32_t* seq_lens_k,
+                                  int num_seqs, int max_seqlen, int max_seqlen_k,
+                                  int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
+                                  int block_size, float scale, void* workspace,
+                                  size_t workspace_bytes, int* dev_status, void* stream) {
+  if (num_seqs < 0 || max_seqlen < 0 || max_seqlen_k < 0 || num_tokens < 0 || num_q_heads <= 0 ||
       num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || block_size <= 0 ||
       max_blocks_per_seq < 0 || !isfinite(scale) || !(scale > 0.f))
     return PGQA_EINVAL;
@@ -351,7 +352,8 @@ pgqa_status_t pgqa_paged_prefill_varlen(void* out, float* lse, const void* q, in
   if (head_dim != 128 && head_dim != 64) return PGQA_EUNSUPPORTED;
   if (block_size != 16) return PGQA_EUNSUPPORTED;
   if (static_cast<int64_t>(num_blocks) * num_kv_heads * 16 > INT32_MAX) return PGQA_EUNSUPPORTED;
-  if (num_seqs > pgqa::prefill_max_seqs() || max_seqlen > pgqa::prefill_max_seqlen())
+  if (num_seqs > pgqa::prefill_max_seqs() || max_seqlen > pgqa::prefill_max_seqlen() ||
+      max_seqlen_k > (1 << 26))
     return PGQA_EUNSUPPORTED;
   if (num_seqs == 0 || max_seqlen == 0 || num_tokens == 0) return PGQA_OK;
   if (workspace == nullptr || workspace_bytes < pgqa::kPrefillWorkspaceBytes)
@@ -369,6 +371,8 @@ pgqa_status_t pgqa_paged_prefill_varlen(void* out, float* lse, const void* q, in
   a.block_tables = block_tables;
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.cu_seqlens = cu_seqlens;
+  a.seq_lens_k = seq_lens_k;
+  a.max_seqlen_k = max_seqlen_k;
   a.workspace = workspace;
   a.num_tokens = num_tokens;
   a.num_seqs = num_seqs;
@@ -382,6 +386,36 @@ pgqa_status_t pgqa_paged_prefill_varlen(void* out, float* lse, const void* q, in
   a.dev_status = dev_status;
   a.stream = static_cast<cudaStream_t>(stream);
   return pgqa::launch_paged_prefill(a);
+}
+
+pgqa_status_t pgqa_paged_prefill_varlen(void* out, float* lse, const void* q, int num_tokens,
+                                        const void* k_cache, const void* v_cache,
+                                        const int32_t* block_tables, int max_blocks_per_seq,
+                                        const int32_t* cu_seqlens, int num_seqs, int max_seqlen,
+                                        int num_q_heads, int num_kv_heads, int head_dim,
+                                        int num_blocks, int block_size, float scale,
+                                        void* workspace, size_t workspace_bytes,
+                                        int* dev_status, void* stream) {
+  return prefill_call(out, lse, q, num_tokens, k_cache, v_cache, block_tables,
+                      max_blocks_per_seq, cu_seqlens, nullptr, num_seqs, max_seqlen, max_seqlen,
+                      num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale,
+                      workspace, workspace_bytes, dev_status, stream);
+}
+
+pgqa_status_t pgqa_paged_prefill_varlen_kv(void* out, float* lse, const void* q, int num_tokens,
+                                           const void* k_cache, const void* v_cache,
+                                           const int32_t* block_tables, int max_blocks_per_seq,
+                                           const int32_t* cu_seqlens_q, const int32_t* seq_lens_k,
+                                           int num_seqs, int max_seqlen_q, int max_seqlen_k,
+                                           int num_q_heads, int num_kv_heads, int head_dim,
+                                           int num_blocks, int block_size, float scale,
+                                           void* workspace, size_t workspace_bytes,
+                                           int* dev_status, void* stream) {
+  if (seq_lens_k == nullptr && num_seqs > 0) return PGQA_EINVAL;
+  return prefill_call(out, lse, q, num_tokens, k_cache, v_cache, block_tables,
+                      max_blocks_per_seq, cu_seqlens_q, seq_lens_k, num_seqs, max_seqlen_q,
+                      max_seqlen_k, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                      scale, workspace, workspace_bytes, dev_status, stream);
 }
 
 }  // extern "C"

@@ -105,6 +105,8 @@ struct PrefillArgs {
   const int32_t* block_tables;
   int max_blocks_per_seq;
   const int32_t* cu_seqlens;
+  const int32_t* seq_lens_k;  // cached tokens per sequence, or null (no cached prefix)
+  int max_seqlen_k;
   void* workspace;  // >= prefill_workspace_bytes(), zero before first use
   int num_tokens;
   int num_seqs, max_seqlen, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size;

@@ -1,19 +1,22 @@
 // Causal variable-length prefill over the paged KV cache, on the tcgen05 tensor
 // cores (sm_103a).
 //
-// Computes, for every sequence i (tokens cu_seqlens[i] .. cu_seqlens[i+1]-1), query
-// head hq and position p, softmax(scale * q_p K^T) V over keys 0..p of sequence i,
-// read through its block table, and lse = ln sum exp(score): the varlen, causal
-// call of the rkmt.cn article (sec. 2.4) over the paged cache of its sec. 3.1, with
-// the attention steps of "LLaMA structure and inference performance" (sec. 3.1) and
-// repeat_kv as the index map kv_head = hq / G (sec. 2.1). FlashAttention-style
-// online softmax over 128-key tiles; the full score matrix is never formed.
+// Computes, for every sequence i (new tokens cu_seqlens[i] .. cu_seqlens[i+1]-1),
+// query head hq and chunk position p, softmax(scale * q_p K^T) V over keys
+// 0..Lk-Lq+p of sequence i, read through its block table, and lse = ln sum
+// exp(score): the varlen, causal call of the rkmt.cn article (sec. 2.4), with
+// separate query and key lengths (the chunk is the last Lq of the Lk cached tokens,
+// bottom-right alignment; Lk = Lq without a cached prefix), over the paged cache of
+// its sec. 3.1, with the attention steps of "LLaMA structure and inference
+// performance" (sec. 3.1) and repeat_kv as the index map kv_head = hq / G (sec. 2.1).
+// FlashAttention-style online softmax over 128-key tiles; the full score matrix is
+// never formed.
 //
 // Work and scheduling
 //  - A work item is one 128-query tile t of a sequence for a pair of query heads of
 //    one kv-head group (A = head h, B = head h + 1; B absent for the last head of an
-//    odd-sized group). Both tiles visit key tiles 0..t (causal tile skipping) over the
-//    same K/V, in lockstep.
+//    odd-sized group). Both tiles visit the key tiles up to the one holding the
+//    tile's last query position (causal tile skipping) over the same K/V, in lockstep.
 //  - Every CTA builds the same dense list of the batch's items, longest first:
 //    items of tile index t (descending), then sequences ordered by their number of
 //    tiles (a stable counting sort in shared memory), then head pairs (so the heads
@@ -90,12 +93,13 @@ struct PrefillParams {
   __nv_bfloat16* out;
   float* lse;
   const int32_t* cu_seqlens;
+  const int32_t* seq_lens_k;  // cached tokens per sequence (Lk), or null: Lk = Lq
   const int32_t* block_tables;
   int* dev_status;
   int* ticket;  // workspace: [0] next ticket, [1] finished CTAs (zero between calls)
   int* tables;  // workspace + 256 B: sorted [kMaxSeqs], lvl_cnt, lvl_off [kMaxLevels]
   int max_blocks_per_seq;
-  int num_seqs, num_tokens, max_seqlen;
+  int num_seqs, num_tokens, max_seqlen, max_seqlen_k;
   int num_q_heads, num_kv_heads, group;
   int num_blocks;
   int n_levels;  // query tiles of the longest allowed sequence
@@ -104,27 +108,37 @@ struct PrefillParams {
   float scale_log2;
 };
 
-__device__ __forceinline__ bool seq_ok(const PrefillParams& p, int s, int* start, int* len) {
-  const int st = __ldg(p.cu_seqlens + s), L = __ldg(p.cu_seqlens + s + 1) - st;
+// Sequence s: its first new token, new tokens (Lq) and cached tokens (Lk); false if
+// it has no new token or is inconsistent.
+__device__ __forceinline__ bool seq_ok(const PrefillParams& p, int s, int* start, int* lq,
+                                       int* lk) {
+  const int st = __ldg(p.cu_seqlens + s), Lq = __ldg(p.cu_seqlens + s + 1) - st;
+  const int Lk = p.seq_lens_k ? __ldg(p.seq_lens_k + s) : Lq;
   *start = st;
-  *len = L;
-  return L > 0 && L <= p.max_seqlen && (L + 15) / 16 <= p.max_blocks_per_seq && st >= 0 &&
-         st + L <= p.num_tokens;
+  *lq = Lq;
+  *lk = Lk;
+  return Lq > 0 && Lq <= p.max_seqlen && Lk >= Lq && Lk <= p.max_seqlen_k &&
+         (Lk + 15) / 16 <= p.max_blocks_per_seq && st >= 0 && st + Lq <= p.num_tokens;
 }
 
 // Query tiles of sequence s (0 for an empty or invalid one).
 __device__ __forceinline__ int tiles_of(const PrefillParams& p, int s) {
-  int st, L;
-  if (!seq_ok(p, s, &st, &L)) return 0;
-  return (L + kBlockM - 1) / kBlockM;
+  int st, Lq, Lk;
+  if (!seq_ok(p, s, &st, &Lq, &Lk)) return 0;
+  return (Lq + kBlockM - 1) / kBlockM;
 }
 
 // One work item: query tile t of one sequence for heads hq (A) and hq + 1 (B, if
 // active_b), as the TMA warp publishes it to the other roles (8 ints per slot).
 // ticket < 0: end of the list.
 struct Item {
-  int ticket, seq, hq, t, start, L, active_b, bad;
-  __device__ int nkt() const { return t + 1; }
+  int ticket, seq, hq, t, start, Lq, Lk, active_b, bad;
+  // key tiles: up to the one holding the tile's last query position (Lk - Lq + 128t
+  // + 127), and no further than the last key
+  __device__ int nkt() const {
+    const int last_q = Lk - Lq + t * kBlockM + kBlockM - 1;
+    return min(last_q, Lk - 1) / kBlockN + 1;
+  }
 };
 
 // Maps ticket t of the dense item list to its item. `lvl` is the caller's level
@@ -143,10 +157,7 @@ __device__ __forceinline__ Item item_of(const PrefillParams& p, int t, int& lvl)
   const int kv = pi / per_group;
   w.hq = kv * p.group + 2 * (pi % per_group);
   w.active_b = w.hq + 1 < (kv + 1) * p.group;
-  int st, L;
-  seq_ok(p, w.seq, &st, &L);
-  w.start = st;
-  w.L = L;
+  seq_ok(p, w.seq, &w.start, &w.Lq, &w.Lk);
   w.bad = 0;
   return w;
 }
@@ -182,9 +193,9 @@ __device__ __forceinline__ void publish(int* slot, const Item& w) {
   slot[2] = w.hq;
   slot[3] = w.t;
   slot[4] = w.start;
-  slot[5] = w.L;
-  slot[6] = w.active_b;
-  slot[7] = w.bad;
+  slot[5] = w.Lq;
+  slot[6] = w.Lk;
+  slot[7] = (w.active_b ? 1 : 0) | (w.bad ? 2 : 0);
 }
 __device__ __forceinline__ Item read_slot(const int* slot) {
   Item w;
@@ -193,9 +204,10 @@ __device__ __forceinline__ Item read_slot(const int* slot) {
   w.hq = slot[2];
   w.t = slot[3];
   w.start = slot[4];
-  w.L = slot[5];
-  w.active_b = slot[6];
-  w.bad = slot[7];
+  w.Lq = slot[5];
+  w.Lk = slot[6];
+  w.active_b = slot[7] & 1;
+  w.bad = (slot[7] >> 1) & 1;
   return w;
 }
 
@@ -300,9 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
   // length errors: reported once per sequence, by CTA 0
   if (c == 0) {
     for (int s = tid; s < p.num_seqs; s += kThreads) {
-      int st, L;
-      const bool ok = seq_ok(p, s, &st, &L) || L == 0;
-      if (!ok || (s == p.num_seqs - 1 && st + L != p.num_tokens))
+      int st, Lq, Lk;
+      const bool ok = seq_ok(p, s, &st, &Lq, &Lk) || Lq == 0;
+      if (!ok || (s == p.num_seqs - 1 && st + Lq != p.num_tokens))
         record_status(p.dev_status, PGQA_EINVAL);
     }
   }
@@ -350,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     auto chunk_rows = [&](const Item& w, int ch) {
       int y = p.oob_row;
       const int lp = ch * 32 + lane;
-      if (w.ticket >= 0 && lp * 16 < w.L) {
+      if (w.ticket >= 0 && lp * 16 < w.Lk) {
         const int32_t pbn =
             __ldg(p.block_tables + static_cast<size_t>(w.seq) * p.max_blocks_per_seq + lp);
         if (pbn >= 0 && pbn < p.num_blocks) y = (pbn * p.num_kv_heads + w.hq / p.group) * 16;
@@ -492,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       if (t < total) {
         w = item_of(p, t, lvl);
         const int32_t* bt = p.block_tables + static_cast<size_t>(w.seq) * p.max_blocks_per_seq;
-        const int npages = (min(w.L, w.nkt() * kBlockN) + 15) / 16;
+        const int npages = (min(w.Lk, w.nkt() * kBlockN) + 15) / 16;
         bool bad = false;
         for (int pg = lane; pg < npages; pg += 32) {  // block ids checked before Q is out
           const int32_t pbn = __ldg(bt + pg);
@@ -626,17 +638,20 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       const int gl0 = gl;  // ring index of this item's K_0 (then V_0, K_1, V_1, ...)
       gl += 2 * w.nkt();
       if (X == 1 && !w.active_b) continue;
-      const int tq = w.t;                  // this tile's index in the sequence
-      const int qpos = tq * kBlockM + r;   // this row's position in the sequence
-      const int lim = min(qpos, w.L - 1);  // last key this row attends
+      const int tq = w.t;                   // this tile's index among the new tokens
+      const int qpos = tq * kBlockM + r;    // this row's position among the new tokens
+      const int off = w.Lk - w.Lq;          // cached tokens before the new ones
+      const int lim = min(off + qpos, w.Lk - 1);  // last key this row attends
+      const int first_lim = off + tq * kBlockM;   // the tile's first row's last key
+      const int nkt = w.nkt();
       float m_ref = -INFINITY, l = 0.f;
-      for (int j = 0; j <= tq; ++j) {
+      for (int j = 0; j < nkt; ++j) {
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(&s_full[X], tcnt & 1)))) break;
         tc_fence_after();
         const int kbase = j * kBlockN;
         uint32_t sr[128];
         tmem_ld128(lane_base + s_col, sr);
-        if (j == tq) {  // the diagonal tile: the only one with masked keys
+        if (kbase + kBlockN - 1 > first_lim) {  // a tile with masked keys (the diagonal)
 #pragma unroll
           for (int q = 0; q < 128; ++q)
             if (kbase + q > lim) sr[q] = __float_as_uint(-INFINITY);
@@ -700,10 +715,10 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         // that P = 0 there contributes exactly nothing. Only the last key tile of the
         // item reaches past the end; tile A's softmax zeroes it (P_B V is issued after
         // P_A V, which waits for this).
-        if (X == 0 && kbase + kBlockN > w.L) {
+        if (X == 0 && kbase + kBlockN > w.Lk) {
           const int gi = gl0 + 2 * j + 1, vs = gi % kStages;
           if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full[vs], (gi / kStages) & 1)))) break;
-          if (kbase + r >= w.L) {
+          if (kbase + r >= w.Lk) {
             uint8_t* vrow = smem + C::kRing + vs * C::kTile + r * 128;
 #pragma unroll
             for (int sub = 0; sub < C::kSub; ++sub) {
@@ -722,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       // epilogue: O / l -> bf16, lse
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(&o_full[X], (tcnt - 1) & 1)))) break;
       tc_fence_after();
-      const bool store = qpos < w.L;
+      const bool store = qpos < w.Lq;
       const size_t orow =
           static_cast<size_t>(w.start + (store ? qpos : 0)) * p.num_q_heads + w.hq + X;
       uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D);
@@ -782,6 +797,8 @@ pgqa_status_t launch_prefill_variant(const PrefillArgs& a) {
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
   p.cu_seqlens = a.cu_seqlens;
+  p.seq_lens_k = a.seq_lens_k;
+  p.max_seqlen_k = a.seq_lens_k ? a.max_seqlen_k : a.max_seqlen;
   p.block_tables = a.block_tables;
   p.dev_status = a.dev_status;
   p.ticket = static_cast<int*>(a.workspace);

@@ -459,6 +459,77 @@ def pin_prefill_rows_subset():
         assert np.array_equal(so[t, h], full_o[t, h]) and sl[t, h] == full_l[t, h]
 
 
+# ------------------------------------------- prefill over a cached prefix (chunked)
+
+def _chunk_case(lens_k, lens_q, Hq, Hkv, D, seed):
+    """Full per-sequence K/V of Lk tokens; queries for the last Lq of them."""
+    K = [rand_bf16((Hkv, L, D), seed + 1 + b) for b, L in enumerate(lens_k)]
+    V = [rand_bf16((Hkv, L, D), seed + 70 + b) for b, L in enumerate(lens_k)]
+    q = rand_bf16((sum(lens_q), Hq, D), seed)
+    cu = torch.tensor([0] + np.cumsum(lens_q).tolist(), dtype=torch.int32)
+    return q, K, V, cu, torch.tensor(lens_k, dtype=torch.int32)
+
+
+def pin_chunked_vs_sdpa_bottom_right():
+    """torch SDPA with an explicit mask: chunk row i sees keys 0..Lk-Lq+i."""
+    lens_k, lens_q = [23, 40, 5], [7, 1, 5]
+    Hq, Hkv, D = 4, 2, 16
+    q, K, V, cu, lk = _chunk_case(lens_k, lens_q, Hq, Hkv, D, 181)
+    kc, vc, table = shuffle_pool(*identity_pool(K, V, lens_k), 182)
+    out, lse = O.paged_prefill_kv(q, kc, vc, table, cu, lk, 0.25)
+    for i, (Lk, Lq) in enumerate(zip(lens_k, lens_q)):
+        a = int(cu[i])
+        qi = q[a:a + Lq].permute(1, 0, 2)                     # [Hq, Lq, D]
+        Kr = K[i].repeat_interleave(Hq // Hkv, 0)
+        Vr = V[i].repeat_interleave(Hq // Hkv, 0)
+        mask = torch.arange(Lk)[None, :] <= (Lk - Lq + torch.arange(Lq))[:, None]
+        want = F.scaled_dot_product_attention(qi.double()[None], Kr.double()[None],
+                                              Vr.double()[None], attn_mask=mask,
+                                              scale=0.25)[0].permute(1, 0, 2)
+        _close(out[a:a + Lq], want.numpy(), 1e-11, 1e-12, "chunked prefill vs sdpa")
+
+
+def pin_chunked_equals_full_prefill_rows():
+    """A chunk's rows are the same rows of a prefill over the whole sequence."""
+    lens = [33, 18]
+    lens_q = [9, 18]
+    Hq, Hkv, D = 2, 1, 8
+    qf, K, V, cuf = _prefill_case(lens, Hq, Hkv, D, 191)
+    pool = identity_pool(K, V, lens)
+    full_o, full_l = O.paged_prefill(qf, *pool, cuf, 0.3)
+    rows = torch.cat([qf[int(cuf[i + 1]) - n:int(cuf[i + 1])] for i, n in enumerate(lens_q)])
+    cu = torch.tensor([0] + np.cumsum(lens_q).tolist(), dtype=torch.int32)
+    o, l = O.paged_prefill_kv(rows, *pool, cu, torch.tensor(lens, dtype=torch.int32), 0.3)
+    for i, n in enumerate(lens_q):
+        e = int(cuf[i + 1])
+        assert np.array_equal(o[int(cu[i]):int(cu[i + 1])], full_o[e - n:e])
+        assert np.array_equal(l[int(cu[i]):int(cu[i + 1])], full_l[e - n:e])
+
+
+def pin_chunked_last_row_is_decode():
+    """The last row of a chunk attends to the whole context: a decode step."""
+    lens_k, lens_q = [50, 17], [4, 3]
+    Hq, Hkv, D = 4, 2, 8
+    q, K, V, cu, lk = _chunk_case(lens_k, lens_q, Hq, Hkv, D, 201)
+    pool = identity_pool(K, V, lens_k)
+    o, l = O.paged_prefill_kv(q, *pool, cu, lk, 0.2)
+    last = torch.stack([q[int(cu[i + 1]) - 1] for i in range(len(lens_k))])
+    do, dl = O.paged_decode(last, *pool, lk, 0.2)
+    for i in range(len(lens_k)):
+        t = int(cu[i + 1]) - 1
+        _close(o[t], do[i], 1e-13, 1e-14, "chunk last row vs decode")
+        _close(l[t], dl[i], 1e-13, 1e-14, "chunk last row lse vs decode")
+
+
+def pin_chunked_without_prefix_is_prefill():
+    lens = [12, 3]
+    q, K, V, cu = _prefill_case(lens, 4, 2, 8, 211)
+    pool = identity_pool(K, V, lens)
+    o1, l1 = O.paged_prefill(q, *pool, cu, 0.3)
+    o2, l2 = O.paged_prefill_kv(q, *pool, cu, torch.tensor(lens, dtype=torch.int32), 0.3)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]
 
 

@@ -117,3 +117,16 @@ def test_prefill_argument_validation():
     assert f(*args) == pgqa.ENOWORKSPACE                           # no workspace given
     assert f(*args[:10], 600000, *args[11:]) == pgqa.EUNSUPPORTED  # longer than 524288 tokens
     assert pgqa.prefill_workspace_size(2, 8, 64) == 256 + (4096 + 2 * 2048) * 4
+
+
+def test_prefill_kv_argument_validation():
+    f = pgqa.lib.pgqa_paged_prefill_varlen_kv
+    P = 1 << 20
+    #       out lse q  T    k  v  bt maxb cuq lk S  maxq maxk Hq Hkv D   NB  bs  scale ws wsb st stream
+    args = [P, None, P, 100, P, P, P, 64, P, P, 2, 64, 1000, 8, 2, 128, 64, 16, 0.1, P, 33024, None,
+            None]
+    assert f(*args[:9], None, *args[10:]) == pgqa.EINVAL           # no key lengths
+    assert f(*args[:12], 1 << 27, *args[13:]) == pgqa.EUNSUPPORTED  # keys beyond 2^26
+    assert f(*args[:12], -1, *args[13:]) == pgqa.EINVAL
+    assert f(*args[:10], 0, *args[11:]) == pgqa.OK                 # nothing to do
+    assert f(*args[:19], None, 0, *args[21:]) == pgqa.ENOWORKSPACE

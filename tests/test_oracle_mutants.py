@@ -19,7 +19,12 @@ MUTANTS = {
     "normalise_by_max": ("double p = exp(scores[j] - l);", "double p = exp(scores[j] - m);"),
     "transposed_K": ("s += q[d] * K[(size_t)j * D + d];", "s += q[d] * K[(size_t)d * L + j];"),
     "gqa_map_modulo_decode": ("int hq = h * G + g;", "int hq = g * Hkv + h;"),
-    "gqa_map_modulo_prefill": ("h = hq / G;", "h = hq % Hkv;"),
+    "gqa_map_modulo_prefill": ("L = p + 1;                           /* causal: keys 0..p */\n        h = hq / G;",
+                               "L = p + 1;                           /* causal: keys 0..p */\n        h = hq % Hkv;"),
+    "gqa_map_modulo_chunked": ("L = Lk - Lq + p + 1; /* keys 0..Lk-Lq+p */\n        h = hq / G;",
+                               "L = Lk - Lq + p + 1; /* keys 0..Lk-Lq+p */\n        h = hq % Hkv;"),
+    "chunk_top_left_alignment": ("L = Lk - Lq + p + 1;", "L = p + 1;"),
+    "chunk_one_key_short": ("L = Lk - Lq + p + 1;", "L = Lk - Lq + p;"),
     "cache_layout_row_major_heads": ("return (((size_t)block * Hkv + h) * bs + row) * D + d;",
                                      "return (((size_t)block * bs + row) * Hkv + h) * D + d;"),
     "row_off_by_one": ("int row = j % block_size;", "int row = (j + 1) % block_size;"),

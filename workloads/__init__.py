@@ -124,6 +124,40 @@ class PrefillInputs:
         return max(self.seq_lens) if self.num_seqs else 0
 
 
+@dataclass
+class ChunkedPrefillInputs:
+    """A prefill over a cached prefix (all CPU tensors): sequence i has Lk = seq_lens_k[i]
+    tokens, the last Lq of which are the new chunk (cu_seqlens_q); key/value hold all
+    Lk tokens of every sequence, written into the cache through slot_mapping."""
+    q: torch.Tensor               # [Tq, Hq, D] bf16, the chunks' queries
+    key: torch.Tensor             # [Tk, Hkv, D] bf16, every cached token
+    value: torch.Tensor
+    slot_mapping: torch.Tensor    # [Tk] int64
+    cu_seqlens_q: torch.Tensor    # [S + 1] int32
+    seq_lens_k: torch.Tensor      # [S] int32
+    block_tables: torch.Tensor    # [S, max_blocks] int32
+    k_cache: torch.Tensor         # [NB, Hkv, bs, D] bf16, initial (pre-write) contents
+    v_cache: torch.Tensor
+    scale: float
+    name: str = ""
+
+    @property
+    def num_seqs(self):
+        return self.cu_seqlens_q.numel() - 1
+
+    @property
+    def lens_q(self):
+        return (self.cu_seqlens_q[1:] - self.cu_seqlens_q[:-1]).tolist()
+
+    @property
+    def max_seqlen_q(self):
+        return max(self.lens_q) if self.num_seqs else 0
+
+    @property
+    def max_seqlen_k(self):
+        return int(self.seq_lens_k.max()) if self.num_seqs else 0
+
+
 def _blocks_needed(L: int, bs: int) -> int:
     return (L + bs - 1) // bs
 
@@ -261,6 +295,40 @@ def make_prefill(seq_lens: Sequence[int], num_q_heads: int, num_kv_heads: int, h
                          scale=1.0 / math.sqrt(head_dim), name=name)
 
 
+def make_chunked_prefill(lens_k: Sequence[int], lens_q: Sequence[int], num_q_heads: int,
+                         num_kv_heads: int, head_dim: int, num_blocks: int, seed: int,
+                         block_size: int = BLOCK_SIZE, name: str = "") -> ChunkedPrefillInputs:
+    """Sequence i caches lens_k[i] tokens; its new chunk is the last lens_q[i] of them.
+    The cache starts all-NaN, so a read of a row no sequence owns poisons the result."""
+    assert len(lens_k) == len(lens_q) and all(0 <= q <= k for k, q in zip(lens_k, lens_q))
+    g = _gen(seed)
+    S = len(lens_k)
+    Tk, Tq = int(sum(lens_k)), int(sum(lens_q))
+    cu = torch.zeros(S + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(list(lens_q), dtype=torch.int64), 0).to(torch.int32)
+    q = _randn_bf16((Tq, num_q_heads, head_dim), g)
+    key = _randn_bf16((Tk, num_kv_heads, head_dim), g)
+    value = _randn_bf16((Tk, num_kv_heads, head_dim), g)
+    shape = (num_blocks, num_kv_heads, block_size, head_dim)
+    k_cache = torch.full(shape, float("nan"), dtype=torch.bfloat16)
+    v_cache = torch.full(shape, float("nan"), dtype=torch.bfloat16)
+    perm = torch.randperm(num_blocks, generator=g)
+    max_blocks = max([_blocks_needed(L, block_size) for L in lens_k] + [1])
+    table, used = _assign_tables(lens_k, perm, 0, block_size, max_blocks)
+    if used > num_blocks:
+        raise ValueError("block pool too small")
+    slots = torch.empty(Tk, dtype=torch.int64)
+    base = 0
+    for i, L in enumerate(lens_k):
+        p = torch.arange(L, dtype=torch.int64)
+        slots[base:base + L] = table[i, p // block_size].to(torch.int64) * block_size + p % block_size
+        base += L
+    return ChunkedPrefillInputs(q=q, key=key, value=value, slot_mapping=slots, cu_seqlens_q=cu,
+                                seq_lens_k=torch.tensor(list(lens_k), dtype=torch.int32),
+                                block_tables=table, k_cache=k_cache, v_cache=v_cache,
+                                scale=1.0 / math.sqrt(head_dim), name=name)
+
+
 def _pool_for(lens: Sequence[int], base: int, rotations: int, bs: int = BLOCK_SIZE) -> int:
     """Smallest pool (a multiple of 1024 blocks, at least ``base``) that holds
     ``rotations + 1`` disjoint copies of the tables for ``lens``."""
@@ -306,6 +374,27 @@ def varlen_prefill(seed: int = 0) -> PrefillInputs:
     lens = _uniform_lens(16, 128, 2048, seed + 4)
     return make_prefill(lens, 32, 8, 128, 2048, seed + 4,
                         name="varlen causal prefill 16 seqs L U[128,2048] Hq32 Hkv8 D128")
+
+
+def chunked_prefill(seed: int = 0) -> ChunkedPrefillInputs:
+    """Prefill over a cached prefix: 16 sequences with a cached prefix uniform on
+    [512, 3584] tokens and a new chunk uniform on [128, 512], 32 query / 8 kv heads,
+    head_dim 128, a shuffled 4096-block pool."""
+    prefix = _uniform_lens(16, 512, 3584, seed + 6)
+    chunk = _uniform_lens(16, 128, 512, seed + 7)
+    lens_k = [a + b for a, b in zip(prefix, chunk)]
+    return make_chunked_prefill(lens_k, chunk, 32, 8, 128, 4096, seed + 6,
+                                name="chunked prefill 16 seqs prefix U[512,3584] + chunk "
+                                     "U[128,512] Hq32 Hkv8 D128")
+
+
+def speculative_verify(seed: int = 0, draft: int = 5) -> ChunkedPrefillInputs:
+    """Speculative verification: batch 64, contexts uniform on [256, 1024] (the last
+    `draft` tokens are the drafts being checked), 32 query / 8 kv heads, head_dim 128."""
+    lens_k = _uniform_lens(64, 256, 1024, seed + 8)
+    return make_chunked_prefill(lens_k, [draft] * 64, 32, 8, 128, 8192, seed + 8,
+                                name=f"speculative verification B64 ctx U[256,1024] "
+                                     f"{draft} tokens/seq Hq32 Hkv8 D128")
 
 
 def prefix_sharing_decode(seed: int = 0, rotations: int = 0) -> DecodeInputs:
