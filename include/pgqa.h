@@ -184,6 +184,23 @@ pgqa_status_t pgqa_paged_attention_decode(void* out, float* lse, const void* q,
                                           void* workspace, size_t workspace_bytes,
                                           int* dev_status, void* stream);
 
+/*
+ * Sliding-window paged decode: as pgqa_paged_attention_decode, but a context of L
+ * keys attends only to its last `window` keys, L-window .. L-1 (the sliding-window
+ * mask of "PageAttention + FlashAttention, the golden combination", sec. 4.1:
+ * query i sees keys i-W+1 .. i). Only the pages holding those keys are read.
+ *   window        >= 1 (PGQA_EINVAL otherwise); a window of at least the context
+ *                 is plain decode.
+ * Every other argument, the workspace (pgqa_decode_workspace_size) and the error
+ * behaviour are as for pgqa_paged_attention_decode.
+ */
+pgqa_status_t pgqa_paged_attention_decode_window(
+    void* out, float* lse, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int num_blocks, int block_size,
+    float scale, int window, int cache_dtype, const float* k_scale, const float* v_scale,
+    int max_context_len, void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
+
 /* Size of the library-owned scratch array used by
  * pgqa_paged_attention_decode_noalloc (8 MiB per GPU that loads the library). */
 #define PGQA_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)

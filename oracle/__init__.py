@@ -46,6 +46,9 @@ def _bind(path):
     lib.oracle_paged_prefill_kv.argtypes = [P, P, P, I, P, P, P, I, P, P, I, I, I, I, I, I, D, P,
                                             I64, P, P, I]
     lib.oracle_paged_prefill_kv.restype = I
+    lib.oracle_paged_decode_window.argtypes = [P, P, P, I, P, P, P, I, P, I, I, I, I, I, I, D, I,
+                                               P, P, I]
+    lib.oracle_paged_decode_window.restype = I
     lib.oracle_dense_row.argtypes = [P, P, P, I, I, D, P, P]
     lib.oracle_dense_row.restype = None
     lib.oracle_has_openmp.argtypes = []
@@ -201,6 +204,28 @@ def paged_prefill(q, k_cache, v_cache, block_tables, cu_seqlens, scale, rows=Non
                                       bs, float(scale), _ptr(r), n_rows, _ptr(out), _ptr(lse),
                                       threads or default_threads())
     _check(rc, "paged_prefill")
+    return out, lse
+
+
+def paged_decode_window(q, k_cache, v_cache, block_tables, context_lens, scale, window,
+                        dtype=BF16, k_scale=None, v_scale=None, threads=None):
+    """Sliding-window decode: each context's last `window` keys only. Returns
+    (out [B, Hq, D] float64, lse [B, Hq] float64)."""
+    q = _np(q, np.uint16)
+    elem = np.uint16 if dtype == BF16 else np.uint8
+    kc, vc = _np(k_cache, elem), _np(v_cache, elem)
+    bt, cl = _np(block_tables, np.int32), _np(context_lens, np.int32)
+    ks = None if k_scale is None else _np(k_scale, np.float32)
+    vs = None if v_scale is None else _np(v_scale, np.float32)
+    B, Hq, D = q.shape
+    NB, Hkv, bs, _ = kc.shape
+    out = np.zeros((B, Hq, D), np.float64)
+    lse = np.zeros((B, Hq), np.float64)
+    rc = _load().oracle_paged_decode_window(_ptr(q), _ptr(kc), _ptr(vc), dtype, _ptr(ks),
+                                            _ptr(vs), _ptr(bt), bt.shape[1], _ptr(cl), B, Hq, Hkv,
+                                            D, NB, bs, float(scale), int(window), _ptr(out),
+                                            _ptr(lse), threads or default_threads())
+    _check(rc, "paged_decode_window")
     return out, lse
 
 

@@ -37,6 +37,9 @@
  *    (and the fp8 K scale); an empty context gives out = 0, lse = -inf.
  *  - Causal prefill without a cached prefix: query position p of a sequence
  *    sees keys 0..p of the same sequence.
+ *  - Sliding-window decode ([P2] sec. 4.1 builds a mask that lets query i see
+ *    keys max(0, i-W+1)..i): the decode step of a context of L keys attends to
+ *    keys max(0, L-W)..L-1, the last W of them.
  *  - Prefill over a cached prefix ([P1] sec. 2.4 passes separate cumulative
  *    lengths for queries and keys): a chunk of Lq new tokens of a sequence whose
  *    cache holds Lk >= Lq tokens (the chunk's own tokens last) sits at the end of
@@ -330,6 +333,60 @@ int oracle_paged_prefill(const uint16_t* q, const void* k_cache, const void* v_c
             for (int d = 0; d < D; ++d) qd[d] = oracle_bf16_to_f64(qrow[d]);
             attend_row(qd, K, V, L, D, scale, scores, out + ((size_t)t * Hq + hq) * D,
                        lse + (size_t)t * Hq + hq);
+        }
+        free(K);
+        free(V);
+        free(qd);
+        free(scores);
+    }
+    return status;
+}
+
+/* Sliding-window decode: as oracle_paged_decode, attending only to keys
+ * max(0, L-W)..L-1 of each context ([P2] sec. 4.1, query i sees keys i-W+1..i). */
+int oracle_paged_decode_window(const uint16_t* q, const void* k_cache, const void* v_cache,
+                               int dtype, const float* k_scale, const float* v_scale,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int B, int Hq, int Hkv, int D,
+                               int num_blocks, int block_size, double scale, int window,
+                               double* out, double* lse, int nthreads) {
+    int G, status = ORACLE_OK;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || block_size <= 0 ||
+        window <= 0)
+        return ORACLE_EINVAL;
+    if (dtype == ORACLE_E4M3 && (!k_scale || !v_scale)) return ORACLE_EINVAL;
+    G = Hq / Hkv;
+    (void)nthreads;
+#pragma omp parallel for schedule(dynamic) num_threads(nthreads > 0 ? nthreads : 1)
+    for (int64_t bh = 0; bh < (int64_t)B * Hkv; ++bh) {
+        int b = (int)(bh / Hkv), h = (int)(bh % Hkv);
+        int L = context_lens[b];
+        int first = L > window ? L - window : 0; /* the window's first key */
+        double *K, *V, *qd, *scores;
+        int rc;
+        if (L < 0) {
+#pragma omp critical
+            status = ORACLE_EINVAL;
+            continue;
+        }
+        K = (double*)malloc(sizeof(double) * ((size_t)L * D + 1));
+        V = (double*)malloc(sizeof(double) * ((size_t)L * D + 1));
+        qd = (double*)malloc(sizeof(double) * D);
+        scores = (double*)malloc(sizeof(double) * ((size_t)L + 1));
+        rc = oracle_gather_kv(k_cache, v_cache, dtype, k_scale, v_scale,
+                              block_tables + (size_t)b * max_blocks_per_seq, max_blocks_per_seq, L,
+                              h, Hkv, D, num_blocks, block_size, K, V);
+        if (rc != ORACLE_OK) {
+#pragma omp critical
+            status = rc;
+        } else {
+            for (int g = 0; g < G; ++g) {
+                int hq = h * G + g;
+                const uint16_t* qrow = q + ((size_t)b * Hq + hq) * D;
+                for (int d = 0; d < D; ++d) qd[d] = oracle_bf16_to_f64(qrow[d]);
+                attend_row(qd, K + (size_t)first * D, V + (size_t)first * D, L - first, D, scale,
+                           scores, out + ((size_t)b * Hq + hq) * D, lse + (size_t)b * Hq + hq);
+            }
         }
         free(K);
         free(V);

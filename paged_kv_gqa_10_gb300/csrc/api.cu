@@ -265,16 +265,15 @@ size_t pgqa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_head
   return a > b ? a : b;
 }
 
-pgqa_status_t pgqa_paged_attention_decode(void* out, float* lse, const void* q,
-                                          const void* k_cache, const void* v_cache,
-                                          const int32_t* block_tables, int max_blocks_per_seq,
-                                          const int32_t* context_lens, int num_seqs,
-                                          int num_q_heads, int num_kv_heads, int head_dim,
-                                          int num_blocks, int block_size, float scale,
-                                          int cache_dtype, const float* k_scale,
-                                          const float* v_scale, int max_context_len,
-                                          void* workspace, size_t workspace_bytes,
-                                          int* dev_status, void* stream) {
+// Shared by both decode entry points (window 0: the whole context).
+static pgqa_status_t decode_call(void* out, float* lse, const void* q, const void* k_cache,
+                                 const void* v_cache, const int32_t* block_tables,
+                                 int max_blocks_per_seq, const int32_t* context_lens,
+                                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int num_blocks, int block_size, float scale, int window,
+                                 int cache_dtype, const float* k_scale, const float* v_scale,
+                                 int max_context_len, void* workspace, size_t workspace_bytes,
+                                 int* dev_status, void* stream) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 ||
       block_size <= 0 || max_context_len < 0 || max_blocks_per_seq < 0 || !isfinite(scale))
     return PGQA_EINVAL;
@@ -321,11 +320,41 @@ pgqa_status_t pgqa_paged_attention_decode(void* out, float* lse, const void* q,
   a.k_scale = k_scale;
   a.v_scale = v_scale;
   a.max_context_len = max_context_len;
+  a.window = window;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   a.dev_status = dev_status;
   a.stream = static_cast<cudaStream_t>(stream);
   return pgqa::launch_paged_decode(a, plan);
+}
+
+pgqa_status_t pgqa_paged_attention_decode(void* out, float* lse, const void* q,
+                                          const void* k_cache, const void* v_cache,
+                                          const int32_t* block_tables, int max_blocks_per_seq,
+                                          const int32_t* context_lens, int num_seqs,
+                                          int num_q_heads, int num_kv_heads, int head_dim,
+                                          int num_blocks, int block_size, float scale,
+                                          int cache_dtype, const float* k_scale,
+                                          const float* v_scale, int max_context_len,
+                                          void* workspace, size_t workspace_bytes,
+                                          int* dev_status, void* stream) {
+  return decode_call(out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks,
+                     block_size, scale, 0, cache_dtype, k_scale, v_scale, max_context_len,
+                     workspace, workspace_bytes, dev_status, stream);
+}
+
+pgqa_status_t pgqa_paged_attention_decode_window(
+    void* out, float* lse, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int num_blocks, int block_size,
+    float scale, int window, int cache_dtype, const float* k_scale, const float* v_scale,
+    int max_context_len, void* workspace, size_t workspace_bytes, int* dev_status, void* stream) {
+  if (window <= 0) return PGQA_EINVAL;
+  return decode_call(out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks,
+                     block_size, scale, window, cache_dtype, k_scale, v_scale, max_context_len,
+                     workspace, workspace_bytes, dev_status, stream);
 }
 
 size_t pgqa_prefill_workspace_size(int num_seqs, int num_q_heads, int max_seqlen) {

@@ -74,6 +74,7 @@ struct DecodeParams {
   int num_seqs, num_q_heads, num_kv_heads, group;
   int num_blocks;
   int max_context_len;
+  int window;        // > 0: each context's last `window` keys only
   float scale_log2;  // scale * log2(e)
 };
 
@@ -107,12 +108,25 @@ constexpr int ctas_per_sm() {
   return (227 * 1024) / (Cfg<D, kFp8>::kSmem + 1024) >= 2 ? 2 : 1;
 }
 
+// First key attended in a context of L keys: L - window with a sliding window (the
+// last `window` keys: query i sees keys i-W+1..i, "PageAttention + FlashAttention,
+// the golden combination", sec. 4.1), else 0.
+__device__ __forceinline__ int first_key(const DecodeParams& p, int L) {
+  return p.window > 0 && L > p.window ? L - p.window : 0;
+}
+
+// Pages of sequence b the step reads (those holding keys first_key .. L-1).
 __device__ __forceinline__ int pages_of(const DecodeParams& p, int b, bool* valid = nullptr) {
   const int L = __ldg(p.context_lens + b);
   const int n = (L + 15) >> 4;
   const bool ok = L >= 0 && L <= p.max_context_len && n <= p.max_blocks_per_seq;
   if (valid) *valid = ok;
-  return ok ? n : 0;
+  return ok && L > 0 ? n - (first_key(p, L) >> 4) : 0;
+}
+
+// Logical page of sequence b's first page read.
+__device__ __forceinline__ int first_page(const DecodeParams& p, int b) {
+  return first_key(p, __ldg(p.context_lens + b)) >> 4;
 }
 
 // Sum over the CTA (every thread of the CTA must call it).
@@ -154,6 +168,7 @@ __device__ __forceinline__ long long block_scan(long long v, long long* scratch,
 // A CTA's walk over units: unit (b, h) holds pages [S, S + P) of the global order.
 struct Walk {
   int b, h, P;
+  int fp;  // logical page of the unit's first page read
   long long S;
   __device__ __forceinline__ void next(const DecodeParams& p) {
     S += P;
@@ -163,6 +178,7 @@ struct Walk {
         ++b;
         P = b < p.num_seqs ? pages_of(p, b) : 0;
       } while (P == 0 && b < p.num_seqs);
+      fp = b < p.num_seqs ? first_page(p, b) : 0;
     }
   }
 };
@@ -388,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
   Walk w0;
   w0.b = misc[0];
   w0.P = pages_of(p, w0.b);
+  w0.fp = first_page(p, w0.b);
   w0.h = static_cast<int>((r0 - scratch[kScanSlots - 1]) / w0.P);
   w0.S = scratch[kScanSlots - 1] + static_cast<long long>(w0.h) * w0.P;
 
@@ -425,7 +442,8 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
         const int cnt = min(32, min(fw.P - fpg, n - fetched));
         if (lane < cnt) {
           const int32_t pbn =
-              __ldg(p.block_tables + static_cast<size_t>(fw.b) * p.max_blocks_per_seq + fpg + lane);
+              __ldg(p.block_tables + static_cast<size_t>(fw.b) * p.max_blocks_per_seq + fw.fp +
+                    fpg + lane);
           yring[(fetched + lane) % kYRing] =
               (pbn < 0 || pbn >= p.num_blocks) ? -1 : (pbn * Hkv + fw.h) * 16;
         }
@@ -528,6 +546,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
     const int seg1 = static_cast<int>((r1 < w.S + w.P ? r1 : w.S + w.P) - w.S);
     const int npg = seg1 - seg0;
     const int L = __ldg(p.context_lens + w.b);
+    const int kfirst = first_key(p, L);
 
     // Q^T fragments (B operand) of this unit, then start loading the next unit's
     uint32_t qf[C::kNkc][2];
@@ -567,7 +586,9 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
       bad |= meta[s];
       const uint32_t stK = smem_u32(ring + s * C::kStageBytes);
       const uint32_t stV = stK + C::kPageBytes;
-      const int nv = min(16, L - (seg0 + j) * 16);  // valid tokens in this page
+      const int pk0 = (w.fp + seg0 + j) * 16;       // key of the page's first row
+      const int nv = min(16, L - pk0);               // rows below nv hold keys < L
+      const int lo = max(0, kfirst - pk0);           // rows below lo are outside the window
 
       // ---- S^T = K Q^T
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -593,8 +614,8 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
       // fragment: sc[0] (tok gid, head 2tig), sc[1] (gid, 2tig+1),
       //           sc[2] (gid+8, 2tig),      sc[3] (gid+8, 2tig+1)
       float s0 = sc[0] * sl2, s1 = sc[1] * sl2, s2 = sc[2] * sl2, s3 = sc[3] * sl2;
-      if (gid >= nv) s0 = s1 = -INFINITY;
-      if (gid + 8 >= nv) s2 = s3 = -INFINITY;
+      if (gid >= nv || gid < lo) s0 = s1 = -INFINITY;
+      if (gid + 8 >= nv || gid + 8 < lo) s2 = s3 = -INFINITY;
       float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
@@ -625,6 +646,8 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
           (2 * tig < nv ? 0x0000ffffu : 0u) | (2 * tig + 1 < nv ? 0xffff0000u : 0u);
       const uint32_t m89 =
           (2 * tig + 8 < nv ? 0x0000ffffu : 0u) | (2 * tig + 9 < nv ? 0xffff0000u : 0u);
+      // (rows below lo hold real keys and get P = 0; only rows past the context,
+      // which may hold NaN, need zeroing)
       if constexpr (!kFp8) {
 #pragma unroll
         for (int dc = 0; dc < C::kNkc; ++dc) {
@@ -770,6 +793,7 @@ pgqa_status_t launch_variant(const DecodeArgs& a, const DecodePlan& plan) {
   p.group = a.num_q_heads / a.num_kv_heads;
   p.num_blocks = a.num_blocks;
   p.max_context_len = a.max_context_len;
+  p.window = a.window;
   p.scale_log2 = a.scale * kLog2e;
   if (launch_after_previous(paged_decode_kernel<D, kFp8>, dim3(plan.grid), dim3(kThreads),
                             C::kSmem, a.stream, kmap, vmap, p) != cudaSuccess)

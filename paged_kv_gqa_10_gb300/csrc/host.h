@@ -77,6 +77,7 @@ struct DecodeArgs {
   const float* k_scale;
   const float* v_scale;
   int max_context_len;
+  int window;  // > 0: only the last `window` keys of each context are attended
   void* workspace;
   size_t workspace_bytes;
   int* dev_status;

@@ -459,6 +459,57 @@ def pin_prefill_rows_subset():
         assert np.array_equal(so[t, h], full_o[t, h]) and sl[t, h] == full_l[t, h]
 
 
+# ------------------------------------------------------- sliding-window decode
+
+def pin_window_vs_sdpa_mask():
+    """torch SDPA with an explicit mask over the whole context: keys L-W..L-1 only."""
+    lens, W = [40, 9, 100], 16
+    Hq, Hkv, D = 4, 2, 16
+    q, K, V = _decode_case(lens, Hq, Hkv, D, 221)
+    kc, vc, table = shuffle_pool(*identity_pool(K, V, lens), 222)
+    cl = torch.tensor(lens, dtype=torch.int32)
+    out, lse = O.paged_decode_window(q, kc, vc, table, cl, 0.3, W)
+    for b, L in enumerate(lens):
+        Kr = K[b].repeat_interleave(Hq // Hkv, 0)
+        Vr = V[b].repeat_interleave(Hq // Hkv, 0)
+        mask = (torch.arange(L) >= L - W)[None, :]
+        want = F.scaled_dot_product_attention(q[b][:, None].double()[None], Kr.double()[None],
+                                              Vr.double()[None], attn_mask=mask,
+                                              scale=0.3)[0][:, 0]
+        _close(out[b], want.numpy(), 1e-11, 1e-12, "window decode vs sdpa")
+
+
+def pin_window_is_decode_of_the_window():
+    """A window over a long context equals plain decode of a cache that holds only the
+    window's keys; a window at least the context is plain decode."""
+    lens, W = [70, 23], 20
+    Hq, Hkv, D = 4, 1, 8
+    q, K, V = _decode_case(lens, Hq, Hkv, D, 231)
+    pool = identity_pool(K, V, lens)
+    cl = torch.tensor(lens, dtype=torch.int32)
+    wo, wl = O.paged_decode_window(q, *pool, cl, 0.2, W)
+    tails = [min(L, W) for L in lens]
+    Kt = [K[b][:, L - n:] for b, (L, n) in enumerate(zip(lens, tails))]
+    Vt = [V[b][:, L - n:] for b, (L, n) in enumerate(zip(lens, tails))]
+    do, dl = O.paged_decode(q, *identity_pool(Kt, Vt, tails), torch.tensor(tails, dtype=torch.int32), 0.2)
+    assert np.array_equal(wo, do) and np.array_equal(wl, dl)
+    fo, fl = O.paged_decode(q, *pool, cl, 0.2)
+    go, gl = O.paged_decode_window(q, *pool, cl, 0.2, max(lens))
+    assert np.array_equal(fo, go) and np.array_equal(fl, gl)
+
+
+def pin_window_of_one_is_last_value():
+    lens = [5, 33]
+    q, K, V = _decode_case(lens, 2, 1, 8, 241)
+    out, lse = O.paged_decode_window(q, *identity_pool(K, V, lens),
+                                     torch.tensor(lens, dtype=torch.int32), 0.5, 1)
+    for b, L in enumerate(lens):
+        for h in range(2):
+            assert np.array_equal(out[b, h], V[b][0, L - 1].double().numpy())
+            s = 0.5 * float((q[b, h].double() * K[b][0, L - 1].double()).sum())
+            assert abs(lse[b, h] - s) < 1e-12
+
+
 # ------------------------------------------- prefill over a cached prefix (chunked)
 
 def _chunk_case(lens_k, lens_q, Hq, Hkv, D, seed):

@@ -18,12 +18,19 @@ MUTANTS = {
     "lse_without_max": ("l = m + log(sum);", "l = log(sum);"),
     "normalise_by_max": ("double p = exp(scores[j] - l);", "double p = exp(scores[j] - m);"),
     "transposed_K": ("s += q[d] * K[(size_t)j * D + d];", "s += q[d] * K[(size_t)d * L + j];"),
-    "gqa_map_modulo_decode": ("int hq = h * G + g;", "int hq = g * Hkv + h;"),
+    "gqa_map_modulo_decode": ("int hq = h * G + g;\n                const uint16_t* qrow = q + ((size_t)b * Hq + hq) * D;\n                for (int d = 0; d < D; ++d) qd[d] = oracle_bf16_to_f64(qrow[d]);\n                attend_row(qd, K, V, L, D,",
+                              "int hq = g * Hkv + h;\n                const uint16_t* qrow = q + ((size_t)b * Hq + hq) * D;\n                for (int d = 0; d < D; ++d) qd[d] = oracle_bf16_to_f64(qrow[d]);\n                attend_row(qd, K, V, L, D,"),
+    "gqa_map_modulo_window": ("int hq = h * G + g;\n                const uint16_t* qrow = q + ((size_t)b * Hq + hq) * D;\n                for (int d = 0; d < D; ++d) qd[d] = oracle_bf16_to_f64(qrow[d]);\n                attend_row(qd, K + (size_t)first * D,",
+                              "int hq = g * Hkv + h;\n                const uint16_t* qrow = q + ((size_t)b * Hq + hq) * D;\n                for (int d = 0; d < D; ++d) qd[d] = oracle_bf16_to_f64(qrow[d]);\n                attend_row(qd, K + (size_t)first * D,"),
     "gqa_map_modulo_prefill": ("L = p + 1;                           /* causal: keys 0..p */\n        h = hq / G;",
                                "L = p + 1;                           /* causal: keys 0..p */\n        h = hq % Hkv;"),
     "gqa_map_modulo_chunked": ("L = Lk - Lq + p + 1; /* keys 0..Lk-Lq+p */\n        h = hq / G;",
                                "L = Lk - Lq + p + 1; /* keys 0..Lk-Lq+p */\n        h = hq % Hkv;"),
     "chunk_top_left_alignment": ("L = Lk - Lq + p + 1;", "L = p + 1;"),
+    "window_one_key_wide": ("int first = L > window ? L - window : 0;",
+                            "int first = L > window ? L - window + 1 : 0;"),
+    "window_ignored": ("attend_row(qd, K + (size_t)first * D, V + (size_t)first * D, L - first,",
+                       "attend_row(qd, K, V, L,"),
     "chunk_one_key_short": ("L = Lk - Lq + p + 1;", "L = Lk - Lq + p;"),
     "cache_layout_row_major_heads": ("return (((size_t)block * Hkv + h) * bs + row) * D + d;",
                                      "return (((size_t)block * bs + row) * Hkv + h) * D + d;"),
