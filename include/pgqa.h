@@ -39,8 +39,9 @@
  *    log of the sum of exp(score) over the attended keys.
  *  - All calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream) and run on the current CUDA device.
- *  - Supported now: head_dim 64 or 128, block_size 16, 1 <= num_q_heads /
- *    num_kv_heads <= 8 for decode (any group size for prefill), bf16 q/out.
+ *  - Supported now: head_dim 64 or 128, bf16 q/out; block_size 8, 16 or 32
+ *    and 1 <= num_q_heads / num_kv_heads <= 8 for decode; block_size 16 and
+ *    any group size for prefill; any block_size for kv_cache_write.
  *
  * Errors
  *  - Argument errors found on the host return a negative pgqa_status_t and
@@ -163,6 +164,9 @@ size_t pgqa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_head
  *   q             [num_seqs][num_q_heads][head_dim] bf16, read.
  *   block_tables  [num_seqs][max_blocks_per_seq] int32, read.
  *   context_lens  [num_seqs] int32, read; 0 gives out = 0, lse = -inf.
+ *   block_size    8, 16 or 32 tokens (PGQA_EUNSUPPORTED otherwise); the kernel
+ *                 reads 16-token pages: half a 32-token block, or two 8-token
+ *                 blocks whose ids are checked separately.
  *   scale         softmax scale (usually 1/sqrt(head_dim)).
  *   cache_dtype, k_scale, v_scale   as for pgqa_kv_cache_write.
  *   max_context_len  an upper bound on context_lens; a longer context is a

@@ -286,10 +286,12 @@ static pgqa_status_t decode_call(void* out, float* lse, const void* q, const voi
     return PGQA_EUNSUPPORTED;
   }
   const int group = num_q_heads / num_kv_heads;
-  if (group > 8 || block_size != 16) return PGQA_EUNSUPPORTED;
+  if (group > 8 || (block_size != 8 && block_size != 16 && block_size != 32))
+    return PGQA_EUNSUPPORTED;
   if (!(head_dim == 128 || (head_dim == 64 && cache_dtype == PGQA_DTYPE_BF16)))
     return PGQA_EUNSUPPORTED;
-  if (static_cast<int64_t>(num_blocks) * num_kv_heads * 16 > INT32_MAX) return PGQA_EUNSUPPORTED;
+  if (static_cast<int64_t>(num_blocks) * num_kv_heads * block_size > INT32_MAX)
+    return PGQA_EUNSUPPORTED;
   if (num_seqs == 0) return PGQA_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PGQA_EINVAL;
   if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))

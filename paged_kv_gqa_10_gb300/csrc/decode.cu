@@ -74,6 +74,7 @@ struct DecodeParams {
   int num_seqs, num_q_heads, num_kv_heads, group;
   int num_blocks;
   int max_context_len;
+  int block_size;    // 8, 16 or 32 tokens per block; the kernel works on 16-token pages
   int window;        // > 0: each context's last `window` keys only
   float scale_log2;  // scale * log2(e)
 };
@@ -97,7 +98,8 @@ struct Cfg {
                                                                       // unit_done[2], merge_free[2]
   static constexpr int kOffMeta = kOffBar + (2 * kStages + 4) * 8;    // [S] int
   static constexpr int kOffY = kOffMeta + kStages * 4;                // [kYRing] int
-  static constexpr int kOffMisc = kOffY + kYRing * 4;                 // 32 ints, kScanSlots int64
+  static constexpr int kOffY2 = kOffY + kYRing * 4;                   // [kYRing] int (block 8)
+  static constexpr int kOffMisc = kOffY2 + kYRing * 4;                // 32 ints, kScanSlots int64
   static constexpr int kSmem = 1024 + kOffMisc + 32 * 4 + kScanSlots * 8;
   static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle rows");
 };
@@ -119,7 +121,8 @@ __device__ __forceinline__ int first_key(const DecodeParams& p, int L) {
 __device__ __forceinline__ int pages_of(const DecodeParams& p, int b, bool* valid = nullptr) {
   const int L = __ldg(p.context_lens + b);
   const int n = (L + 15) >> 4;
-  const bool ok = L >= 0 && L <= p.max_context_len && n <= p.max_blocks_per_seq;
+  const bool ok = L >= 0 && L <= p.max_context_len &&
+                  (L + p.block_size - 1) / p.block_size <= p.max_blocks_per_seq;
   if (valid) *valid = ok;
   return ok && L > 0 ? n - (first_key(p, L) >> 4) : 0;
 }
@@ -168,7 +171,8 @@ __device__ __forceinline__ long long block_scan(long long v, long long* scratch,
 // A CTA's walk over units: unit (b, h) holds pages [S, S + P) of the global order.
 struct Walk {
   int b, h, P;
-  int fp;  // logical page of the unit's first page read
+  int fp;  // 16-token page of the unit's first page read
+  int L;   // the sequence's context length
   long long S;
   __device__ __forceinline__ void next(const DecodeParams& p) {
     S += P;
@@ -179,6 +183,7 @@ struct Walk {
         P = b < p.num_seqs ? pages_of(p, b) : 0;
       } while (P == 0 && b < p.num_seqs);
       fp = b < p.num_seqs ? first_page(p, b) : 0;
+      L = b < p.num_seqs ? __ldg(p.context_lens + b) : 0;
     }
   }
 };
@@ -349,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
   uint64_t* merge_free = unit_done + 2;  // [2] the merge warp has read them
   int* meta = reinterpret_cast<int*>(smem + C::kOffMeta);  // per stage: bad block id seen
   int* yring = reinterpret_cast<int*>(smem + C::kOffY);    // row coordinate of page i % kYRing
+  int* yring2 = reinterpret_cast<int*>(smem + C::kOffY2);  // its second 8-row block (block 8)
   int* misc = reinterpret_cast<int*>(smem + C::kOffMisc);
   long long* scratch = reinterpret_cast<long long*>(misc + 32);  // kScanSlots slots
 
@@ -405,6 +411,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
   w0.b = misc[0];
   w0.P = pages_of(p, w0.b);
   w0.fp = first_page(p, w0.b);
+  w0.L = __ldg(p.context_lens + w0.b);
   w0.h = static_cast<int>((r0 - scratch[kScanSlots - 1]) / w0.P);
   w0.S = scratch[kScanSlots - 1] + static_cast<long long>(w0.h) * w0.P;
 
@@ -441,11 +448,20 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
       if (fetched < n && fetched < pend + kYRing - 32) {
         const int cnt = min(32, min(fw.P - fpg, n - fetched));
         if (lane < cnt) {
-          const int32_t pbn =
-              __ldg(p.block_tables + static_cast<size_t>(fw.b) * p.max_blocks_per_seq + fw.fp +
-                    fpg + lane);
-          yring[(fetched + lane) % kYRing] =
-              (pbn < 0 || pbn >= p.num_blocks) ? -1 : (pbn * Hkv + fw.h) * 16;
+          // cache rows of 16-token page lp: one block of 16, half of a block of 32, or
+          // two blocks of 8 (the second only if the context reaches it)
+          const int32_t* btb = p.block_tables + static_cast<size_t>(fw.b) * p.max_blocks_per_seq;
+          const int lp = fw.fp + fpg + lane, bs = p.block_size;
+          const int blk = bs == 32 ? lp >> 1 : bs == 8 ? 2 * lp : lp;
+          const int32_t pbn = __ldg(btb + blk);
+          const bool ok0 = pbn >= 0 && pbn < p.num_blocks;
+          int y0 = ok0 ? (pbn * Hkv + fw.h) * bs + (bs == 32 ? (lp & 1) * 16 : 0) : -1, y1 = 0;
+          if (bs == 8) {
+            const int32_t pbn1 = (blk + 1) * 8 < fw.L ? __ldg(btb + blk + 1) : pbn;
+            y1 = (pbn1 >= 0 && pbn1 < p.num_blocks) ? (pbn1 * Hkv + fw.h) * 8 : -1;
+          }
+          yring[(fetched + lane) % kYRing] = y0;
+          yring2[(fetched + lane) % kYRing] = y1;
         }
         fetched += cnt;
         fpg += cnt;
@@ -461,23 +477,35 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
         const int i = lane + kNW * next_li;
         const int s = lane * SPW + next_li % SPW, use = next_li / SPW;
         if (i < fetched && (use == 0 || mbar_try_wait(&empty[s], (use - 1) & 1))) {
-          int y = yring[i % kYRing];
+          int y = yring[i % kYRing], y1 = yring2[i % kYRing];
           int bad = 0;
-          if (y < 0) {
+          if (y < 0 || y1 < 0) {
             bad = 1;
-            y = 0;  // load a valid page; the unit's result is discarded
+            y = y1 = 0;  // load a valid page; the unit's result is discarded
             record_status(p.dev_status, PGQA_EBADINDEX);
           }
           meta[s] = bad;
           uint8_t* st = ring + s * C::kStageBytes;
           mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+          if (p.block_size != 8) {  // one 16-row box per 128-byte column block
 #pragma unroll
-          for (int sub = 0; sub < C::kSub; ++sub)
-            tma_load_2d(st + sub * 2048, &kmap, &full[s], sub * (128 / C::kElem), y);
+            for (int sub = 0; sub < C::kSub; ++sub)
+              tma_load_2d(st + sub * 2048, &kmap, &full[s], sub * (128 / C::kElem), y);
 #pragma unroll
-          for (int sub = 0; sub < C::kSub; ++sub)
-            tma_load_2d(st + C::kPageBytes + sub * 2048, &vmap, &full[s],
-                        sub * (128 / C::kElem), y);
+            for (int sub = 0; sub < C::kSub; ++sub)
+              tma_load_2d(st + C::kPageBytes + sub * 2048, &vmap, &full[s],
+                          sub * (128 / C::kElem), y);
+          } else {  // two 8-row boxes (rows 8-15 land 1 KB in: same swizzle phase)
+#pragma unroll
+            for (int sub = 0; sub < C::kSub; ++sub) {
+              tma_load_2d(st + sub * 2048, &kmap, &full[s], sub * (128 / C::kElem), y);
+              tma_load_2d(st + sub * 2048 + 1024, &kmap, &full[s], sub * (128 / C::kElem), y1);
+              tma_load_2d(st + C::kPageBytes + sub * 2048, &vmap, &full[s],
+                          sub * (128 / C::kElem), y);
+              tma_load_2d(st + C::kPageBytes + sub * 2048 + 1024, &vmap, &full[s],
+                          sub * (128 / C::kElem), y1);
+            }
+          }
           ++next_li;
           progress = true;
         }
@@ -764,11 +792,12 @@ pgqa_status_t launch_variant(const DecodeArgs& a, const DecodePlan& plan) {
   using C = Cfg<D, kFp8>;
   const CUtensorMapDataType dt =
       kFp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.num_kv_heads * 16;
+  const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.num_kv_heads * a.block_size;
+  const uint32_t box_rows = a.block_size == 8 ? 8 : 16;
   CUtensorMap kmap, vmap;
-  if (!tensor_map_2d(&kmap, a.k_cache, dt, D, rows, C::kRowBytes, 128 / C::kElem, 16,
+  if (!tensor_map_2d(&kmap, a.k_cache, dt, D, rows, C::kRowBytes, 128 / C::kElem, box_rows,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tensor_map_2d(&vmap, a.v_cache, dt, D, rows, C::kRowBytes, 128 / C::kElem, 16,
+      !tensor_map_2d(&vmap, a.v_cache, dt, D, rows, C::kRowBytes, 128 / C::kElem, box_rows,
                      CU_TENSOR_MAP_SWIZZLE_128B))
     return PGQA_ECUDA;
   if (!smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<D, kFp8>), C::kSmem))
@@ -794,6 +823,7 @@ pgqa_status_t launch_variant(const DecodeArgs& a, const DecodePlan& plan) {
   p.num_blocks = a.num_blocks;
   p.max_context_len = a.max_context_len;
   p.window = a.window;
+  p.block_size = a.block_size;
   p.scale_log2 = a.scale * kLog2e;
   if (launch_after_previous(paged_decode_kernel<D, kFp8>, dim3(plan.grid), dim3(kThreads),
                             C::kSmem, a.stream, kmap, vmap, p) != cudaSuccess)

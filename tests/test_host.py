@@ -80,7 +80,9 @@ def _call_decode(**over):
     (dict(Hq=7), pgqa.EINVAL),                 # heads not a multiple of kv heads
     (dict(Hq=32, Hkv=2), pgqa.EUNSUPPORTED),   # group of 16
     (dict(D=96), pgqa.EUNSUPPORTED),
-    (dict(bs=32), pgqa.EUNSUPPORTED),
+    (dict(bs=64), pgqa.EUNSUPPORTED),          # decode reads 8-, 16- and 32-token blocks
+    (dict(bs=4), pgqa.EUNSUPPORTED),
+    (dict(bs=32, NB=1 << 25), pgqa.EUNSUPPORTED),  # cache rows past int32
     (dict(dtype=7), pgqa.EUNSUPPORTED),
     (dict(dtype=1), pgqa.EINVAL),              # E4M3 without scales
     (dict(ks=1 << 20, vs=1 << 20), pgqa.EINVAL),  # scales given for bf16

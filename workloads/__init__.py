@@ -423,6 +423,23 @@ def kv_read_bytes(inp: DecodeInputs, unique: bool = False) -> int:
     return sum(seen.values()) * row
 
 
+def chunked_flops(inp: "ChunkedPrefillInputs") -> int:
+    """Useful FLOPs of a prefill over a cached prefix: chunk position p attends to
+    Lk - Lq + p + 1 keys (QK^T and PV, 2 flops per multiply-add each)."""
+    Hq, D = inp.q.shape[1], inp.q.shape[2]
+    total = 0
+    for Lq, Lk in zip(inp.lens_q, inp.seq_lens_k.tolist()):
+        pairs = Lq * (Lk - Lq) + Lq * (Lq + 1) // 2
+        total += 4 * Hq * D * pairs
+    return total
+
+
+def chunked_kv_bytes(inp: "ChunkedPrefillInputs") -> int:
+    """K and V bytes of every cached key of every sequence, read once per kv-head."""
+    Hkv, D = inp.key.shape[1], inp.key.shape[2]
+    return int(inp.seq_lens_k.sum()) * Hkv * D * 2 * 2
+
+
 def causal_flops(seq_lens: Sequence[int], num_q_heads: int, head_dim: int) -> int:
     """Useful FLOPs of causal prefill: 2 matmuls x 2 flop per multiply-add over the
     unmasked (query, key) pairs, L(L+1)/2 per sequence and query head."""
