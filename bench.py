@@ -440,6 +440,121 @@ def measure_prefill(args, dev):
     }
 
 
+def measure_cached_prefix(args, dev):
+    """The rows past prefill and decode: prefill over a cached prefix (chunked prefill)
+    and speculative verification (5 tokens per sequence), each through
+    pgqa_paged_prefill_varlen_kv; the K/V are written once, then a CUDA graph of back to
+    back launches is timed with events."""
+    import paged_kv_gqa_10_gb300 as pgqa
+    hbm, bf16_peak, kind = _peaks()
+    res = {}
+    for name, make in (("chunked_prefill", workloads.chunked_prefill),
+                       ("speculative_verify", workloads.speculative_verify)):
+        inp = make()
+        kc, vc = inp.k_cache.to(dev), inp.v_cache.to(dev)
+        q, bt = inp.q.to(dev), inp.block_tables.to(dev)
+        cu, lk = inp.cu_seqlens_q.to(dev), inp.seq_lens_k.to(dev)
+        T, Hq, D = inp.q.shape
+        out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws = torch.zeros(pgqa.prefill_workspace_size(inp.num_seqs, Hq, inp.max_seqlen_q),
+                         dtype=torch.uint8, device=dev)
+        pgqa.kv_cache_write(inp.key.to(dev), inp.value.to(dev), inp.slot_mapping.to(dev), kc, vc,
+                            dev_status=status)
+
+        def call():
+            pgqa.paged_prefill_varlen_kv(out, lse, q, kc, vc, bt, cu, lk, inp.max_seqlen_q,
+                                         inp.max_seqlen_k, inp.scale, workspace=ws,
+                                         dev_status=status)
+
+        for _ in range(args.warmup):
+            call()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        reps = 8
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                call()
+        g.replay()
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = max(2, args.steps // 10)
+        e0.record(stream)
+        for _ in range(n):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        ms = e0.elapsed_time(e1) / (n * reps)
+        flops = workloads.chunked_flops(inp)
+        kvb = workloads.chunked_kv_bytes(inp)
+        tflops = flops / (ms * 1e-3) / 1e12
+        gbs = kvb / (ms * 1e-3) / 1e9
+        entry = {"workload": inp.name, "ms": ms, "flops": flops, "TFLOP/s": tflops,
+                 "kv_bytes": kvb, "KV GB/s": gbs,
+                 "call": "pgqa_paged_prefill_varlen_kv, a CUDA graph of back-to-back launches "
+                         f"over the same {kvb / 1e6:.0f} MB of K/V (part of it may still be in "
+                         "the 129 MB L2 from the previous launch)"}
+        if name == "chunked_prefill":
+            entry["roofline"] = {"bound": "tensor", "achieved": tflops, "peak": bf16_peak,
+                                 "unit": "TFLOP/s", "frac": tflops / bf16_peak,
+                                 "peak_kind": kind + " bf16 burst (cuBLAS)"}
+        else:
+            entry["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                                 "frac": gbs / hbm, "peak_kind": kind}
+        res[name] = entry
+    return res
+
+
+def measure_window_decode(args, dev, window=2048):
+    """Sliding-window decode on the 70B-shaped batch (contexts U[1024, 4096], window
+    2048 keys): a CUDA graph of back-to-back launches cycling over the rotating table
+    sets (no launch finds the previous one's pages in L2), KV bytes of the window."""
+    import paged_kv_gqa_10_gb300 as pgqa
+    inp = workloads.llama70b_decode(rotations=ROTATIONS)
+    b = DecodeBench(inp, dev)
+    for r in range(b.R):
+        b.append(r)
+    elem = 2
+    row = inp.num_kv_heads * inp.head_dim * elem * 2
+    kvb = sum(min(L, window) for L in inp.context_lens.tolist()) * row
+
+    def call(r):
+        pgqa.paged_attention_decode_window(b.out, b.lse, b.q, b.kc, b.vc, b.bts[r], b.cl,
+                                           inp.scale, window, inp.max_context_len,
+                                           workspace=b.ws, dev_status=b.status)
+
+    for i in range(args.warmup):
+        call(i % b.R)
+    b.check()
+    n_rep = 4 * b.R
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n_rep):
+            call(i % b.R)
+    g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(1, args.steps // 4)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    b.check()
+    ms = e0.elapsed_time(e1) / (reps * n_rep)
+    gbs = kvb / (ms * 1e-3) / 1e9
+    hbm, _, kind = _peaks()
+    return {"workload": f"sliding-window decode, window {window}: " + inp.name, "ms": ms,
+            "kv_bytes": kvb, "KV GB/s": gbs,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": gbs / hbm, "peak_kind": kind}}
+
+
 DECODE_WORKLOADS = {
     "llama3_8b": (lambda: workloads.llama3_8b_decode(rotations=ROTATIONS), WORKLOAD),
     "70b_bf16": (lambda: workloads.llama70b_decode(rotations=ROTATIONS),
@@ -501,6 +616,8 @@ def run_ours(args):
     }
     if pref is not None:
         line["prefill"] = pref
+        line["next"] = measure_cached_prefix(args, dev)
+        line["next"]["sliding_window_decode"] = measure_window_decode(args, dev)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = _cpu_baseline(inp, args.cpu_seconds)
     print(json.dumps(line), flush=True)
