@@ -509,6 +509,52 @@ def measure_cached_prefix(args, dev):
     return res
 
 
+def measure_e4m3_prefill(args, dev):
+    """The varlen causal prefill workload over an E4M3 cache (per-kv-head scales
+    amax / 448, written once by the cache-write kernel), timed per launch with events
+    like the bf16 prefill."""
+    import paged_kv_gqa_10_gb300 as pgqa
+    _, bf16_peak, kind = _peaks()
+    inp = workloads.varlen_prefill()
+    kc, vc, ks, vs = (t.to(dev) for t in workloads.e4m3_prefill_cache(inp))
+    q, bt, cu = inp.q.to(dev), inp.block_tables.to(dev), inp.cu_seqlens.to(dev)
+    T, Hq, D = inp.q.shape
+    out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.zeros(pgqa.prefill_workspace_size(inp.num_seqs, Hq, inp.max_seqlen),
+                     dtype=torch.uint8, device=dev)
+    pgqa.kv_cache_write(inp.key.to(dev), inp.value.to(dev), inp.slot_mapping.to(dev), kc, vc,
+                        k_scale=ks, v_scale=vs, dev_status=status)
+
+    def call():
+        pgqa.paged_prefill_varlen_e4m3(out, lse, q, kc, vc, bt, cu, None, inp.max_seqlen, 0,
+                                       inp.scale, ks, vs, workspace=ws, dev_status=status)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    stream = torch.cuda.current_stream()
+    n = max(3, args.steps // 5)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for i in range(n):
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ms = sum(e[0].elapsed_time(e[1]) for e in ev) / n
+    flops = workloads.causal_flops(inp.seq_lens, Hq, D)
+    tflops = flops / (ms * 1e-3) / 1e12
+    return {"workload": inp.name + ", E4M3 cache", "ms": ms, "flops": flops,
+            "TFLOP/s": tflops, "call": "pgqa_paged_prefill_varlen_e4m3, events around each launch",
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16_peak,
+                         "unit": "TFLOP/s", "frac": tflops / bf16_peak,
+                         "peak_kind": kind + " bf16 burst (cuBLAS); the MMAs run on f16 "
+                                             "operands at the same nominal rate"}}
+
+
 def measure_window_decode(args, dev, window=2048):
     """Sliding-window decode on the 70B-shaped batch (contexts U[1024, 4096], window
     2048 keys): a CUDA graph of back-to-back launches cycling over the rotating table
@@ -618,6 +664,7 @@ def run_ours(args):
         line["prefill"] = pref
         line["next"] = measure_cached_prefix(args, dev)
         line["next"]["sliding_window_decode"] = measure_window_decode(args, dev)
+        line["next"]["e4m3_prefill"] = measure_e4m3_prefill(args, dev)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = _cpu_baseline(inp, args.cpu_seconds)
     print(json.dumps(line), flush=True)

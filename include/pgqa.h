@@ -41,7 +41,8 @@
  *    default stream) and run on the current CUDA device.
  *  - Supported now: head_dim 64 or 128, bf16 q/out; block_size 8, 16 or 32
  *    and 1 <= num_q_heads / num_kv_heads <= 8 for decode; block_size 16 and
- *    any group size for prefill; any block_size for kv_cache_write.
+ *    any group size for prefill (bf16 or E4M3 cache); any block_size for
+ *    kv_cache_write.
  *
  * Errors
  *  - Argument errors found on the host return a negative pgqa_status_t and
@@ -268,8 +269,8 @@ size_t pgqa_prefill_workspace_size(int num_seqs, int num_q_heads, int max_seqlen
  *                 bytes, 16-byte aligned; its first 256 bytes ZERO-FILLED before
  *                 its first use (every call that completes leaves them zero).
  *                 Calls sharing a workspace must not overlap in time.
- * bf16 cache only; q/out/k_cache/v_cache 16-byte aligned. Inconsistent
- * cu_seqlens (negative lengths, a length above max_seqlen or beyond the block
+ * bf16 cache (an E4M3 one: pgqa_paged_prefill_varlen_e4m3); q/out/k_cache/v_cache
+ * 16-byte aligned. Inconsistent cu_seqlens (negative lengths, a length above max_seqlen or beyond the block
  * table, a last entry other than num_tokens) are a device error (PGQA_EINVAL in
  * *dev_status); nothing is written for the sequences concerned.
  */
@@ -310,6 +311,28 @@ pgqa_status_t pgqa_paged_prefill_varlen_kv(void* out, float* lse, const void* q,
                                            int num_blocks, int block_size, float scale,
                                            void* workspace, size_t workspace_bytes,
                                            int* dev_status, void* stream);
+
+/*
+ * Prefill over an E4M3 cache: pgqa_paged_prefill_varlen_kv over a cache written by
+ * pgqa_kv_cache_write with cache_dtype PGQA_DTYPE_E4M3 (the FP8 cache the rkmt.cn
+ * article pairs with GQA, ch. 1; stored value = code * scale_h per kv-head).
+ *   seq_lens_k    [num_seqs] int32 as for pgqa_paged_prefill_varlen_kv, or NULL for
+ *                 no cached prefix (Lk = Lq; max_seqlen_k is then ignored).
+ *   k_scale, v_scale  [num_kv_heads] fp32 device arrays, read; every entry must be
+ *                 positive and finite (else PGQA_EINVAL in *dev_status).
+ * Arithmetic: the codes are widened exactly to f16 and q is rounded to f16 (exact
+ * for |q| in [2^-14, 65504]); scores and the output accumulate in fp32, P is
+ * rounded to f16 for the P V product; out is rounded to bf16.
+ * Every other argument, the workspace and the error behaviour are as for
+ * pgqa_paged_prefill_varlen_kv.
+ */
+pgqa_status_t pgqa_paged_prefill_varlen_e4m3(
+    void* out, float* lse, const void* q, int num_tokens, const void* k_cache,
+    const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* cu_seqlens_q, const int32_t* seq_lens_k, int num_seqs, int max_seqlen_q,
+    int max_seqlen_k, int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
+    int block_size, float scale, const float* k_scale, const float* v_scale, void* workspace,
+    size_t workspace_bytes, int* dev_status, void* stream);
 
 #ifdef __cplusplus
 }

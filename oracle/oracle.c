@@ -285,7 +285,8 @@ int oracle_paged_decode(const uint16_t* q, const void* k_cache, const void* v_ca
  * attends to keys 0..p of sequence i, read through block_tables[i].
  * rows: optional list of n_rows (token, q_head) pairs to compute (int32 pairs);
  * NULL computes every (token, head). out: [T][Hq][D] double, lse: [T][Hq] double
- * (only the requested rows are written). bf16 cache only. */
+ * (only the requested rows are written). dtype/k_scale/v_scale as for
+ * oracle_paged_decode (an E4M3 cache is dequantised per kv-head). */
 int oracle_paged_prefill(const uint16_t* q, const void* k_cache, const void* v_cache, int dtype,
                          const float* k_scale, const float* v_scale, const int32_t* block_tables,
                          int max_blocks_per_seq, const int32_t* cu_seqlens, int num_seqs, int Hq,

@@ -71,6 +71,8 @@ def _load():
                                        SZ, P, P], I),
         "pgqa_paged_prefill_varlen_kv": ([P, P, P, I, P, P, P, I, P, P, I, I, I, I, I, I, I, I,
                                           F, P, SZ, P, P], I),
+        "pgqa_paged_prefill_varlen_e4m3": ([P, P, P, I, P, P, P, I, P, P, I, I, I, I, I, I, I,
+                                            I, F, P, P, P, SZ, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -339,3 +341,33 @@ def paged_prefill_varlen_kv(out, lse, q, k_cache, v_cache, block_tables, cu_seql
         int(max_seqlen_k), Hq, Hkv, D, NB, bs, float(scale), _ptr(workspace), ws_bytes,
         _ptr(dev_status), _stream(stream))
     _check(rc, "paged_prefill_varlen_kv")
+
+
+def paged_prefill_varlen_e4m3(out, lse, q, k_cache, v_cache, block_tables, cu_seqlens_q,
+                              seq_lens_k, max_seqlen_q, max_seqlen_k, scale, k_scale, v_scale,
+                              workspace=None, dev_status=None, stream=None):
+    """Prefill over an E4M3 cache (uint8 codes, per-kv-head k_scale / v_scale [Hkv]
+    fp32). seq_lens_k None: no cached prefix (whole-sequence causal prefill, and
+    max_seqlen_k is ignored); else as paged_prefill_varlen_kv."""
+    _dev(out, "out", torch.bfloat16)
+    _dev(lse, "lse", torch.float32)
+    _dev(q, "q", torch.bfloat16)
+    _dev(k_cache, "k_cache", torch.uint8)
+    _dev(v_cache, "v_cache", torch.uint8)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    _dev(seq_lens_k, "seq_lens_k", torch.int32)
+    _dev(k_scale, "k_scale", torch.float32)
+    _dev(v_scale, "v_scale", torch.float32)
+    _dev(workspace, "workspace")
+    _dev(dev_status, "dev_status", torch.int32)
+    T, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    S = cu_seqlens_q.shape[0] - 1
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = _handle().pgqa_paged_prefill_varlen_e4m3(
+        _ptr(out), _ptr(lse), _ptr(q), T, _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(cu_seqlens_q), _ptr(seq_lens_k), S, int(max_seqlen_q),
+        int(max_seqlen_k), Hq, Hkv, D, NB, bs, float(scale), _ptr(k_scale), _ptr(v_scale),
+        _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
+    _check(rc, "paged_prefill_varlen_e4m3")

@@ -366,20 +366,29 @@ size_t pgqa_prefill_workspace_size(int num_seqs, int num_q_heads, int max_seqlen
   return pgqa::kPrefillWorkspaceBytes;
 }
 
-// Shared by both prefill entry points (seq_lens_k null: no cached prefix).
+// Shared by the prefill entry points (seq_lens_k null: no cached prefix).
 static pgqa_status_t prefill_call(void* out, float* lse, const void* q, int num_tokens,
                                   const void* k_cache, const void* v_cache,
                                   const int32_t* block_tables, int max_blocks_per_seq,
                                   const int32_t* cu_seqlens, const int32_t* seq_lens_k,
                                   int num_seqs, int max_seqlen, int max_seqlen_k,
                                   int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
-                                  int block_size, float scale, void* workspace,
+                                  int block_size, float scale, int cache_dtype,
+                                  const float* k_scale, const float* v_scale, void* workspace,
                                   size_t workspace_bytes, int* dev_status, void* stream) {
   if (num_seqs < 0 || max_seqlen < 0 || max_seqlen_k < 0 || num_tokens < 0 || num_q_heads <= 0 ||
       num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || block_size <= 0 ||
       max_blocks_per_seq < 0 || !isfinite(scale) || !(scale > 0.f))
     return PGQA_EINVAL;
   if (num_q_heads % num_kv_heads != 0) return PGQA_EINVAL;
+  if (cache_dtype == PGQA_DTYPE_E4M3) {
+    if (k_scale == nullptr || v_scale == nullptr) return PGQA_EINVAL;
+    if (!aligned(k_scale, 4) || !aligned(v_scale, 4)) return PGQA_EINVAL;
+  } else if (cache_dtype == PGQA_DTYPE_BF16) {
+    if (k_scale != nullptr || v_scale != nullptr) return PGQA_EINVAL;
+  } else {
+    return PGQA_EUNSUPPORTED;
+  }
   if (head_dim != 128 && head_dim != 64) return PGQA_EUNSUPPORTED;
   if (block_size != 16) return PGQA_EUNSUPPORTED;
   if (static_cast<int64_t>(num_blocks) * num_kv_heads * 16 > INT32_MAX) return PGQA_EUNSUPPORTED;
@@ -414,6 +423,9 @@ static pgqa_status_t prefill_call(void* out, float* lse, const void* q, int num_
   a.num_blocks = num_blocks;
   a.block_size = block_size;
   a.scale = scale;
+  a.cache_dtype = cache_dtype;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   a.dev_status = dev_status;
   a.stream = static_cast<cudaStream_t>(stream);
   return pgqa::launch_paged_prefill(a);
@@ -430,7 +442,8 @@ pgqa_status_t pgqa_paged_prefill_varlen(void* out, float* lse, const void* q, in
   return prefill_call(out, lse, q, num_tokens, k_cache, v_cache, block_tables,
                       max_blocks_per_seq, cu_seqlens, nullptr, num_seqs, max_seqlen, max_seqlen,
                       num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale,
-                      workspace, workspace_bytes, dev_status, stream);
+                      PGQA_DTYPE_BF16, nullptr, nullptr, workspace, workspace_bytes, dev_status,
+                      stream);
 }
 
 pgqa_status_t pgqa_paged_prefill_varlen_kv(void* out, float* lse, const void* q, int num_tokens,
@@ -446,7 +459,23 @@ pgqa_status_t pgqa_paged_prefill_varlen_kv(void* out, float* lse, const void* q,
   return prefill_call(out, lse, q, num_tokens, k_cache, v_cache, block_tables,
                       max_blocks_per_seq, cu_seqlens_q, seq_lens_k, num_seqs, max_seqlen_q,
                       max_seqlen_k, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size,
-                      scale, workspace, workspace_bytes, dev_status, stream);
+                      scale, PGQA_DTYPE_BF16, nullptr, nullptr, workspace, workspace_bytes,
+                      dev_status, stream);
+}
+
+pgqa_status_t pgqa_paged_prefill_varlen_e4m3(
+    void* out, float* lse, const void* q, int num_tokens, const void* k_cache,
+    const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* cu_seqlens_q, const int32_t* seq_lens_k, int num_seqs, int max_seqlen_q,
+    int max_seqlen_k, int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
+    int block_size, float scale, const float* k_scale, const float* v_scale, void* workspace,
+    size_t workspace_bytes, int* dev_status, void* stream) {
+  if (k_scale == nullptr || v_scale == nullptr) return PGQA_EINVAL;
+  return prefill_call(out, lse, q, num_tokens, k_cache, v_cache, block_tables,
+                      max_blocks_per_seq, cu_seqlens_q, seq_lens_k, num_seqs, max_seqlen_q,
+                      seq_lens_k ? max_seqlen_k : max_seqlen_q, num_q_heads, num_kv_heads,
+                      head_dim, num_blocks, block_size, scale, PGQA_DTYPE_E4M3, k_scale, v_scale,
+                      workspace, workspace_bytes, dev_status, stream);
 }
 
 }  // extern "C"

@@ -112,6 +112,9 @@ struct PrefillArgs {
   int num_tokens;
   int num_seqs, max_seqlen, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size;
   float scale;
+  int cache_dtype;        // PGQA_DTYPE_BF16 or PGQA_DTYPE_E4M3
+  const float* k_scale;   // [num_kv_heads], E4M3 only
+  const float* v_scale;
   int* dev_status;
   cudaStream_t stream;
 };

@@ -48,6 +48,20 @@
 //    the first 64 columns of S_X, O rescaled in TMEM only when the running max grows
 //    by more than 2^8 (exact either way: P and l use the same reference max); at the
 //    end O / l -> bf16 out and lse.
+// E4M3 cache (per-kv-head scales; stored value = code * scale_h)
+//  - The MMAs run on f16 operands: every E4M3 code is exactly an f16, q is rounded
+//    to f16 once (exact for |q| in f16's normal range), P is written as f16, and the
+//    scales leave the MMAs: k_scale_h multiplies the softmax scale, v_scale_h the
+//    output (1/l becomes v_scale_h/l).
+//  - The TMA warp loads a tile's codes (8 pages of 16 rows, unswizzled) into its
+//    ring slot, where the f16 tile will be: rows 0-63 and 64-127 each into a part of
+//    the slot that only the f16 rows of the same half overwrite. Warps 10 and 11
+//    (the planner's work moves to the TMA warp) then each widen one half of the
+//    rows in place: load all of the half's codes, convert, store the f16 rows in
+//    the 128-byte-swizzled K-major layout TMA would have written (rows past the
+//    sequence end as zeros), and arrive on the slot's `converted` barrier, which
+//    the MMA warp waits for instead of the TMA one. They also convert Q_A and Q_B
+//    from bf16 to f16 in place before the item's first S MMAs.
 // All waits are bounded (a wait that gives up records PGQA_ETIMEOUT).
 #include <cuda_bf16.h>
 
@@ -74,12 +88,16 @@ static_assert(256 + (kMaxSeqs + 2 * kMaxLevels) * 4 == kPrefillWorkspaceBytes,
 template <int D>
 struct PCfg {
   static constexpr int kSub = D / 64;        // 128-byte (64-element) column blocks
-  static constexpr int kTile = 128 * D * 2;  // [128 rows][D] bf16
+  static constexpr int kTile = 128 * D * 2;  // [128 rows][D] bf16 (f16 for an E4M3 cache)
   static constexpr int kStages = D == 128 ? 5 : 8;  // K/V ring: 160 KB / 128 KB
   static constexpr int kQ = 0;               // Q_A, Q_B
   static constexpr int kRing = 2 * kTile;    // kStages K/V tiles, in load order
   static constexpr int kBar = kRing + kStages * kTile;
   static constexpr int kSmem = 1024 + kBar + 512;
+  // E4M3 codes of rows 64h .. 64h+63 (D bytes each) inside a ring slot: where only
+  // the f16 rows of the same half land (D = 128: under f16 columns 64..127 of the
+  // same rows; D = 64: the second quarter of half h's f16 rows)
+  __host__ __device__ static constexpr int code_half(int h) { return D == 128 ? 16384 + 8192 * h : 8192 * h + 4096; }
 };
 
 // Scratch in the ring while the tables are built (before any tile is loaded).
@@ -160,6 +178,69 @@ __device__ __forceinline__ Item item_of(const PrefillParams& p, int t, int& lvl)
   seq_ok(p, w.seq, &w.start, &w.Lq, &w.Lk);
   w.bad = 0;
   return w;
+}
+
+// Ticket t decoded, with the block ids its key tiles read checked (warp-collective;
+// t warp-uniform). Past the list: the end-of-list marker.
+__device__ __forceinline__ Item plan_item(const PrefillParams& p, int t, int total, int& lvl,
+                                          int lane) {
+  Item w{-1, 0, 0, 0, 0, 0, 0, 0, 0};
+  if (t < total) {
+    w = item_of(p, t, lvl);
+    const int32_t* bt = p.block_tables + static_cast<size_t>(w.seq) * p.max_blocks_per_seq;
+    const int npages = (min(w.Lk, w.nkt() * kBlockN) + 15) / 16;
+    bool bad = false;
+    for (int pg = lane; pg < npages; pg += 32) {  // block ids checked before Q is out
+      const int32_t pbn = __ldg(bt + pg);
+      bad |= pbn < 0 || pbn >= p.num_blocks;
+    }
+    w.bad = __any_sync(0xffffffffu, bad);
+  }
+  return w;
+}
+
+// Eight bf16 to eight f16, round to nearest even (exact in f16's normal range).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  return make_uint4(pack_f16(bf16_lo(v.x), bf16_hi(v.x)), pack_f16(bf16_lo(v.y), bf16_hi(v.y)),
+                    pack_f16(bf16_lo(v.z), bf16_hi(v.z)), pack_f16(bf16_lo(v.w), bf16_hi(v.w)));
+}
+
+// Sixteen E4M3 codes (byte i = element i) to sixteen f16 (exact), as two 8-element
+// halves.
+__device__ __forceinline__ void e4m3x16_to_f16(uint4 v, uint4& lo, uint4& hi) {
+  lo = make_uint4(e4m3x2_to_f16x2(v.x & 0xffffu), e4m3x2_to_f16x2(v.x >> 16),
+                  e4m3x2_to_f16x2(v.y & 0xffffu), e4m3x2_to_f16x2(v.y >> 16));
+  hi = make_uint4(e4m3x2_to_f16x2(v.z & 0xffffu), e4m3x2_to_f16x2(v.z >> 16),
+                  e4m3x2_to_f16x2(v.w & 0xffffu), e4m3x2_to_f16x2(v.w >> 16));
+}
+
+// Widens rows 64h .. 64h+63 of the E4M3 tile in ring slot `slot` (codes at
+// code_half(h)) to f16 in place, in the 128-byte-swizzled K-major layout (16-byte
+// chunk k of row r at chunk k ^ (r & 7) of the row's 128-byte line, 64-column blocks
+// 16 KB apart). Rows at or past `valid` (keys past the sequence end) become zeros.
+// Every code of the half is loaded before any store: the f16 rows overwrite them.
+template <int D>
+__device__ __forceinline__ void widen_tile_half(uint8_t* slot, int h, int lane, int valid) {
+  constexpr int kChunks = D / 16;             // 16-byte chunks per code row
+  constexpr int kRowsPerPass = 32 / kChunks;  // rows one warp-wide load covers
+  constexpr int kPasses = 64 / kRowsPerPass;
+  const int c = lane % kChunks, r0 = lane / kChunks;
+  const uint8_t* codes = slot + PCfg<D>::code_half(h);
+  uint4 v[kPasses];
+#pragma unroll
+  for (int i = 0; i < kPasses; ++i)
+    v[i] = *reinterpret_cast<const uint4*>(codes + (r0 + i * kRowsPerPass) * D + c * 16);
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < kPasses; ++i) {
+    const int r = 64 * h + r0 + i * kRowsPerPass;
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+    if (r < valid) e4m3x16_to_f16(v[i], lo, hi);
+    uint8_t* line = slot + (c >> 2) * 16384 + r * 128;
+    const int k0 = 2 * (c & 3);
+    *reinterpret_cast<uint4*>(line + ((k0 ^ (r & 7)) << 4)) = lo;
+    *reinterpret_cast<uint4*>(line + (((k0 + 1) ^ (r & 7)) << 4)) = hi;
+  }
 }
 
 __device__ __forceinline__ uint64_t f2(float lo, float hi) {
@@ -281,10 +362,13 @@ __device__ __forceinline__ void build_tables(const PrefillParams& p, uint8_t* sc
   }
 }
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+    const __grid_constant__ CUtensorMap vmap, const PrefillParams p,
+    const float* __restrict__ k_scale, const float* __restrict__ v_scale) {
+  // (the E4M3 scales, [num_kv_heads] each, are separate parameters: a larger
+  // parameter struct pushes the bf16 softmax past its register budget)
   using C = PCfg<D>;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -300,8 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
   uint64_t* o_full = p_full + 2;             // [2] P_X V accumulated
   uint64_t* plan_full = o_full + 2;          // [2] planner -> TMA warp item queue
   uint64_t* plan_empty = plan_full + 2;      // [2]
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(plan_empty + 2);
-  int* slots = reinterpret_cast<int*>(plan_empty + 3);  // [2][8]: the item, by item parity
+  uint64_t* q_conv = plan_empty + 2;         // E4M3: Q_A, Q_B converted to f16
+  uint64_t* conv = q_conv + 1;               // E4M3: [kStages] ring slot widened to f16
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(conv + kStages);
+  int* slots = reinterpret_cast<int*>(conv + kStages + 1);  // [2][8]: the item, by parity
   int* plans = slots + 16;                              // [2][8]: the planner's queue
   int* misc = plans + 16;                               // [0] total items
 
@@ -317,18 +403,27 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       if (!ok || (s == p.num_seqs - 1 && st + Lq != p.num_tokens))
         record_status(p.dev_status, PGQA_EINVAL);
     }
+    if constexpr (F8) {  // E4M3 scales must be positive and finite
+      for (int h = tid; h < p.num_kv_heads; h += kThreads) {
+        const float ks = __ldg(k_scale + h), vs = __ldg(v_scale + h);
+        if (!(ks > 0.f && ks < INFINITY && vs > 0.f && vs < INFINITY))
+          record_status(p.dev_status, PGQA_EINVAL);
+      }
+    }
   }
-  static_assert((2 + 2 * kStages + 10 + 1) * 8 + 32 * 4 + 16 <= 512, "barrier area");
+  static_assert((2 + 3 * kStages + 11 + 1) * 8 + 32 * 4 + 16 <= 512, "barrier area");
   build_tables(p, smem + C::kRing, misc);
   if (tid == 0) {
     mbar_init(q_full, 1);
     // Q buffers are reused once the item's last S MMAs are done (one commit) and all
-    // 8 softmax warps have taken the item (one arrival each), so q_full can never
-    // run two phases ahead of a softmax warp's wait
-    mbar_init(q_empty, 1 + 8);
+    // 8 softmax warps (and both converter warps) have taken the item (one arrival
+    // each), so q_full can never run two phases ahead of their waits
+    mbar_init(q_empty, 1 + 8 + (F8 ? 2 : 0));
+    mbar_init(q_conv, 2);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&conv[s], 2);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
@@ -375,17 +470,23 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       Item w;
       int ch0, ch1;
     };
-    int n_plans = 0;
+    int n_plans = 0, lvl = p.n_levels - 1;
     auto plan_next = [&]() {
       Plan pl;
-      pl.w = Item{-1, 0, 0, 0, 0, 0, 0, 0};
-      const int q = n_plans & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&plan_full[q], (n_plans >> 1) & 1))) {
-        ok = false;  // the end marker stands in for the item
+      pl.w = Item{-1, 0, 0, 0, 0, 0, 0, 0, 0};
+      if constexpr (F8) {  // the planner warp converts: plan here
+        int t = 0;
+        if (lane == 0) t = atomicAdd(p.ticket, 1);
+        pl.w = plan_item(p, __shfl_sync(0xffffffffu, t, 0), total, lvl, lane);
       } else {
-        pl.w = read_slot(plans + q * 8);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&plan_empty[q]);
+        const int q = n_plans & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&plan_full[q], (n_plans >> 1) & 1))) {
+          ok = false;  // the end marker stands in for the item
+        } else {
+          pl.w = read_slot(plans + q * 8);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&plan_empty[q]);
+        }
       }
       ++n_plans;
       pl.ch0 = chunk_rows(pl.w, 0);
@@ -400,15 +501,19 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         if (g >= kStages && !mbar_wait(&empty[s], ((g / kStages) - 1) & 1))
           ok = false;
         else
-          mbar_arrive_expect_tx(&full[s], C::kTile);
+          mbar_arrive_expect_tx(&full[s], F8 ? C::kTile / 2 : C::kTile);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) return;
       if (lane < 8) {
-        uint8_t* dst = smem + C::kRing + s * C::kTile + lane * 2048;
+        uint8_t* slot = smem + C::kRing + s * C::kTile;
+        if constexpr (F8) {  // the page's 16 code rows, where the widening expects them
+          tma_load_2d(slot + C::code_half(lane >> 2) + (lane & 3) * 16 * D, map, &full[s], 0, y);
+        } else {
 #pragma unroll
-        for (int sub = 0; sub < C::kSub; ++sub)
-          tma_load_2d(dst + sub * 16384, map, &full[s], sub * 64, y);
+          for (int sub = 0; sub < C::kSub; ++sub)
+            tma_load_2d(slot + lane * 2048 + sub * 16384, map, &full[s], sub * 64, y);
+        }
       }
       ++g;
     };
@@ -485,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         done &= mbar_wait(&full[i % kStages], (i / kStages) & 1);
       if (!done) record_status(p.dev_status, PGQA_ETIMEOUT);
     }
-  } else if (warp == kWarpPlan) {
+  } else if (!F8 && warp == kWarpPlan) {
     // ================================================================ planner
     // Takes tickets, decodes them and checks the items' block ids, two items ahead
     // of the TMA warp, so no table read sits on the load path.
@@ -499,19 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       }
       int t = 0;
       if (lane == 0) t = atomicAdd(p.ticket, 1);
-      t = __shfl_sync(0xffffffffu, t, 0);
-      Item w{-1, 0, 0, 0, 0, 0, 0, 0};  // the end-of-list marker unless a ticket is left
-      if (t < total) {
-        w = item_of(p, t, lvl);
-        const int32_t* bt = p.block_tables + static_cast<size_t>(w.seq) * p.max_blocks_per_seq;
-        const int npages = (min(w.Lk, w.nkt() * kBlockN) + 15) / 16;
-        bool bad = false;
-        for (int pg = lane; pg < npages; pg += 32) {  // block ids checked before Q is out
-          const int32_t pbn = __ldg(bt + pg);
-          bad |= pbn < 0 || pbn >= p.num_blocks;
-        }
-        w.bad = __any_sync(0xffffffffu, bad);
-      }
+      const Item w = plan_item(p, __shfl_sync(0xffffffffu, t, 0), total, lvl, lane);
       if (lane == 0) {
         publish(plans + q * 8, w);
         mbar_arrive(&plan_full[q]);
@@ -519,11 +612,45 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       if (w.ticket < 0) break;
     }
     if (!ok && lane == 0) record_status(p.dev_status, PGQA_ETIMEOUT);
+  } else if (F8 && warp >= kWarpPlan) {
+    // ================================================================ E4M3 widening
+    // Warp 10 + h widens rows 64h .. 64h+63 of every K/V tile, in ring order, and
+    // half of Q_A's and Q_B's bytes.
+    const int h = warp - kWarpPlan;
+    int it = 0, g = 0;
+    bool ok = true;
+    for (;;) {
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(q_full, it & 1)))) break;
+      const Item w = read_slot(slots + (it & 1) * 8);
+      ++it;
+      if (w.ticket < 0) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_empty);
+      for (int X = 0; X < (w.active_b ? 2 : 1); ++X) {
+        uint4* qx = reinterpret_cast<uint4*>(smem + C::kQ + X * C::kTile + h * (C::kTile / 2));
+#pragma unroll 4
+        for (int i = lane; i < C::kTile / 32; i += 32) qx[i] = bf16x8_to_f16x8(qx[i]);
+      }
+      fence_proxy_async_smem();  // the MMAs read what these generic stores wrote
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_conv);
+      const int nkt = w.nkt();
+      for (int j = 0; j < 2 * nkt; ++j, ++g) {  // K_0, V_0, K_1, V_1, ...
+        const int st = g % kStages;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (g / kStages) & 1)))) break;
+        widen_tile_half<D>(smem + C::kRing + st * C::kTile, h, lane, w.Lk - (j >> 1) * kBlockN);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&conv[st]);
+      }
+      if (!ok) break;
+    }
+    if (!ok && lane == 0) record_status(p.dev_status, PGQA_ETIMEOUT);
   } else if (warp == kWarpMma) {
     // ================================================================ MMA issuer
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16_f32(128, kBlockN, false);
-      const uint32_t id_o = idesc_bf16_f32(128, D, true);
+      const uint32_t id_s = F8 ? idesc_f16_f32(128, kBlockN, false) : idesc_bf16_f32(128, kBlockN, false);
+      const uint32_t id_o = F8 ? idesc_f16_f32(128, D, true) : idesc_bf16_f32(128, D, true);
       const uint32_t q_addr = smem_u32(smem + C::kQ), ring = smem_u32(smem + C::kRing);
       int it = 0, g = 0, np[2] = {0, 0}, pv_issued[2] = {0, 0};
       bool ok = true;
@@ -559,10 +686,10 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         ++pv_issued[X];
         return true;
       };
-      // waits for ring load gi to land; returns its stage in st
+      // waits for ring load gi to land (E4M3: and be widened); returns its stage in st
       auto take = [&](int gi, int& st) {
         st = gi % kStages;
-        if (!(ok = mbar_wait(&full[st], (gi / kStages) & 1))) return false;
+        if (!(ok = mbar_wait(F8 ? &conv[st] : &full[st], (gi / kStages) & 1))) return false;
         tc_fence_after();
         return true;
       };
@@ -574,6 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       auto start_item = [&](Item& nw) {
         if (!(ok = mbar_wait(q_full, it & 1))) return false;
         nw = read_slot(slots + (it & 1) * 8);
+        if (F8 && nw.ticket >= 0 && !(ok = mbar_wait(q_conv, it & 1))) return false;
         ++it;
         tc_fence_after();
         return nw.ticket >= 0;
@@ -622,8 +750,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     const int r = wq * 32 + lane;  // query row in the tile = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t s_col = X * 128, o_col = 256 + X * 128;
-    const float sc = p.scale_log2;  // > 0 (checked on the host)
-    const uint64_t sc2 = f2(sc, sc);
+    float sc = p.scale_log2;  // softmax scale in log2 units, > 0 (checked on the host)
+    uint64_t sc2 = f2(sc, sc);
     int it = 0, gl = 0, tcnt = 0;
     bool ok = true;
     for (;;) {
@@ -644,6 +772,11 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       const int lim = min(off + qpos, w.Lk - 1);  // last key this row attends
       const int first_lim = off + tq * kBlockM;   // the tile's first row's last key
       const int nkt = w.nkt();
+      const int kvh = w.hq / p.group;
+      if constexpr (F8) {  // E4M3: the softmax scale times k_scale_h
+        sc = p.scale_log2 * __ldg(k_scale + kvh);
+        sc2 = f2(sc, sc);
+      }
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < nkt; ++j) {
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(&s_full[X], tcnt & 1)))) break;
@@ -676,8 +809,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
           l *= alpha;
           m_ref = mx;
         }
-        // P = 2^(s * scale - m_ref) as bf16, two keys per TMEM column over the first
-        // 64 columns of S_X (masked keys: 2^-inf = 0); the row sum over 8 chains
+        // P = 2^(s * scale - m_ref) as bf16 (E4M3: f16), two keys per TMEM column over
+        // the first 64 columns of S_X (masked keys: 2^-inf = 0); the row sum over 8
+        // chains
         const uint64_t neg_m2 = f2(-m_ref, -m_ref);
         uint64_t acc[4] = {0, 0, 0, 0};
         uint32_t pk[64];
@@ -688,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
                a0, a1);
           const float e0 = ex2(a0), e1 = ex2(a1);
           acc[c & 3] = add2(acc[c & 3], f2(e0, e1));
-          pk[c] = pack_bf16(e0, e1);
+          pk[c] = F8 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
         }
         tmem_st64(lane_base + s_col, pk);
         {
@@ -714,8 +848,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
         // V rows past the sequence end may hold anything (NaN included): zero them so
         // that P = 0 there contributes exactly nothing. Only the last key tile of the
         // item reaches past the end; tile A's softmax zeroes it (P_B V is issued after
-        // P_A V, which waits for this).
-        if (X == 0 && kbase + kBlockN > w.Lk) {
+        // P_A V, which waits for this). E4M3: the widening wrote those rows as zeros.
+        if (!F8 && X == 0 && kbase + kBlockN > w.Lk) {
           const int gi = gl0 + 2 * j + 1, vs = gi % kStages;
           if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full[vs], (gi / kStages) & 1)))) break;
           if (kbase + r >= w.Lk) {
@@ -741,7 +875,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       const size_t orow =
           static_cast<size_t>(w.start + (store ? qpos : 0)) * p.num_q_heads + w.hq + X;
       uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D);
-      const float inv = 1.f / l;
+      const float inv = (F8 ? __ldg(v_scale + kvh) : 1.f) / l;
 #pragma unroll
       for (int half = 0; half < D / 64; ++half) {
         uint32_t o[64];
@@ -775,21 +909,25 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
   }
 }
 
-template <int D>
+template <int D, bool F8>
 pgqa_status_t launch_prefill_variant(const PrefillArgs& a) {
   using C = PCfg<D>;
   const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.num_kv_heads * 16;
   CUtensorMap qmap, kmap, vmap;
+  // bf16 cache: 64-column boxes, 128-byte swizzle; E4M3: one unswizzled box per page
+  const CUtensorMapDataType kv_type =
+      F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t row_bytes = F8 ? D : D * 2;
+  const uint32_t box_inner = F8 ? D : 64;
+  const CUtensorMapSwizzle kv_swz = F8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
   if (!tensor_map_3d(&qmap, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, a.num_q_heads,
                      a.num_tokens, static_cast<uint64_t>(D) * 2,
                      static_cast<uint64_t>(a.num_q_heads) * D * 2, 64, 1, kBlockM,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tensor_map_2d(&kmap, a.k_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, rows, D * 2, 64, 16,
-                     CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tensor_map_2d(&vmap, a.v_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, rows, D * 2, 64, 16,
-                     CU_TENSOR_MAP_SWIZZLE_128B))
+      !tensor_map_2d(&kmap, a.k_cache, kv_type, D, rows, row_bytes, box_inner, 16, kv_swz) ||
+      !tensor_map_2d(&vmap, a.v_cache, kv_type, D, rows, row_bytes, box_inner, 16, kv_swz))
     return PGQA_ECUDA;
-  if (!smem_attr_ready(reinterpret_cast<const void*>(paged_prefill_kernel<D>), C::kSmem))
+  if (!smem_attr_ready(reinterpret_cast<const void*>(paged_prefill_kernel<D, F8>), C::kSmem))
     return PGQA_ECUDA;
   const int sms = num_sms_current_device();
   if (sms <= 0) return PGQA_ECUDA;
@@ -817,8 +955,8 @@ pgqa_status_t launch_prefill_variant(const PrefillArgs& a) {
   p.scale_log2 = a.scale * kLog2e;
   const long long items = static_cast<long long>(p.n_levels) * a.num_seqs * p.pairs;
   const int grid = static_cast<int>(items < sms ? items : sms);
-  if (launch_after_previous(paged_prefill_kernel<D>, dim3(grid), dim3(kThreads), C::kSmem,
-                            a.stream, qmap, kmap, vmap, p) != cudaSuccess)
+  if (launch_after_previous(paged_prefill_kernel<D, F8>, dim3(grid), dim3(kThreads), C::kSmem,
+                            a.stream, qmap, kmap, vmap, p, a.k_scale, a.v_scale) != cudaSuccess)
     return PGQA_ECUDA;
   return cudaPeekAtLastError() == cudaSuccess ? PGQA_OK : PGQA_ECUDA;
 }
@@ -829,8 +967,11 @@ int prefill_max_seqs() { return kMaxSeqs; }
 int prefill_max_seqlen() { return kMaxLevels * kBlockM; }
 
 pgqa_status_t launch_paged_prefill(const PrefillArgs& a) {
-  if (a.head_dim == 128) return launch_prefill_variant<128>(a);
-  if (a.head_dim == 64) return launch_prefill_variant<64>(a);
+  const bool f8 = a.cache_dtype == PGQA_DTYPE_E4M3;
+  if (a.head_dim == 128) return f8 ? launch_prefill_variant<128, true>(a)
+                                   : launch_prefill_variant<128, false>(a);
+  if (a.head_dim == 64) return f8 ? launch_prefill_variant<64, true>(a)
+                                  : launch_prefill_variant<64, false>(a);
   return PGQA_EUNSUPPORTED;
 }
 

@@ -147,4 +147,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// The same with f16 A and B (format code 0 for both operands).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major) {
+  return (1u << 4)                                   // D format: f32
+         | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
 }  // namespace pgqa

@@ -581,6 +581,47 @@ def pin_chunked_without_prefix_is_prefill():
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
+# ------------------------------------------------------- prefill over an E4M3 cache
+
+def pin_e4m3_prefill_cache():
+    """Both prefill functions over an E4M3 cache of random codes equal library
+    attention (causal; bottom-right for the chunked form) on the cache dequantised
+    by torch's float8 view with separate per-kv-head K and V scales."""
+    lens_k, lens_q = [19, 40], [19, 6]
+    Hq, Hkv, D = 4, 2, 16
+    g = torch.Generator().manual_seed(231)
+    nbs = [-(-L // BS) for L in lens_k]
+    kc = torch.randint(0, 0x7F, (sum(nbs), Hkv, BS, D), generator=g, dtype=torch.uint8)
+    kc |= torch.randint(0, 2, kc.shape, generator=g, dtype=torch.uint8) << 7
+    kc[kc == 0xFF] = 0x80
+    vc = kc.flip(0).clone()
+    table = torch.tensor([[1, 0, -1], [3, 2, 4]], dtype=torch.int32)
+    ks, vs = torch.tensor([0.01, 0.02]), torch.tensor([0.03, 0.005])
+    deq = lambda c, s: c.view(torch.float8_e4m3fn).double() * s.double().view(1, -1, 1, 1)
+    kd, vd = deq(kc, ks), deq(vc, vs)
+    q = rand_bf16((sum(lens_q), Hq, D), 232)
+    cu = torch.tensor([0] + np.cumsum(lens_q).tolist(), dtype=torch.int32)
+    lk = torch.tensor(lens_k, dtype=torch.int32)
+    out, lse = O.paged_prefill_kv(q, kc, vc, table, cu, lk, 0.25, dtype=O.E4M3, k_scale=ks,
+                                  v_scale=vs)
+    for i, (Lk, Lq) in enumerate(zip(lens_k, lens_q)):
+        blocks = table[i, :nbs[i]].long()
+        Kb = kd[blocks].permute(1, 0, 2, 3).reshape(Hkv, -1, D)[:, :Lk]
+        Vb = vd[blocks].permute(1, 0, 2, 3).reshape(Hkv, -1, D)[:, :Lk]
+        a = int(cu[i])
+        qi = q[a:a + Lq].permute(1, 0, 2).double()
+        mask = torch.arange(Lk)[None, :] <= (Lk - Lq + torch.arange(Lq))[:, None]
+        want = F.scaled_dot_product_attention(qi[None], Kb.repeat_interleave(2, 0)[None],
+                                              Vb.repeat_interleave(2, 0)[None], attn_mask=mask,
+                                              scale=0.25)[0].permute(1, 0, 2)
+        _close(out[a:a + Lq], want.numpy(), 1e-11, 1e-13, "e4m3 chunked prefill vs sdpa")
+    # sequence 0 has no prefix: the whole-sequence form gives the same rows
+    cu0 = torch.tensor([0, lens_k[0]], dtype=torch.int32)
+    o0, l0 = O.paged_prefill(q[:lens_k[0]], kc, vc, table[:1], cu0, 0.25, dtype=O.E4M3,
+                             k_scale=ks, v_scale=vs)
+    assert np.array_equal(o0, out[:lens_k[0]]) and np.array_equal(l0, lse[:lens_k[0]])
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]
 
 

@@ -132,3 +132,18 @@ def test_prefill_kv_argument_validation():
     assert f(*args[:12], -1, *args[13:]) == pgqa.EINVAL
     assert f(*args[:10], 0, *args[11:]) == pgqa.OK                 # nothing to do
     assert f(*args[:19], None, 0, *args[21:]) == pgqa.ENOWORKSPACE
+
+
+def test_prefill_e4m3_argument_validation():
+    f = pgqa.lib.pgqa_paged_prefill_varlen_e4m3
+    P = 1 << 20
+    #       out lse q  T    k  v  bt maxb cuq lk    S  maxq maxk Hq Hkv D   NB  bs  scale ks vs
+    args = [P, None, P, 100, P, P, P, 64, P, None, 2, 64, 0, 8, 2, 128, 64, 16, 0.1, P, P,
+            P, 33024, None, None]  # ws wsb st stream
+    assert f(*args[:19], None, *args[20:]) == pgqa.EINVAL          # no k_scale
+    assert f(*args[:20], None, *args[21:]) == pgqa.EINVAL          # no v_scale
+    assert f(*args[:19], P + 2, *args[20:]) == pgqa.EINVAL         # misaligned scales
+    assert f(*args[:15], 96, *args[16:]) == pgqa.EUNSUPPORTED      # head_dim 96
+    assert f(*args[:17], 32, *args[18:]) == pgqa.EUNSUPPORTED      # 32-token blocks
+    assert f(*args[:10], 0, *args[11:]) == pgqa.OK                 # nothing to do
+    assert f(*args[:21], None, 0, *args[23:]) == pgqa.ENOWORKSPACE

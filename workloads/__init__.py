@@ -329,6 +329,19 @@ def make_chunked_prefill(lens_k: Sequence[int], lens_q: Sequence[int], num_q_hea
                                 scale=1.0 / math.sqrt(head_dim), name=name)
 
 
+def e4m3_prefill_cache(inp):
+    """An E4M3 cache for a prefill batch (PrefillInputs or ChunkedPrefillInputs): K and
+    V pools of the batch's shape filled with the NaN code 0x7F (so a read of a row no
+    sequence owns poisons the result) and per-kv-head scales amax / 448 over the
+    tokens the batch writes (K and V separately). Returns (k_cache, v_cache,
+    k_scale, v_scale); the codes themselves come from the cache write."""
+    shape = tuple(inp.k_cache.shape)
+    k_cache = torch.full(shape, 0x7F, dtype=torch.uint8)
+    v_cache = torch.full(shape, 0x7F, dtype=torch.uint8)
+    scale = lambda x: (x.float().abs().amax(dim=(0, 2)).clamp_min(1e-12) / 448.0).float()
+    return k_cache, v_cache, scale(inp.key), scale(inp.value)
+
+
 def _pool_for(lens: Sequence[int], base: int, rotations: int, bs: int = BLOCK_SIZE) -> int:
     """Smallest pool (a multiple of 1024 blocks, at least ``base``) that holds
     ``rotations + 1`` disjoint copies of the tables for ``lens``."""
