@@ -196,7 +196,10 @@ def run_reference(args):
 
 
 class DecodeBench:
-    """Device state of one decode workload and its step (append + decode)."""
+    """Device state of one decode workload and its step: the new token's K/V appended
+    and attention over the whole context, as one fused launch
+    (pgqa_paged_attention_decode_append) or, with fused=False, as two calls
+    (pgqa_kv_cache_write, then pgqa_paged_attention_decode)."""
 
     def __init__(self, inp, dev):
         import paged_kv_gqa_10_gb300 as pgqa
@@ -224,7 +227,10 @@ class DecodeBench:
         # lengths, and writes out and lse
         self.alg_bytes = (self.kv_bytes + self.q.numel() * 2 + self.out.numel() * 2 +
                           self.lse.numel() * 4 + nblk * 4 + B * 4)
+        # the fused launch also reads the new rows and writes them into the cache
+        self.alg_bytes_fused = self.alg_bytes + 2 * 2 * self.nk.numel() * 2
         self.graphs = None
+        self.fused = True
 
     def append(self, r, slots=None, key=None, value=None):
         self.pgqa.kv_cache_write(self.nk if key is None else key, self.nv if value is None else value,
@@ -237,10 +243,20 @@ class DecodeBench:
             self.cl, self.inp.scale, self.inp.max_context_len, k_scale=self.ks, v_scale=self.vs,
             workspace=self.ws if self.ws_n else None, dev_status=self.status)
 
+    def decode_append(self, r, table=None):
+        self.pgqa.paged_attention_decode_append(
+            self.out, self.lse, self.q, self.nk, self.nv, self.kc, self.vc,
+            self.bts[r] if table is None else table, self.cl, self.inp.scale,
+            self.inp.max_context_len, k_scale=self.ks, v_scale=self.vs,
+            workspace=self.ws if self.ws_n else None, dev_status=self.status)
+
     def step(self, i):
         r = i % self.R
-        self.append(r)
-        self.decode(r)
+        if self.fused:
+            self.decode_append(r)
+        else:
+            self.append(r)
+            self.decode(r)
 
     def capture(self):
         """One CUDA graph per rotation, each holding one step (append + decode), and one
@@ -319,15 +335,23 @@ def measure_decode(inp, args, dev, dist=None, clocks_index=None):
         dist.barrier()
     b.check()
     ms_eager = _elapsed(lambda i: b.step(args.warmup + i), args.steps)
-    # decode kernel alone: one CUDA graph of back-to-back decode launches cycling over
-    # the disjoint block-table sets (no launch finds the previous one's pages in L2),
-    # timed with events on the launching stream; the cache already holds every step's
-    # appended token, so the launches compute exactly what the step does
+    # the same steps as two calls (cache write, then decode), for comparison
+    b.fused = False
+    b.capture()
+    b.run_steps(first, b.R)
+    b.check()
+    ms_two = _elapsed(lambda i: b.run_steps(first, args.steps) if i == 0 else None, 1)
+    b.check()
+    b.fused = True
+    # the step's kernel alone: one CUDA graph of back-to-back fused launches cycling
+    # over the disjoint block-table sets (no launch finds the previous one's pages in
+    # L2), timed with events on the launching stream; every launch appends the same
+    # rows again, so the launches compute exactly what the step does
     n_rep = 4 * b.R
     g_dec = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_dec):
         for i in range(n_rep):
-            b.decode(i % b.R)
+            b.decode_append(i % b.R)
     g_dec.replay()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
@@ -345,10 +369,9 @@ def measure_decode(inp, args, dev, dist=None, clocks_index=None):
     pin = lambda t: t.pin_memory()
     h_q, h_k, h_v, h_cl = pin(inp.q), pin(inp.step_key), pin(inp.step_value), pin(inp.context_lens)
     h_bt = [pin(t) for t in b.tables]
-    h_sl = [pin(t) for t in b.slots]
     h_out = torch.empty(tuple(b.out.shape), dtype=torch.bfloat16).pin_memory()
     h_lse = torch.empty(tuple(b.lse.shape), dtype=torch.float32).pin_memory()
-    d_bt, d_sl = torch.empty_like(b.bts[0]), torch.empty_like(b.sls[0])
+    d_bt = torch.empty_like(b.bts[0])
 
     def e2e_step(i):
         r = i % b.R
@@ -357,13 +380,11 @@ def measure_decode(inp, args, dev, dist=None, clocks_index=None):
         b.nv.copy_(h_v, non_blocking=True)
         b.cl.copy_(h_cl, non_blocking=True)
         d_bt.copy_(h_bt[r], non_blocking=True)
-        d_sl.copy_(h_sl[r], non_blocking=True)
-        b.append(r, slots=d_sl)
-        b.decode(r, table=d_bt)
+        b.decode_append(r, table=d_bt)
         h_out.copy_(b.out, non_blocking=True)
         h_lse.copy_(b.lse, non_blocking=True)
 
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_cl, h_bt[0], h_sl[0]))
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_cl, h_bt[0]))
     d2h = h_out.numel() * 2 + h_lse.numel() * 4
     for i in range(args.warmup):
         e2e_step(i)
@@ -371,10 +392,10 @@ def measure_decode(inp, args, dev, dist=None, clocks_index=None):
     e2e_ms = _elapsed(lambda i: e2e_step(args.warmup + i), args.steps)
     b.check()
     res = {"bench": b, "ms_graph": ms_graph / args.steps, "ms_eager": ms_eager / args.steps,
-           "dec_ms": dec_ms, "e2e_ms": e2e_ms / args.steps, "h2d": h2d, "d2h": d2h,
+           "ms_two": ms_two / args.steps, "dec_ms": dec_ms, "e2e_ms": e2e_ms / args.steps, "h2d": h2d, "d2h": d2h,
            "clocks": clocks}
     if dist:
-        for k in ("ms_graph", "ms_eager", "dec_ms", "e2e_ms"):
+        for k in ("ms_graph", "ms_eager", "ms_two", "dec_ms", "e2e_ms"):
             t = torch.tensor([res[k]], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             res[k] = float(t.item())
@@ -630,7 +651,7 @@ def run_ours(args):
             dist.destroy_process_group()
         return 0
     hbm_peak, _, peak_kind = _peaks()
-    achieved = b.alg_bytes / (m["dec_ms"] * 1e-3) / 1e9
+    achieved = b.alg_bytes_fused / (m["dec_ms"] * 1e-3) / 1e9
     dec_files = ["paged_kv_gqa_10_gb300/csrc/decode.cu", "paged_kv_gqa_10_gb300/csrc/ptx.cuh"]
     B, Hq, D = inp.q.shape
     dt = "e4m3 KV, bf16 q/out" if inp.cache_dtype == "e4m3" else "bf16"
@@ -642,22 +663,27 @@ def run_ours(args):
         "config": {"workload": desc, "batch": B, "q_heads": Hq, "kv_heads": inp.num_kv_heads,
                    "head_dim": D, "block_size": 16, "kv_bytes_per_step": kv_bytes,
                    "unique_kv_bytes_per_step": workloads.kv_read_bytes(inp, unique=True),
-                   "step": "kv_cache_write(one new token per sequence) + paged_attention_decode, "
-                           f"replayed as CUDA graphs of {b.R} steps (one per block-table set)",
+                   "step": "one launch of paged_attention_decode_append: each sequence's new "
+                           "token written at position L-1 (the bytes kv_cache_write writes) and "
+                           "attention over the whole context; replayed as CUDA graphs of "
+                           f"{b.R} steps (one per block-table set)",
                    "eager_ms_per_step": m["ms_eager"],
+                   "two_call_ms_per_step": m["ms_two"],
+                   "two_call_value": kv_bytes * world / (m["ms_two"] * 1e-3) / 1e9,
                    "l2": f"{b.R} rotating block-table sets over disjoint blocks "
                          f"({b.R * kv_bytes / 1e6:.0f} MB > 129 MB L2)",
                    "parallelism": f"replica per GPU x{world}"},
-        "roofline": {"bound": "hbm", "kernel": f"paged_decode_kernel<{D},{inp.cache_dtype}>",
+        "roofline": {"bound": "hbm",
+                     "kernel": f"paged_decode_kernel<{D},{inp.cache_dtype}> with the append",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_kind": peak_kind,
-                     "alg_bytes_per_launch": b.alg_bytes, "launch_ms": m["dec_ms"],
+                     "alg_bytes_per_launch": b.alg_bytes_fused, "launch_ms": m["dec_ms"],
                      "traffic": _profile_traffic("decode_llama3_8b.json", dec_files)
                      if args.workload == "llama3_8b" else None},
         "e2e": {"value": kv_bytes * world / (m["e2e_ms"] * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"],
                 "ms_per_step": m["e2e_ms"], "calls": "eager C-ABI calls, pinned host buffers"},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": args.steps,
         "clocks": m["clocks"],
     }
     if pref is not None:

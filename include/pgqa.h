@@ -244,6 +244,30 @@ pgqa_status_t pgqa_paged_attention_decode_noalloc(void* out, float* lse, const v
                                                   const float* v_scale, int max_context_len,
                                                   int* dev_status, void* stream);
 
+/*
+ * One decode step with the append fused in: the new token of every sequence is
+ * written into the cache and attended in one launch. context_lens[b] counts the new
+ * token; its K and V rows go to position L-1 of sequence b, i.e. block
+ * block_tables[b][(L-1) / block_size], row (L-1) % block_size: exactly what
+ * pgqa_kv_cache_write writes for a slot mapping pointing there (bf16 copy, or the
+ * same E4M3 codes), and the attention then reads it as pgqa_paged_attention_decode
+ * does (the page-cache update then attention of the surgery-log article, sec. 3.1,
+ * and the LLaMA-structure article's decode step, sec. 3.1).
+ *   key, value    [num_seqs][num_kv_heads][head_dim] bf16, read; 16-byte aligned.
+ *   k_cache, v_cache  read and written.
+ * A sequence whose length is invalid (a device error, as for
+ * pgqa_paged_attention_decode) or 0 gets no append; a bad block id for position L-1
+ * is PGQA_EBADINDEX and nothing is written there. Every other argument, the
+ * workspace and the error behaviour are as for pgqa_paged_attention_decode.
+ */
+pgqa_status_t pgqa_paged_attention_decode_append(
+    void* out, float* lse, const void* q, const void* key, const void* value, void* k_cache,
+    void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int num_blocks, int block_size, float scale, int cache_dtype, const float* k_scale,
+    const float* v_scale, int max_context_len, void* workspace, size_t workspace_bytes,
+    int* dev_status, void* stream);
+
 /* Workspace bytes pgqa_paged_prefill_varlen needs (33024: the ticket counters the
  * CTAs take work items with, and the longest-first item tables each call rebuilds). */
 size_t pgqa_prefill_workspace_size(int num_seqs, int num_q_heads, int max_seqlen);

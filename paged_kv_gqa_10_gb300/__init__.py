@@ -64,6 +64,8 @@ def _load():
                                          I, P, SZ, P, P], I),
         "pgqa_paged_attention_decode_window": ([P, P, P, P, P, P, I, P, I, I, I, I, I, I, F, I,
                                                 I, P, P, I, P, SZ, P, P], I),
+        "pgqa_paged_attention_decode_append": ([P, P, P, P, P, P, P, P, I, P, I, I, I, I, I,
+                                                I, F, I, P, P, I, P, SZ, P, P], I),
         "pgqa_paged_attention_decode_noalloc": ([P, P, P, P, P, P, I, P, I, I, I, I, I, I, F,
                                                  I, P, P, I, P, P], I),
         "pgqa_prefill_workspace_size": ([I, I, I], SZ),
@@ -236,6 +238,36 @@ def paged_attention_decode(out, lse, q, k_cache, v_cache, block_tables, context_
         _cache_dtype(k_cache), _ptr(k_scale), _ptr(v_scale), int(max_context_len),
         _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
     _check(rc, "paged_attention_decode")
+
+
+def paged_attention_decode_append(out, lse, q, key, value, k_cache, v_cache, block_tables,
+                                  context_lens, scale, max_context_len, k_scale=None,
+                                  v_scale=None, workspace=None, dev_status=None, stream=None):
+    """One decode step with the append fused in: key/value [B, Hkv, D] bf16 (the new
+    token of every sequence) go to position context_lens[b] - 1 of each cache, then
+    attention over the whole context. Other arguments as for paged_attention_decode."""
+    _dev(out, "out", torch.bfloat16)
+    _dev(lse, "lse", torch.float32)
+    _dev(q, "q", torch.bfloat16)
+    _dev(key, "key", torch.bfloat16)
+    _dev(value, "value", torch.bfloat16)
+    _dev(k_cache, "k_cache")
+    _dev(v_cache, "v_cache")
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(context_lens, "context_lens", torch.int32)
+    _dev(k_scale, "k_scale", torch.float32)
+    _dev(v_scale, "v_scale", torch.float32)
+    _dev(workspace, "workspace")
+    _dev(dev_status, "dev_status", torch.int32)
+    B, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = _handle().pgqa_paged_attention_decode_append(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, NB, bs,
+        float(scale), _cache_dtype(k_cache), _ptr(k_scale), _ptr(v_scale), int(max_context_len),
+        _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
+    _check(rc, "paged_attention_decode_append")
 
 
 def paged_attention_decode_window(out, lse, q, k_cache, v_cache, block_tables, context_lens,

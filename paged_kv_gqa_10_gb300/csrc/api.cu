@@ -265,7 +265,8 @@ size_t pgqa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_head
   return a > b ? a : b;
 }
 
-// Shared by both decode entry points (window 0: the whole context).
+// Shared by the decode entry points (window 0: the whole context; key/value null: no
+// fused append).
 static pgqa_status_t decode_call(void* out, float* lse, const void* q, const void* k_cache,
                                  const void* v_cache, const int32_t* block_tables,
                                  int max_blocks_per_seq, const int32_t* context_lens,
@@ -273,7 +274,8 @@ static pgqa_status_t decode_call(void* out, float* lse, const void* q, const voi
                                  int num_blocks, int block_size, float scale, int window,
                                  int cache_dtype, const float* k_scale, const float* v_scale,
                                  int max_context_len, void* workspace, size_t workspace_bytes,
-                                 int* dev_status, void* stream) {
+                                 int* dev_status, void* stream, const void* key = nullptr,
+                                 const void* value = nullptr) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 ||
       block_size <= 0 || max_context_len < 0 || max_blocks_per_seq < 0 || !isfinite(scale))
     return PGQA_EINVAL;
@@ -295,6 +297,8 @@ static pgqa_status_t decode_call(void* out, float* lse, const void* q, const voi
   if (num_seqs == 0) return PGQA_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PGQA_EINVAL;
   if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return PGQA_EINVAL;
+  if ((key == nullptr) != (value == nullptr) || !aligned(key, 16) || !aligned(value, 16))
     return PGQA_EINVAL;
   const int sms = pgqa::num_sms_current_device();
   if (sms <= 0) return PGQA_ECUDA;
@@ -323,6 +327,8 @@ static pgqa_status_t decode_call(void* out, float* lse, const void* q, const voi
   a.v_scale = v_scale;
   a.max_context_len = max_context_len;
   a.window = window;
+  a.new_key = key;
+  a.new_value = value;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   a.dev_status = dev_status;
@@ -357,6 +363,20 @@ pgqa_status_t pgqa_paged_attention_decode_window(
                      context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks,
                      block_size, scale, window, cache_dtype, k_scale, v_scale, max_context_len,
                      workspace, workspace_bytes, dev_status, stream);
+}
+
+pgqa_status_t pgqa_paged_attention_decode_append(
+    void* out, float* lse, const void* q, const void* key, const void* value, void* k_cache,
+    void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int num_blocks, int block_size, float scale, int cache_dtype, const float* k_scale,
+    const float* v_scale, int max_context_len, void* workspace, size_t workspace_bytes,
+    int* dev_status, void* stream) {
+  if (num_seqs > 0 && (key == nullptr || value == nullptr)) return PGQA_EINVAL;
+  return decode_call(out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks,
+                     block_size, scale, 0, cache_dtype, k_scale, v_scale, max_context_len,
+                     workspace, workspace_bytes, dev_status, stream, key, value);
 }
 
 size_t pgqa_prefill_workspace_size(int num_seqs, int num_q_heads, int max_seqlen) {

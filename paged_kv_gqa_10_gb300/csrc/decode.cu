@@ -79,6 +79,17 @@ struct DecodeParams {
   float scale_log2;  // scale * log2(e)
 };
 
+// Fused append: the step's new token, key L-1 of every sequence, is written into the
+// cache by the warp that reads the page holding it, which also puts the row into its
+// copy of that page in shared memory (the TMA load may have read the row before or
+// after the global store: no other CTA reads that page). Null pointers: no append.
+struct DecodeAppend {
+  const uint4* key;    // [num_seqs][Hkv][D] bf16
+  const uint4* value;
+  uint8_t* k_cache;    // the caches, written through
+  uint8_t* v_cache;
+};
+
 template <int D, bool kFp8>
 struct Cfg {
   static constexpr int kElem = kFp8 ? 1 : 2;
@@ -338,7 +349,7 @@ __device__ __forceinline__ void merge_units(const DecodeParams& p, const Walk& w
 template <int D, bool kFp8>
 __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_decode_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-    const DecodeParams p) {
+    const DecodeParams p, const DecodeAppend ap) {
   using C = Cfg<D, kFp8>;
   constexpr int S = C::kStages;
   constexpr int SPW = C::kStagesPerWarp;
@@ -366,6 +377,17 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
     tma_prefetch_desc(&vmap);
   }
   grid_dependency_wait();  // the stream's previous kernel (e.g. the KV append) is done
+  grid_launch_dependents();  // the next one may place its CTAs as these exit
+
+  // ---- block-table entries the producers will read soon: CTA c asks L2 for those of
+  //      sequences c, c + ncta, ... while every CTA scans the context lengths
+  for (int b = c; b < B; b += ncta) {
+    const int L = __ldg(p.context_lens + b);
+    const int e0 = first_key(p, L) / p.block_size, e1 = (L + p.block_size - 1) / p.block_size;
+    const int32_t* row = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq;
+    for (int e = e0 + tid * 32; e < e1 && e < p.max_blocks_per_seq; e += kThreads * 32)
+      prefetch_l2(row + e);
+  }
 
   // ---- the global page order holds N pages; this CTA owns [r0, r1)
   long long local = 0;
@@ -594,6 +616,32 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
       if (wn.S < r1) load_q(wn);
     }
 
+    // fused append: the page holding key L-1, if this warp reads it (segment-relative),
+    // this lane's 16-byte chunk of the new K (lanes 0..kAppLanes-1) or V row, still
+    // bf16 (E4M3: two loads, quantised when the page comes), and the row's block id
+    constexpr int kAppLanes = C::kRowBytes / 16;
+    int app_j = -1, app_pbn = -1;
+    uint4 app_x0 = make_uint4(0, 0, 0, 0), app_x1 = app_x0;
+    if (ap.key != nullptr) {
+      const int jl = (L - 1) / 16 - w.fp - seg0;
+      if (jl >= 0 && jl < npg && (i_base + jl) % kNW == warp) {
+        app_j = jl;
+        if (lane < 2 * kAppLanes) {
+          const int c = lane % kAppLanes;
+          const uint4* src = (lane < kAppLanes ? ap.key : ap.value) +
+                             (static_cast<size_t>(w.b) * Hkv + w.h) * (D / 8);
+          if constexpr (!kFp8) {
+            app_x0 = __ldg(src + c);
+          } else {
+            app_x0 = __ldg(src + 2 * c);
+            app_x1 = __ldg(src + 2 * c + 1);
+          }
+        }
+        app_pbn = __ldg(p.block_tables + static_cast<size_t>(w.b) * p.max_blocks_per_seq +
+                        (L - 1) / p.block_size);
+      }
+    }
+
     const float sl2 = p.scale_log2 * (kFp8 ? __ldg(p.k_scale + w.h) : 1.f);
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     float acc[C::kNkc][4];
@@ -612,6 +660,29 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
         break;
       }
       bad |= meta[s];
+      if (j == app_j) {
+        // the new token's row: into the cache and over row (L-1) % 16 of this page
+        if (lane < 2 * kAppLanes) {
+          const bool isv = lane >= kAppLanes;
+          const int c = lane % kAppLanes, rr = (L - 1) & 15;
+          uint4 v = app_x0;
+          if constexpr (kFp8) {
+            const float sc = __ldg((isv ? p.v_scale : p.k_scale) + w.h);
+            const uint2 a = e4m3_quant8(app_x0, sc), b = e4m3_quant8(app_x1, sc);
+            v = make_uint4(a.x, a.y, b.x, b.y);
+          }
+          uint8_t* srow = ring + s * C::kStageBytes + (isv ? C::kPageBytes : 0) + (c >> 3) * 2048;
+          *reinterpret_cast<uint4*>(srow + swz128(rr, c & 7)) = v;
+          if (app_pbn >= 0 && app_pbn < p.num_blocks) {
+            const size_t row = (static_cast<size_t>(app_pbn) * Hkv + w.h) * p.block_size +
+                               (L - 1) % p.block_size;
+            *reinterpret_cast<uint4*>((isv ? ap.v_cache : ap.k_cache) + row * C::kRowBytes +
+                                      c * 16) = v;
+          }
+          fence_proxy_async_smem();  // a later TMA fill of this stage comes after it
+        }
+        __syncwarp();
+      }
       const uint32_t stK = smem_u32(ring + s * C::kStageBytes);
       const uint32_t stV = stK + C::kPageBytes;
       const int pk0 = (w.fp + seg0 + j) * 16;       // key of the page's first row
@@ -825,8 +896,13 @@ pgqa_status_t launch_variant(const DecodeArgs& a, const DecodePlan& plan) {
   p.window = a.window;
   p.block_size = a.block_size;
   p.scale_log2 = a.scale * kLog2e;
+  DecodeAppend ap;
+  ap.key = static_cast<const uint4*>(a.new_key);
+  ap.value = static_cast<const uint4*>(a.new_value);
+  ap.k_cache = static_cast<uint8_t*>(const_cast<void*>(a.k_cache));
+  ap.v_cache = static_cast<uint8_t*>(const_cast<void*>(a.v_cache));
   if (launch_after_previous(paged_decode_kernel<D, kFp8>, dim3(plan.grid), dim3(kThreads),
-                            C::kSmem, a.stream, kmap, vmap, p) != cudaSuccess)
+                            C::kSmem, a.stream, kmap, vmap, p, ap) != cudaSuccess)
     return PGQA_ECUDA;
   return cudaPeekAtLastError() == cudaSuccess ? PGQA_OK : PGQA_ECUDA;
 }

@@ -78,6 +78,10 @@ struct DecodeArgs {
   const float* v_scale;
   int max_context_len;
   int window;  // > 0: only the last `window` keys of each context are attended
+  // fused append (both null: none): the new token's K/V rows [num_seqs][Hkv][D] bf16,
+  // written at position context_len - 1 of each sequence before it is attended
+  const void* new_key;
+  const void* new_value;
   void* workspace;
   size_t workspace_bytes;
   int* dev_status;

@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(256) kv_cache_write_kernel(
     void* __restrict__ k_cache, void* __restrict__ v_cache, int num_blocks, int block_size,
     const float* __restrict__ k_scale, const float* __restrict__ v_scale, int* dev_status) {
   grid_launch_dependents();  // a following attention kernel may get its CTAs in place now
+  grid_dependency_wait();    // the stream's previous kernel (inputs, cache readers) is done
   const int vecs = head_dim / 8;  // 16-byte input vectors per (token, head) row
   const int64_t total = static_cast<int64_t>(num_tokens) * num_kv_heads * vecs;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -48,17 +49,8 @@ __global__ void __launch_bounds__(256) kv_cache_write_kernel(
       *reinterpret_cast<uint4*>(static_cast<uint16_t*>(v_cache) + dst) = vx;
     } else {
       const float ks = __ldg(k_scale + h), vs = __ldg(v_scale + h);
-      auto quant = [](uint4 x, float s) {
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-        uint16_t c[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          c[j] = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(w[j]), s), __fdiv_rn(bf16_hi(w[j]), s));
-        return make_uint2(c[0] | (static_cast<uint32_t>(c[1]) << 16),
-                          c[2] | (static_cast<uint32_t>(c[3]) << 16));
-      };
-      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(k_cache) + dst) = quant(kx, ks);
-      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(v_cache) + dst) = quant(vx, vs);
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(k_cache) + dst) = e4m3_quant8(kx, ks);
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(v_cache) + dst) = e4m3_quant8(vx, vs);
     }
   }
 }
@@ -119,17 +111,13 @@ pgqa_status_t launch_kv_cache_write(const void* key, const void* value,
   const int64_t work = static_cast<int64_t>(num_tokens) * num_kv_heads * (head_dim / 8);
   if (work == 0) return PGQA_OK;
   const int grid = grid_for(work, 256);
-  if (cache_dtype == PGQA_DTYPE_BF16) {
-    kv_cache_write_kernel<false><<<grid, 256, 0, stream>>>(
-        static_cast<const uint4*>(key), static_cast<const uint4*>(value), slot_mapping,
-        num_tokens, num_kv_heads, head_dim, k_cache, v_cache, num_blocks, block_size, k_scale,
-        v_scale, dev_status);
-  } else {
-    kv_cache_write_kernel<true><<<grid, 256, 0, stream>>>(
-        static_cast<const uint4*>(key), static_cast<const uint4*>(value), slot_mapping,
-        num_tokens, num_kv_heads, head_dim, k_cache, v_cache, num_blocks, block_size, k_scale,
-        v_scale, dev_status);
-  }
+  // programmatic launch: the CTAs may be placed while the previous kernel finishes
+  const cudaError_t e = launch_after_previous(
+      cache_dtype == PGQA_DTYPE_BF16 ? kv_cache_write_kernel<false> : kv_cache_write_kernel<true>,
+      dim3(grid), dim3(256), 0, stream, static_cast<const uint4*>(key),
+      static_cast<const uint4*>(value), slot_mapping, num_tokens, num_kv_heads, head_dim, k_cache,
+      v_cache, num_blocks, block_size, k_scale, v_scale, dev_status);
+  if (e != cudaSuccess) return PGQA_ECUDA;
   return cudaPeekAtLastError() == cudaSuccess ? PGQA_OK : PGQA_ECUDA;
 }
 

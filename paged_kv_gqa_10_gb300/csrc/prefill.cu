@@ -394,6 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, ncta = gridDim.x;
   grid_dependency_wait();  // the stream's previous kernel (e.g. the KV scatter) is done
+  grid_launch_dependents();  // the next one may place its CTAs as these exit
 
   // length errors: reported once per sequence, by CTA 0
   if (c == 0) {

@@ -119,6 +119,16 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Generic-proxy shared-memory writes become visible to the async proxy (TMA, MMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Asks L2 to fetch the line holding `p` (no register is written, nothing waits).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -205,6 +215,19 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// Eight bf16 (16 bytes) to eight E4M3 codes of x / s: the quotient rounded to nearest
+// in fp32, then to E4M3 (nearest even, saturated). Every cache write uses this one
+// routine, so the codes are the same whichever kernel writes them.
+__device__ __forceinline__ uint2 e4m3_quant8(uint4 x, float s) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  uint16_t c[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    c[j] = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(w[j]), s), __fdiv_rn(bf16_hi(w[j]), s));
+  return make_uint2(c[0] | (static_cast<uint32_t>(c[1]) << 16),
+                    c[2] | (static_cast<uint32_t>(c[3]) << 16));
+}
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;

@@ -33,11 +33,6 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Generic-proxy shared-memory writes become visible to the async proxy (TMA, MMA).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // D[tmem] (+)= A[smem desc] * B[smem desc]; kind::f16 (bf16 / f16 inputs, f32 accumulate).
 __device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {

@@ -147,3 +147,16 @@ def test_prefill_e4m3_argument_validation():
     assert f(*args[:17], 32, *args[18:]) == pgqa.EUNSUPPORTED      # 32-token blocks
     assert f(*args[:10], 0, *args[11:]) == pgqa.OK                 # nothing to do
     assert f(*args[:21], None, 0, *args[23:]) == pgqa.ENOWORKSPACE
+
+
+def test_decode_append_argument_validation():
+    f = pgqa.lib.pgqa_paged_attention_decode_append
+    P = 1 << 20
+    #       out lse q  key val k  v  bt maxb cl B  Hq Hkv D    NB  bs  scale dt ks    vs
+    args = [P, None, P, P, P, P, P, P, 4, P, 2, 8, 2, 128, 16, 16, 0.1, 0, None, None,
+            64, None, 0, None, None]  # maxctx ws wsb st stream
+    assert f(*args[:3], None, *args[4:]) == pgqa.EINVAL            # no new K rows
+    assert f(*args[:4], None, *args[5:]) == pgqa.EINVAL            # no new V rows
+    assert f(*args[:3], P + 8, *args[4:]) == pgqa.EINVAL           # misaligned rows
+    assert f(*args[:15], 64, *args[16:]) == pgqa.EUNSUPPORTED      # 64-token blocks
+    assert f(*args[:10], 0, *args[11:]) == pgqa.OK                 # nothing to do
