@@ -39,6 +39,14 @@
  *    log of the sum of exp(score) over the attended keys.
  *  - All calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream) and run on the current CUDA device.
+ *  - The kernels launch programmatically: a call's kernel may start while the
+ *    stream's previous kernel finishes, and waits for it before touching q, K/V
+ *    rows, the caches, out, lse or the workspace. The decode calls read
+ *    block_tables and context_lens BEFORE that wait, so the kernel enqueued right
+ *    before a decode call must not write them if it releases its dependents early
+ *    (griddepcontrol.launch_dependents / cudaTriggerProgrammaticLaunchCompletion).
+ *    Copies, and kernels that do not release early (ordinary kernels), are fully
+ *    ordered; no kernel of this library writes either array.
  *  - Supported now: head_dim 64 or 128, bf16 q/out; block_size 8, 16 or 32
  *    and 1 <= num_q_heads / num_kv_heads <= 8 for decode; block_size 16 and
  *    any group size for prefill (bf16 or E4M3 cache); any block_size for

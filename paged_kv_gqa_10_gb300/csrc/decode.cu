@@ -376,8 +376,10 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
     tma_prefetch_desc(&kmap);
     tma_prefetch_desc(&vmap);
   }
-  grid_dependency_wait();  // the stream's previous kernel (e.g. the KV append) is done
-  grid_launch_dependents();  // the next one may place its CTAs as these exit
+  grid_launch_dependents();  // the next kernel may place its CTAs as these exit
+  // Up to grid_dependency_wait() below, this CTA reads only context lengths and block
+  // tables, which no kernel of this library writes: the plan below may run while the
+  // stream's previous kernel finishes (programmatic launch).
 
   // ---- block-table entries the producers will read soon: CTA c asks L2 for those of
   //      sequences c, c + ncta, ... while every CTA scans the context lengths
@@ -398,24 +400,10 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
   const long long r0 = static_cast<long long>(c) * chunk;
   const long long r1 = r0 + chunk < N ? r0 + chunk : N;
 
-  // ---- sequences with nothing to read (empty or invalid), spread over the CTAs:
-  //      out = 0, lse = -inf
-  for (int b = c; b < B; b += ncta) {
-    bool valid;
-    if (pages_of(p, b, &valid) != 0) continue;
-    if (!valid && tid == 0) record_status(p.dev_status, PGQA_EINVAL);
-    for (int i = tid; i < p.num_q_heads * (D / 8); i += kThreads) {
-      const size_t row = static_cast<size_t>(b) * p.num_q_heads + i / (D / 8);
-      reinterpret_cast<uint4*>(p.out + row * D)[i % (D / 8)] = make_uint4(0, 0, 0, 0);
-      if (i % (D / 8) == 0 && p.lse) p.lse[row] = -INFINITY;
-    }
-  }
-  if (r0 >= r1) return;
-
   // ---- find the unit holding r0 (a CTA-wide scan over the sequences)
   if (tid == 0) misc[0] = -1;
   long long running = 0;  // pages of the sequences before `base`
-  for (int base = 0; base < B; base += kThreads) {
+  for (int base = 0; r0 < r1 && base < B; base += kThreads) {
     const int b = base + tid;
     const long long P = b < B ? pages_of(p, b) : 0;
     long long tot;
@@ -429,13 +417,15 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
     __syncthreads();
     if (misc[0] >= 0) break;
   }
-  Walk w0;
-  w0.b = misc[0];
-  w0.P = pages_of(p, w0.b);
-  w0.fp = first_page(p, w0.b);
-  w0.L = __ldg(p.context_lens + w0.b);
-  w0.h = static_cast<int>((r0 - scratch[kScanSlots - 1]) / w0.P);
-  w0.S = scratch[kScanSlots - 1] + static_cast<long long>(w0.h) * w0.P;
+  Walk w0{};
+  if (r0 < r1) {  // (the scan ran: misc[0] and the slot are set and published)
+    w0.b = misc[0];
+    w0.P = pages_of(p, w0.b);
+    w0.fp = first_page(p, w0.b);
+    w0.L = __ldg(p.context_lens + w0.b);
+    w0.h = static_cast<int>((r0 - scratch[kScanSlots - 1]) / w0.P);
+    w0.S = scratch[kScanSlots - 1] + static_cast<long long>(w0.h) * w0.P;
+  }
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -449,6 +439,22 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
     fence_mbar_init();
   }
   __syncthreads();
+
+  grid_dependency_wait();  // the stream's previous kernel (e.g. the KV append) is done
+
+  // ---- sequences with nothing to read (empty or invalid), spread over the CTAs:
+  //      out = 0, lse = -inf
+  for (int b = c; b < B; b += ncta) {
+    bool valid;
+    if (pages_of(p, b, &valid) != 0) continue;
+    if (!valid && tid == 0) record_status(p.dev_status, PGQA_EINVAL);
+    for (int i = tid; i < p.num_q_heads * (D / 8); i += kThreads) {
+      const size_t row = static_cast<size_t>(b) * p.num_q_heads + i / (D / 8);
+      reinterpret_cast<uint4*>(p.out + row * D)[i % (D / 8)] = make_uint4(0, 0, 0, 0);
+      if (i % (D / 8) == 0 && p.lse) p.lse[row] = -INFINITY;
+    }
+  }
+  if (r0 >= r1) return;
 
   // ================================================================ producer
   if (warp == kWarpProd) {
