@@ -54,6 +54,7 @@ constexpr int kWarpProd = kNW, kWarpMerge = kNW + 1;
 constexpr int kThreads = (kNW + 2) * 32;
 constexpr int kMinChunk = 8;  // pages per CTA range, at least
 constexpr int kYRing = 256;   // TMA row coordinates fetched ahead of issue
+static_assert(kYRing >= 64 + 32, "the fetch lookahead must fit the ring");
 constexpr int kScanSlots = kThreads / 32 + 1;  // one per warp, then the found unit start
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -203,17 +204,28 @@ __device__ __forceinline__ void bar_consumers() {
   asm volatile("bar.sync 1, %0;" ::"n"(kNW * 32) : "memory");
 }
 
+// What a unit epilogue reads and writes (passed by value: the epilogue functions are
+// not inlined, so the consumer warps' end-of-range call runs the code the merge warp
+// has already brought into the instruction cache mid-kernel).
+struct Epi {
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_lse;
+  float* part_o;
+  const float* v_scale;
+  int num_q_heads, group;
+};
+
 // Unit epilogue, run by nt threads (t = this thread's index among them).
-// combine_unit: the consumer warps' states of unit w from the merge buffer (M = max m_w,
-// l = sum l_w 2^(m_w - M), O likewise) -> the output, or, for a unit cut by range
-// boundaries (nseg > 1), this CTA's partial.
+// combine_unit: the consumer warps' states of unit (b, h) from the merge buffer
+// (M = max m_w, l = sum l_w 2^(m_w - M), O likewise) -> the output, or, for a unit cut
+// by range boundaries (nseg > 1), this CTA's partial (slot 0 or 1).
 template <int D, bool kFp8>
-__device__ __forceinline__ void combine_unit(const DecodeParams& p, const Walk& w, int nseg,
-                                             int slot, const float* wob, const float* wmlb,
-                                             int t, int nt) {
-  const int G = p.group;
+__device__ __noinline__ void combine_unit(const Epi e, int b, int h, int nseg, int slot,
+                                          const float* wob, const float* wmlb, int t, int nt) {
+  const int G = e.group;
   constexpr int kChunks = D / 8;  // 8 consecutive d per work item
-  const float vsc = kFp8 ? __ldg(p.v_scale + w.h) : 1.f;
+  const float vsc = kFp8 ? __ldg(e.v_scale + h) : 1.f;
   for (int it = t; it < G * kChunks; it += nt) {
     const int g = it / kChunks, cc = it % kChunks;
     float M = -INFINITY;
@@ -235,7 +247,7 @@ __device__ __forceinline__ void combine_unit(const DecodeParams& p, const Walk& 
       o[4] += y.x * wt; o[5] += y.y * wt; o[6] += y.z * wt; o[7] += y.w * wt;
     }
     const float inv = 1.f / lsum;
-    const size_t row = static_cast<size_t>(w.b) * p.num_q_heads + w.h * G + g;
+    const size_t row = static_cast<size_t>(b) * e.num_q_heads + h * G + g;
     if (nseg == 1) {
       uint4 pk = make_uint4(0, 0, 0, 0);
       if (!poisoned) {
@@ -243,59 +255,94 @@ __device__ __forceinline__ void combine_unit(const DecodeParams& p, const Walk& 
         pk = make_uint4(pack_bf16(o[0] * f, o[1] * f), pack_bf16(o[2] * f, o[3] * f),
                         pack_bf16(o[4] * f, o[5] * f), pack_bf16(o[6] * f, o[7] * f));
       }
-      reinterpret_cast<uint4*>(p.out + row * D)[cc] = pk;
-      if (cc == 0 && p.lse) p.lse[row] = poisoned ? -INFINITY : (M + log2f(lsum)) * kLn2;
+      reinterpret_cast<uint4*>(e.out + row * D)[cc] = pk;
+      if (cc == 0 && e.lse) e.lse[row] = poisoned ? -INFINITY : (M + log2f(lsum)) * kLn2;
     } else {
       const size_t ps = (static_cast<size_t>(blockIdx.x) * 2 + slot) * 8 + g;
-      float4* dst = reinterpret_cast<float4*>(p.part_o + ps * D + cc * 8);
+      float4* dst = reinterpret_cast<float4*>(e.part_o + ps * D + cc * 8);
       dst[0] = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
       dst[1] = make_float4(o[4] * inv, o[5] * inv, o[6] * inv, o[7] * inv);
-      if (cc == 0) p.part_lse[ps] = poisoned ? INFINITY : M + log2f(lsum);
+      if (cc == 0) e.part_lse[ps] = poisoned ? INFINITY : M + log2f(lsum);
     }
   }
 }
 
-// merge_partials: the last of the unit's CTAs to arrive merges their partials.
+// merge_partials: the last of the unit's CTAs to arrive merges their partials. The unit
+// starts at page S; CTA c (range [c * chunk, ...)) keeps it in slot 0 when the unit
+// starts at or before its range (its first unit), else in slot 1 (its last). Partials
+// are taken four at a time: a group's loads are all issued before any is used, then
+// merged into a running (M, l, O).
 template <int D, bool kFp8>
-__device__ __forceinline__ void merge_partials(const DecodeParams& p, const Walk& w,
-                                               long long chunk, int t, int nt) {
-  const int G = p.group;
+__device__ __noinline__ void merge_partials(const Epi e, int b, int h, long long S, int P,
+                                            long long chunk, int t, int nt) {
+  const int G = e.group;
   constexpr int kChunks = D / 8;
-  const float vsc = kFp8 ? __ldg(p.v_scale + w.h) : 1.f;
-  const long long c_first = w.S / chunk, c_last = (w.S + w.P - 1) / chunk;
+  constexpr int kGroup = 4;
+  const float vsc = kFp8 ? __ldg(e.v_scale + h) : 1.f;
+  const long long c_first = S / chunk, c_last = (S + P - 1) / chunk;
   for (int it = t; it < G * kChunks; it += nt) {
     const int g = it / kChunks, cc = it % kChunks;
-    float M = -INFINITY;
+    float M = -INFINITY, lsum = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     bool any_bad = false;
-    for (long long cta = c_first; cta <= c_last; ++cta) {
-      const int sl = (w.S <= cta * chunk) ? 0 : 1;
-      const float ls = __ldcg(p.part_lse + (cta * 2 + sl) * 8 + g);
-      any_bad |= ls == INFINITY;
-      M = fmaxf(M, ls);
-    }
-    float lsum = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (!any_bad) {
-      for (long long cta = c_first; cta <= c_last; ++cta) {
-        const int sl = (w.S <= cta * chunk) ? 0 : 1;
-        const size_t ps = static_cast<size_t>(cta * 2 + sl) * 8 + g;
-        const float wt = ex2(__ldcg(p.part_lse + ps) - M);
-        lsum += wt;
-        const float4* src = reinterpret_cast<const float4*>(p.part_o + ps * D + cc * 8);
-        const float4 x = __ldcg(src), y = __ldcg(src + 1);
-        o[0] += x.x * wt; o[1] += x.y * wt; o[2] += x.z * wt; o[3] += x.w * wt;
-        o[4] += y.x * wt; o[5] += y.y * wt; o[6] += y.z * wt; o[7] += y.w * wt;
+    for (long long base = c_first; base <= c_last; base += kGroup) {
+      float ls[kGroup];
+      float4 x[kGroup], y[kGroup];
+#pragma unroll
+      for (int k = 0; k < kGroup; ++k) {
+        const long long cta = base + k;
+        ls[k] = -INFINITY;
+        x[k] = y[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (cta <= c_last) {
+          const size_t ps = static_cast<size_t>(cta * 2 + (S <= cta * chunk ? 0 : 1)) * 8 + g;
+          const float4* src = reinterpret_cast<const float4*>(e.part_o + ps * D + cc * 8);
+          ls[k] = __ldcg(e.part_lse + ps);
+          x[k] = __ldcg(src);
+          y[k] = __ldcg(src + 1);
+        }
       }
+      float Mn = M;
+#pragma unroll
+      for (int k = 0; k < kGroup; ++k) {
+        any_bad |= ls[k] == INFINITY;
+        Mn = fmaxf(Mn, ls[k]);
+      }
+      if (Mn == INFINITY) continue;  // a poisoned partial: the result is discarded
+      const float a = M == -INFINITY ? 0.f : ex2(M - Mn);
+      lsum *= a;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) o[q] *= a;
+#pragma unroll
+      for (int k = 0; k < kGroup; ++k) {
+        const float wt = ls[k] == -INFINITY ? 0.f : ex2(ls[k] - Mn);
+        lsum += wt;
+        o[0] += x[k].x * wt; o[1] += x[k].y * wt; o[2] += x[k].z * wt; o[3] += x[k].w * wt;
+        o[4] += y[k].x * wt; o[5] += y[k].y * wt; o[6] += y[k].z * wt; o[7] += y[k].w * wt;
+      }
+      M = Mn;
     }
-    const size_t row = static_cast<size_t>(w.b) * p.num_q_heads + w.h * G + g;
+    const size_t row = static_cast<size_t>(b) * e.num_q_heads + h * G + g;
     uint4 pk = make_uint4(0, 0, 0, 0);
     if (!any_bad) {
       const float f = vsc / lsum;
       pk = make_uint4(pack_bf16(o[0] * f, o[1] * f), pack_bf16(o[2] * f, o[3] * f),
                       pack_bf16(o[4] * f, o[5] * f), pack_bf16(o[6] * f, o[7] * f));
     }
-    reinterpret_cast<uint4*>(p.out + row * D)[cc] = pk;
-    if (cc == 0 && p.lse) p.lse[row] = any_bad ? -INFINITY : (M + log2f(lsum)) * kLn2;
+    reinterpret_cast<uint4*>(e.out + row * D)[cc] = pk;
+    if (cc == 0 && e.lse) e.lse[row] = any_bad ? -INFINITY : (M + log2f(lsum)) * kLn2;
   }
+}
+
+// Arrival on a unit's ticket, wrapping to 0 on the last of `count` arrivals (so the
+// counter is ready for the next call). Release: this thread's writes, and those it has
+// seen through a barrier, are visible before the count moves; acquire: the arrival
+// that sees count - 1 sees every other arrival's writes. Returns true for that one.
+__device__ __forceinline__ bool ticket_last(int* counter, int count) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(counter), "r"(static_cast<unsigned>(count - 1))
+               : "memory");
+  return old == static_cast<unsigned>(count - 1);
 }
 
 // Segments of unit w over the CTA ranges, and which partial slot this CTA uses.
@@ -307,8 +354,9 @@ __device__ __forceinline__ int unit_segments(const Walk& w, long long chunk) {
 // consumer warps, which have nothing left to stream then, do that one with 128
 // threads), so the consumers hand a unit over and go straight on to the next.
 template <int D, bool kFp8>
-__device__ __forceinline__ void merge_units(const DecodeParams& p, const Walk& w0, long long r0,
-                                            long long r1, long long chunk, const float* wo,
+__device__ __forceinline__ void merge_units(const DecodeParams& p, const Epi epi, const Walk& w0,
+                                            long long r0, long long r1, long long chunk,
+                                            const float* wo,
                                             const float* wml, uint64_t* unit_done,
                                             uint64_t* merge_free) {
   const int lane = threadIdx.x & 31;
@@ -323,24 +371,16 @@ __device__ __forceinline__ void merge_units(const DecodeParams& p, const Walk& w
       return;
     }
     const int nseg = unit_segments(w, chunk);
-    combine_unit<D, kFp8>(p, w, nseg, w.S <= r0 ? 0 : 1, wo + mb * (kNW * 8 * D),
+    combine_unit<D, kFp8>(epi, w.b, w.h, nseg, w.S <= r0 ? 0 : 1, wo + mb * (kNW * 8 * D),
                           wml + mb * (kNW * 8 * 2), lane, 32);
     __syncwarp();  // every lane has read the buffer and issued its writes
     if (lane == 0) mbar_arrive(&merge_free[mb]);
     if (nseg > 1) {
-      unsigned last = 0;
-      if (lane == 0) {
-        __threadfence();
-        // atomicInc wraps to 0 on the last arrival, leaving the ticket ready for the next call
-        const unsigned prev = atomicInc(
-            reinterpret_cast<unsigned*>(p.counters + w.b * p.num_kv_heads + w.h),
-            static_cast<unsigned>(nseg - 1));
-        last = prev == static_cast<unsigned>(nseg - 1);
-      }
-      if (__shfl_sync(0xffffffffu, last, 0)) {
-        __threadfence();
-        merge_partials<D, kFp8>(p, w, chunk, lane, 32);
-      }
+      bool last = false;
+      if (lane == 0) last = ticket_last(p.counters + w.b * p.num_kv_heads + w.h, nseg);
+      last = __shfl_sync(0xffffffffu, last, 0);
+      __syncwarp();  // the lanes' reads of the partials come after lane 0's acquire
+      if (last) merge_partials<D, kFp8>(epi, w.b, w.h, w.S, w.P, chunk, lane, 32);
     }
     w = wn;
   }
@@ -372,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, ncta = gridDim.x;
   const int G = p.group, Hkv = p.num_kv_heads, B = p.num_seqs;
+  const Epi epi{p.out, p.lse, p.part_lse, p.part_o, p.v_scale, p.num_q_heads, p.group};
   if (warp == kWarpProd && lane == 0) {
     tma_prefetch_desc(&kmap);
     tma_prefetch_desc(&vmap);
@@ -440,6 +481,40 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
   }
   __syncthreads();
 
+  // ---- the producer's fetch cursor: row coordinates of this CTA's pages, read from
+  //      the block tables into yring; the first 32 before the wait
+  const int n = static_cast<int>(r1 - r0);  // pages of this CTA, CTA-local index 0..n-1
+  Walk fw = w0;                             // fetch cursor: unit and page within it
+  int fpg = static_cast<int>(r0 - w0.S);
+  int fetched = 0;  // pages whose row coordinate is in yring
+  auto fetch_rows = [&]() {
+    const int cnt = min(32, min(fw.P - fpg, n - fetched));
+    if (lane < cnt) {
+      // cache rows of 16-token page lp: one block of 16, half of a block of 32, or
+      // two blocks of 8 (the second only if the context reaches it)
+      const int32_t* btb = p.block_tables + static_cast<size_t>(fw.b) * p.max_blocks_per_seq;
+      const int lp = fw.fp + fpg + lane, bs = p.block_size;
+      const int blk = bs == 32 ? lp >> 1 : bs == 8 ? 2 * lp : lp;
+      const int32_t pbn = __ldg(btb + blk);
+      const bool ok0 = pbn >= 0 && pbn < p.num_blocks;
+      int y0 = ok0 ? (pbn * Hkv + fw.h) * bs + (bs == 32 ? (lp & 1) * 16 : 0) : -1, y1 = 0;
+      if (bs == 8) {
+        const int32_t pbn1 = (blk + 1) * 8 < fw.L ? __ldg(btb + blk + 1) : pbn;
+        y1 = (pbn1 >= 0 && pbn1 < p.num_blocks) ? (pbn1 * Hkv + fw.h) * 8 : -1;
+      }
+      yring[(fetched + lane) % kYRing] = y0;
+      yring2[(fetched + lane) % kYRing] = y1;
+    }
+    fetched += cnt;
+    fpg += cnt;
+    if (fpg == fw.P) {
+      fw.next(p);
+      fpg = 0;
+    }
+    __syncwarp();
+  };
+  if (warp == kWarpProd && n > 0) fetch_rows();
+
   grid_dependency_wait();  // the stream's previous kernel (e.g. the KV append) is done
 
   // ---- sequences with nothing to read (empty or invalid), spread over the CTAs:
@@ -458,10 +533,6 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
 
   // ================================================================ producer
   if (warp == kWarpProd) {
-    const int n = static_cast<int>(r1 - r0);  // pages of this CTA, CTA-local index 0..n-1
-    Walk fw = w0;                             // fetch cursor: unit and page within it
-    int fpg = static_cast<int>(r0 - w0.S);
-    int fetched = 0;  // pages whose row coordinate is in yring
     // lane w < kNW serves consumer warp w: its pages are w, w + kNW, ...
     const int nw_pages = lane < kNW && n > lane ? (n - lane + kNW - 1) / kNW : 0;
     int next_li = 0;  // next local index of that warp to issue
@@ -471,35 +542,6 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
           0xffffffffu, lane < kNW && next_li < nw_pages ? lane + kNW * next_li : INT_MAX);
       if (pend == INT_MAX) break;  // every page issued
       bool progress = false;
-      // fetch up to 32 row coordinates of the current unit, never overwriting an
-      // entry that is still to be issued
-      if (fetched < n && fetched < pend + kYRing - 32) {
-        const int cnt = min(32, min(fw.P - fpg, n - fetched));
-        if (lane < cnt) {
-          // cache rows of 16-token page lp: one block of 16, half of a block of 32, or
-          // two blocks of 8 (the second only if the context reaches it)
-          const int32_t* btb = p.block_tables + static_cast<size_t>(fw.b) * p.max_blocks_per_seq;
-          const int lp = fw.fp + fpg + lane, bs = p.block_size;
-          const int blk = bs == 32 ? lp >> 1 : bs == 8 ? 2 * lp : lp;
-          const int32_t pbn = __ldg(btb + blk);
-          const bool ok0 = pbn >= 0 && pbn < p.num_blocks;
-          int y0 = ok0 ? (pbn * Hkv + fw.h) * bs + (bs == 32 ? (lp & 1) * 16 : 0) : -1, y1 = 0;
-          if (bs == 8) {
-            const int32_t pbn1 = (blk + 1) * 8 < fw.L ? __ldg(btb + blk + 1) : pbn;
-            y1 = (pbn1 >= 0 && pbn1 < p.num_blocks) ? (pbn1 * Hkv + fw.h) * 8 : -1;
-          }
-          yring[(fetched + lane) % kYRing] = y0;
-          yring2[(fetched + lane) % kYRing] = y1;
-        }
-        fetched += cnt;
-        fpg += cnt;
-        if (fpg == fw.P) {
-          fw.next(p);
-          fpg = 0;
-        }
-        __syncwarp();
-        progress = true;
-      }
       // refill consumer warp `lane`'s next stage if it is free
       if (lane < kNW && next_li < nw_pages) {
         const int i = lane + kNW * next_li;
@@ -538,6 +580,13 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
           progress = true;
         }
       }
+      // then fetch up to 32 more row coordinates of the current unit while fewer than
+      // 64 are ahead of the issue cursor (a table read stalls this warp; the loads
+      // above are out by then), never overwriting an entry still to be issued
+      if (fetched < n && fetched < pend + 64) {
+        fetch_rows();
+        progress = true;
+      }
       if (__any_sync(0xffffffffu, progress)) {
         idle_since = 0;
       } else if (idle_since == 0) {
@@ -561,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
 
   // ================================================================ merge warp
   if (warp == kWarpMerge) {
-    merge_units<D, kFp8>(p, w0, r0, r1, chunk, wo, wml, unit_done, merge_free);
+    merge_units<D, kFp8>(p, epi, w0, r0, r1, chunk, wo, wml, unit_done, merge_free);
     return;
   }
 
@@ -844,21 +893,12 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
     // the range's last unit: nothing left to stream, so the consumer warps finish it
     const int nseg = unit_segments(w, chunk);
     bar_consumers();
-    combine_unit<D, kFp8>(p, w, nseg, w.S <= r0 ? 0 : 1, wob, wmlb, tid, kNW * 32);
+    combine_unit<D, kFp8>(epi, w.b, w.h, nseg, w.S <= r0 ? 0 : 1, wob, wmlb, tid, kNW * 32);
     if (nseg > 1) {
       bar_consumers();  // this CTA's partial writes are issued
-      if (tid == 0) {
-        __threadfence();
-        // atomicInc wraps to 0 on the last arrival, leaving the ticket ready for the next call
-        const unsigned prev = atomicInc(reinterpret_cast<unsigned*>(p.counters + w.b * Hkv + w.h),
-                                        static_cast<unsigned>(nseg - 1));
-        misc[1] = prev == static_cast<unsigned>(nseg - 1);
-      }
-      bar_consumers();
-      if (misc[1]) {
-        __threadfence();
-        merge_partials<D, kFp8>(p, w, chunk, tid, kNW * 32);
-      }
+      if (tid == 0) misc[1] = ticket_last(p.counters + w.b * Hkv + w.h, nseg);
+      bar_consumers();  // (and the reads below come after the acquire)
+      if (misc[1]) merge_partials<D, kFp8>(epi, w.b, w.h, w.S, w.P, chunk, tid, kNW * 32);
     }
     ++cu;
   }
