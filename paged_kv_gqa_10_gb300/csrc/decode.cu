@@ -98,15 +98,17 @@ struct Cfg {
   static constexpr int kSub = kRowBytes / 128;     // 128-byte TMA boxes per row
   static constexpr int kPageBytes = 16 * kRowBytes;
   static constexpr int kStageBytes = 2 * kPageBytes;  // K page + V page
-  // about 16 KB of pages in flight per consumer warp
-  static constexpr int kStagesPerWarp = kStageBytes >= 8192 ? 2 : 16384 / kStageBytes;
+  // about 16 KB of pages in flight per consumer warp (E4M3: 20 KB, with one merge
+  // buffer instead of two paying for the fifth stage)
+  static constexpr int kStagesPerWarp = kStageBytes >= 8192 ? 2 : kFp8 ? 5 : 16384 / kStageBytes;
+  static constexpr int kMergeBufs = kFp8 ? 1 : 2;  // unit states in flight to the merge warp
   static constexpr int kStages = kNW * kStagesPerWarp;
   static constexpr int kNkc = D / 16;              // 16-wide chunks of head_dim
   static constexpr int kRing = kStages * kStageBytes;
   static constexpr int kMerge = kNW * 8 * D * 4;   // per-warp O of one unit
   static constexpr int kOffMerge = kRing;          // [2] by unit parity
-  static constexpr int kOffMl = kOffMerge + 2 * kMerge;               // [2][kNW][8][2] float
-  static constexpr int kOffBar = kOffMl + 2 * kNW * 8 * 2 * 4;        // full[S], empty[S],
+  static constexpr int kOffMl = kOffMerge + kMergeBufs * kMerge;      // [bufs][kNW][8][2] float
+  static constexpr int kOffBar = kOffMl + kMergeBufs * kNW * 8 * 2 * 4;  // full[S], empty[S],
                                                                       // unit_done[2], merge_free[2]
   static constexpr int kOffMeta = kOffBar + (2 * kStages + 4) * 8;    // [S] int
   static constexpr int kOffY = kOffMeta + kStages * 4;                // [kYRing] int
@@ -365,8 +367,9 @@ __device__ __forceinline__ void merge_units(const DecodeParams& p, const Epi epi
     Walk wn = w;
     wn.next(p);
     if (!(wn.S < r1)) return;  // w is the range's last unit
-    const int mb = cu & 1;
-    if (!__all_sync(0xffffffffu, mbar_wait(&unit_done[mb], (cu >> 1) & 1))) {
+    constexpr int kBufs = Cfg<D, kFp8>::kMergeBufs;
+    const int mb = cu % kBufs;
+    if (!__all_sync(0xffffffffu, mbar_wait(&unit_done[mb], (cu / kBufs) & 1))) {
       if (lane == 0) record_status(p.dev_status, PGQA_ETIMEOUT);
       return;
     }
@@ -744,14 +747,15 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
       const int nv = min(16, L - pk0);               // rows below nv hold keys < L
       const int lo = max(0, kfirst - pk0);           // rows below lo are outside the window
 
-      // ---- S^T = K Q^T
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      // ---- S^T = K Q^T, over two accumulators (even / odd 16-wide chunks of head_dim)
+      //      so the MMA chain is half as long
+      float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (!kFp8) {
 #pragma unroll
         for (int kc = 0; kc < C::kNkc; ++kc) {
           uint32_t a0, a1, a2, a3;
           ldsm_x4(stK + (kc >> 2) * 2048 + swz128(rowK, (kc & 3) * 2 + cK), a0, a1, a2, a3);
-          mma_bf16(sc, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
+          mma_bf16((kc & 1) ? sd : sc, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
         }
       } else {
 #pragma unroll
@@ -760,11 +764,13 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
           ldsm_x4(stK + swz128(rowK, kc + cK), r0v, r1v, r2v, r3v);
           mma_f16(sc, e4m3x2_to_f16x2(r0v & 0xffff), e4m3x2_to_f16x2(r1v & 0xffff),
                   e4m3x2_to_f16x2(r0v >> 16), e4m3x2_to_f16x2(r1v >> 16), qf[kc][0], qf[kc][1]);
-          mma_f16(sc, e4m3x2_to_f16x2(r2v & 0xffff), e4m3x2_to_f16x2(r3v & 0xffff),
+          mma_f16(sd, e4m3x2_to_f16x2(r2v & 0xffff), e4m3x2_to_f16x2(r3v & 0xffff),
                   e4m3x2_to_f16x2(r2v >> 16), e4m3x2_to_f16x2(r3v >> 16), qf[kc + 1][0],
                   qf[kc + 1][1]);
         }
       }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) sc[q] += sd[q];
       // fragment: sc[0] (tok gid, head 2tig), sc[1] (gid, 2tig+1),
       //           sc[2] (gid+8, 2tig),      sc[3] (gid+8, 2tig+1)
       float s0 = sc[0] * sl2, s1 = sc[1] * sl2, s2 = sc[2] * sl2, s3 = sc[3] * sl2;
@@ -851,8 +857,10 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
       l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], o);
     }
     const bool poisoned_w = __any_sync(0xffffffffu, bad != 0) || !__all_sync(0xffffffffu, alive);
-    const int mb = cu & 1;
-    if (cu >= 2 && !__all_sync(0xffffffffu, mbar_wait(&merge_free[mb], ((cu >> 1) - 1) & 1))) {
+    constexpr int kBufs = C::kMergeBufs;
+    const int mb = cu % kBufs;
+    if (cu >= kBufs &&
+        !__all_sync(0xffffffffu, mbar_wait(&merge_free[mb], ((cu / kBufs) - 1) & 1))) {
       alive = false;
       if (lane == 0) record_status(p.dev_status, PGQA_ETIMEOUT);
     }
