@@ -114,7 +114,8 @@ struct Cfg {
   static constexpr int kOffY = kOffMeta + kStages * 4;                // [kYRing] int
   static constexpr int kOffY2 = kOffY + kYRing * 4;                   // [kYRing] int (block 8)
   static constexpr int kOffMisc = kOffY2 + kYRing * 4;                // 32 ints, kScanSlots int64
-  static constexpr int kSmem = 1024 + kOffMisc + 32 * 4 + kScanSlots * 8;
+  static constexpr int kOffRuns = kOffMisc + 32 * 4 + kScanSlots * 8;   // Run[3]
+  static constexpr int kSmem = 1024 + kOffRuns + 3 * 48;
   static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle rows");
 };
 
@@ -201,6 +202,65 @@ struct Walk {
     }
   }
 };
+
+// The order a CTA works through its range [r0, r1): runs of consecutive pages of the
+// global order, `count` pages from page `first` of unit w on (crossing into the
+// following units). The unit holding r1 - 1 (its part in the range) comes first, then
+// the unit holding r0, then the whole units between: the two units the CTA may share
+// with its neighbours are done early (their cross-CTA merge happens mid-kernel) and the
+// range ends on a unit of its own, whose epilogue needs no other CTA.
+struct Run {
+  Walk w;
+  int first, count;
+};
+static_assert(sizeof(Run) <= 48, "run slot");
+
+// Walks the units of the runs in order: unit w, its pages [seg0, seg0 + npg()).
+struct Cursor {
+  Walk w;
+  int seg0, left, run, nruns;
+  __device__ __forceinline__ int npg() const { return min(w.P - seg0, left); }
+  __device__ __forceinline__ void start(const Run* runs, int n) {
+    nruns = n;
+    run = 0;
+    w = runs[0].w;
+    seg0 = runs[0].first;
+    left = runs[0].count;
+  }
+  // false past the last unit
+  __device__ __forceinline__ bool next(const DecodeParams& p, const Run* runs) {
+    left -= npg();
+    if (left > 0) {
+      w.next(p);
+      seg0 = 0;
+      return true;
+    }
+    if (++run >= nruns) return false;
+    w = runs[run].w;
+    seg0 = runs[run].first;
+    left = runs[run].count;
+    return true;
+  }
+};
+
+// The runs of range [r0, r1), w0 = the unit holding r0; returns how many (1 to 3).
+__device__ __forceinline__ int plan_runs(const DecodeParams& p, const Walk& w0, long long r0,
+                                         long long r1, Run* runs) {
+  Walk wt = w0;
+  while (wt.S + wt.P < r1) wt.next(p);  // the unit holding r1 - 1
+  if (wt.S <= r0) {                     // the range lies inside one unit
+    runs[0] = Run{w0, static_cast<int>(r0 - w0.S), static_cast<int>(r1 - r0)};
+    return 1;
+  }
+  const long long h1 = w0.S + w0.P;  // end of the unit holding r0 (<= wt.S)
+  runs[0] = Run{wt, 0, static_cast<int>(r1 - wt.S)};
+  runs[1] = Run{w0, static_cast<int>(r0 - w0.S), static_cast<int>(h1 - r0)};
+  if (h1 == wt.S) return 2;
+  Walk wm = w0;
+  wm.next(p);
+  runs[2] = Run{wm, 0, static_cast<int>(wt.S - h1)};
+  return 3;
+}
 
 __device__ __forceinline__ void bar_consumers() {
   asm volatile("bar.sync 1, %0;" ::"n"(kNW * 32) : "memory");
@@ -356,17 +416,17 @@ __device__ __forceinline__ int unit_segments(const Walk& w, long long chunk) {
 // consumer warps, which have nothing left to stream then, do that one with 128
 // threads), so the consumers hand a unit over and go straight on to the next.
 template <int D, bool kFp8>
-__device__ __forceinline__ void merge_units(const DecodeParams& p, const Epi epi, const Walk& w0,
-                                            long long r0, long long r1, long long chunk,
-                                            const float* wo,
+__device__ __forceinline__ void merge_units(const DecodeParams& p, const Epi epi,
+                                            const Run* runs, int nruns, long long r0,
+                                            long long chunk, const float* wo,
                                             const float* wml, uint64_t* unit_done,
                                             uint64_t* merge_free) {
   const int lane = threadIdx.x & 31;
-  int cu = 0;
-  for (Walk w = w0;; ++cu) {
-    Walk wn = w;
-    wn.next(p);
-    if (!(wn.S < r1)) return;  // w is the range's last unit
+  Cursor cur;
+  cur.start(runs, nruns);
+  for (int cu = 0;; ++cu) {
+    const Walk w = cur.w;
+    if (!cur.next(p, runs)) return;  // w is the range's last unit
     constexpr int kBufs = Cfg<D, kFp8>::kMergeBufs;
     const int mb = cu % kBufs;
     if (!__all_sync(0xffffffffu, mbar_wait(&unit_done[mb], (cu / kBufs) & 1))) {
@@ -385,7 +445,6 @@ __device__ __forceinline__ void merge_units(const DecodeParams& p, const Epi epi
       __syncwarp();  // the lanes' reads of the partials come after lane 0's acquire
       if (last) merge_partials<D, kFp8>(epi, w.b, w.h, w.S, w.P, chunk, lane, 32);
     }
-    w = wn;
   }
 }
 
@@ -411,6 +470,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
   int* yring2 = reinterpret_cast<int*>(smem + C::kOffY2);  // its second 8-row block (block 8)
   int* misc = reinterpret_cast<int*>(smem + C::kOffMisc);
   long long* scratch = reinterpret_cast<long long*>(misc + 32);  // kScanSlots slots
+  Run* runs = reinterpret_cast<Run*>(smem + C::kOffRuns);         // the range's order
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, ncta = gridDim.x;
@@ -472,6 +532,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
   }
 
   if (tid == 0) {
+    misc[2] = r0 < r1 ? plan_runs(p, w0, r0, r1, runs) : 0;
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
@@ -487,11 +548,14 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
   // ---- the producer's fetch cursor: row coordinates of this CTA's pages, read from
   //      the block tables into yring; the first 32 before the wait
   const int n = static_cast<int>(r1 - r0);  // pages of this CTA, CTA-local index 0..n-1
-  Walk fw = w0;                             // fetch cursor: unit and page within it
-  int fpg = static_cast<int>(r0 - w0.S);
-  int fetched = 0;  // pages whose row coordinate is in yring
+  const int nruns = misc[2];
+  // fetch cursor: run, unit and page within it, pages left in the run
+  int frun = 0;
+  Walk fw = nruns > 0 ? runs[0].w : w0;
+  int fpg = nruns > 0 ? runs[0].first : 0, fleft = nruns > 0 ? runs[0].count : 0;
+  int fetched = 0;  // pages whose row coordinate is in yring (CTA-local order)
   auto fetch_rows = [&]() {
-    const int cnt = min(32, min(fw.P - fpg, n - fetched));
+    const int cnt = min(32, min(fw.P - fpg, fleft));
     if (lane < cnt) {
       // cache rows of 16-token page lp: one block of 16, half of a block of 32, or
       // two blocks of 8 (the second only if the context reaches it)
@@ -510,7 +574,14 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
     }
     fetched += cnt;
     fpg += cnt;
-    if (fpg == fw.P) {
+    fleft -= cnt;
+    if (fleft == 0) {
+      if (++frun < nruns) {
+        fw = runs[frun].w;
+        fpg = runs[frun].first;
+        fleft = runs[frun].count;
+      }
+    } else if (fpg == fw.P) {
       fw.next(p);
       fpg = 0;
     }
@@ -613,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
 
   // ================================================================ merge warp
   if (warp == kWarpMerge) {
-    merge_units<D, kFp8>(p, epi, w0, r0, r1, chunk, wo, wml, unit_done, merge_free);
+    merge_units<D, kFp8>(p, epi, runs, nruns, r0, chunk, wo, wml, unit_done, merge_free);
     return;
   }
 
@@ -648,11 +719,14 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
       }
     }
   };
-  load_q(w0);
-  for (Walk w = w0; w.S < r1; w.next(p)) {
-    const int seg0 = static_cast<int>((r0 > w.S ? r0 : w.S) - w.S);
-    const int seg1 = static_cast<int>((r1 < w.S + w.P ? r1 : w.S + w.P) - w.S);
-    const int npg = seg1 - seg0;
+  Cursor cur;
+  cur.start(runs, nruns);
+  load_q(cur.w);
+  for (bool more = true; more;) {
+    const Walk w = cur.w;
+    const int seg0 = cur.seg0, npg = cur.npg();
+    Cursor nxt = cur;  // the next unit, if any
+    more = nxt.next(p, runs);
     const int L = __ldg(p.context_lens + w.b);
     const int kfirst = first_key(p, L);
 
@@ -668,11 +742,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
         qf[kc][1] = pack_f16(bf16_lo(qraw[kc][1]), bf16_hi(qraw[kc][1]));
       }
     }
-    {
-      Walk wn = w;
-      wn.next(p);
-      if (wn.S < r1) load_q(wn);
-    }
+    if (more) load_q(nxt.w);
 
     // fused append: the page holding key L-1, if this warp reads it (segment-relative),
     // this lane's 16-byte chunk of the new K (lanes 0..kAppLanes-1) or V row, still
@@ -891,9 +961,8 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
       ml[3] = poisoned_w ? NAN : l_run[1];
     }
     __syncwarp();
-    Walk wn = w;
-    wn.next(p);
-    if (wn.S < r1) {  // the merge warp takes the unit
+    cur = nxt;
+    if (more) {  // the merge warp takes the unit
       if (lane == 0) mbar_arrive(&unit_done[mb]);
       ++cu;
       continue;
