@@ -159,6 +159,14 @@ struct Item {
   }
 };
 
+// Query heads per tile: 1, or G/2 in the grouped layout (groups of 4 or 8 heads and
+// chunks of at most 256/G tokens, as in speculative verification): tile A then holds
+// the group's first G/2 heads and tile B the rest, for every token of the chunk, one
+// row per (token, head), token-major. The host chooses it by setting pairs = Hkv.
+__device__ __forceinline__ int heads_per_tile(const PrefillParams& p) {
+  return p.pairs == p.num_kv_heads && p.group >= 4 ? p.group / 2 : 1;
+}
+
 // Maps ticket t of the dense item list to its item. `lvl` is the caller's level
 // cursor (the tickets a CTA receives only grow, so it only moves down).
 __device__ __forceinline__ Item item_of(const PrefillParams& p, int t, int& lvl) {
@@ -171,10 +179,11 @@ __device__ __forceinline__ Item item_of(const PrefillParams& p, int t, int& lvl)
   w.t = lvl;
   const int j = t - lvl_off[lvl];
   w.seq = sorted[j / p.pairs];
-  const int per_group = (p.group + 1) / 2, pi = j % p.pairs;
+  const bool grouped = heads_per_tile(p) > 1;
+  const int per_group = grouped ? 1 : (p.group + 1) / 2, pi = j % p.pairs;
   const int kv = pi / per_group;
-  w.hq = kv * p.group + 2 * (pi % per_group);
-  w.active_b = w.hq + 1 < (kv + 1) * p.group;
+  w.hq = kv * p.group + (grouped ? 0 : 2 * (pi % per_group));
+  w.active_b = grouped || w.hq + 1 < (kv + 1) * p.group;
   seq_ok(p, w.seq, &w.start, &w.Lq, &w.Lk);
   w.bad = 0;
   return w;
@@ -539,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
                           w.start + w.t * kBlockM);
               if (w.active_b)
                 tma_load_3d(smem + C::kQ + C::kTile + sub * 16384, &qmap, q_full, sub * 64,
-                            w.hq + 1, w.start + w.t * kBlockM);
+                            w.hq + heads_per_tile(p), w.start + w.t * kBlockM);
             }
           }
         }
@@ -768,7 +777,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       gl += 2 * w.nkt();
       if (X == 1 && !w.active_b) continue;
       const int tq = w.t;                   // this tile's index among the new tokens
-      const int qpos = tq * kBlockM + r;    // this row's position among the new tokens
+      const int hpt = heads_per_tile(p);    // grouped layout: row r = (token r / hpt, head)
+      const int qpos = tq * kBlockM + r / hpt;  // this row's position among the new tokens
+      const int hq_row = w.hq + X * hpt + r % hpt;  // this row's query head
       const int off = w.Lk - w.Lq;          // cached tokens before the new ones
       const int lim = min(off + qpos, w.Lk - 1);  // last key this row attends
       const int first_lim = off + tq * kBlockM;   // the tile's first row's last key
@@ -874,7 +885,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       tc_fence_after();
       const bool store = qpos < w.Lq;
       const size_t orow =
-          static_cast<size_t>(w.start + (store ? qpos : 0)) * p.num_q_heads + w.hq + X;
+          static_cast<size_t>(w.start + (store ? qpos : 0)) * p.num_q_heads + hq_row;
       uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D);
       const float inv = (F8 ? __ldg(v_scale + kvh) : 1.f) / l;
 #pragma unroll
@@ -921,10 +932,14 @@ pgqa_status_t launch_prefill_variant(const PrefillArgs& a) {
   const uint64_t row_bytes = F8 ? D : D * 2;
   const uint32_t box_inner = F8 ? D : 64;
   const CUtensorMapSwizzle kv_swz = F8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+  // grouped layout (see heads_per_tile) for short chunks of groups of 4 or 8 heads: a Q
+  // tile is G/2 heads x 256/G tokens (128 rows, token-major), else 1 head x 128 tokens
+  const int group = a.num_q_heads / a.num_kv_heads;
+  const bool grouped = (group == 4 || group == 8) && a.max_seqlen <= 256 / group;
   if (!tensor_map_3d(&qmap, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, a.num_q_heads,
                      a.num_tokens, static_cast<uint64_t>(D) * 2,
-                     static_cast<uint64_t>(a.num_q_heads) * D * 2, 64, 1, kBlockM,
-                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+                     static_cast<uint64_t>(a.num_q_heads) * D * 2, 64, grouped ? group / 2 : 1,
+                     grouped ? 256 / group : kBlockM, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !tensor_map_2d(&kmap, a.k_cache, kv_type, D, rows, row_bytes, box_inner, 16, kv_swz) ||
       !tensor_map_2d(&vmap, a.v_cache, kv_type, D, rows, row_bytes, box_inner, 16, kv_swz))
     return PGQA_ECUDA;
@@ -951,7 +966,7 @@ pgqa_status_t launch_prefill_variant(const PrefillArgs& a) {
   p.group = a.num_q_heads / a.num_kv_heads;
   p.num_blocks = a.num_blocks;
   p.n_levels = (a.max_seqlen + kBlockM - 1) / kBlockM;
-  p.pairs = a.num_kv_heads * ((p.group + 1) / 2);
+  p.pairs = grouped ? a.num_kv_heads : a.num_kv_heads * ((p.group + 1) / 2);
   p.oob_row = static_cast<int>(rows);
   p.scale_log2 = a.scale * kLog2e;
   const long long items = static_cast<long long>(p.n_levels) * a.num_seqs * p.pairs;

@@ -193,3 +193,30 @@ def test_key_length_shorter_than_chunk_is_reported():
     run.write()
     run.prefill()
     assert run.status_code() == pgqa.EINVAL
+
+
+@pytest.mark.parametrize("G,lens_q", [(4, [1, 5, 64, 17, 33, 2]), (8, [1, 6, 32, 9, 31, 2])])
+def test_grouped_rows_layout(G, lens_q):
+    """Chunks of at most 256/G tokens for groups of 4 or 8 take the grouped layout (a
+    tile holds G/2 heads of every token of the chunk): every row against the oracle,
+    chunk lengths up to the layout's limit, prefixes across tile edges."""
+    lens_k = [1, 300, 64, 129, 700, 2]
+    inp, run, kc, vc = _case(lens_k, lens_q, 2 * G, 2, 128, seed=370 + G)
+    ref_out, ref_lse = oracle_rows(inp, kc, vc)
+    assert_attention_close(run.out, run.lse, ref_out, ref_lse, f"grouped rows G={G}")
+
+
+@pytest.mark.parametrize("G", [4, 8])
+def test_grouped_rows_whole_sequences(G):
+    """The plain varlen prefill with every sequence within the grouped layout's limit."""
+    lens = [1, 17, 256 // G, 5]
+    nb = sum(-(-L // 16) for L in lens) + 8
+    inp = workloads.make_chunked_prefill(lens, lens, 2 * G, 2, 64, nb, seed=380 + G)
+    run = ChunkRun(inp)
+    run.write()
+    pgqa.paged_prefill_varlen(run.out, run.lse, run.q, run.kc, run.vc, run.bt, run.cu, max(lens),
+                              inp.scale, workspace=run.ws, dev_status=run.status)
+    assert run.status_code() == 0
+    kc, vc = oracle_cache(inp)
+    ref_out, ref_lse = oracle_rows(inp, kc, vc)
+    assert_attention_close(run.out, run.lse, ref_out, ref_lse, f"grouped whole sequences G={G}")

@@ -185,3 +185,12 @@ def test_nonpositive_scale_is_reported():
     run.ks[1] = 0.0
     run.prefill()
     assert run.status_code() == pgqa.EINVAL
+
+
+def test_grouped_rows_speculative_e4m3():
+    lens_k = [37, 256, 513, 1000, 64, 129]
+    nb = sum(-(-L // 16) for L in lens_k) + 8
+    inp = workloads.make_chunked_prefill(lens_k, [5] * len(lens_k), 32, 8, 128, nb, seed=480)
+    run, kc, vc = _run(inp)
+    ref_out, ref_lse = run.oracle_rows(kc, vc)
+    assert_attention_close(run.out, run.lse, ref_out, ref_lse, "e4m3 grouped rows")
