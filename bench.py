@@ -139,6 +139,21 @@ def _dist():
     return None, rank, local, world
 
 
+def reduce_max(res, keys, dist, device):
+    """Every rank's timings replaced by their maximum over the ranks (the slowest rank
+    sets the whole job's time)."""
+    for k in keys:
+        t = torch.tensor([float(res[k])], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        res[k] = float(t.item())
+    return res
+
+
+def job_value(bytes_per_rank, world, ms):
+    """Whole-job GB/s: every rank streams its own replica of the batch (weak scaling)."""
+    return bytes_per_rank * world / (ms * 1e-3) / 1e9
+
+
 def _cpu_baseline(inp, target_s=10.0):
     """The oracle, as it stands, on the host cores: the whole batch, repeated
     until about target_s seconds of CPU work have been timed."""
@@ -395,10 +410,7 @@ def measure_decode(inp, args, dev, dist=None, clocks_index=None):
            "ms_two": ms_two / args.steps, "dec_ms": dec_ms, "e2e_ms": e2e_ms / args.steps, "h2d": h2d, "d2h": d2h,
            "clocks": clocks}
     if dist:
-        for k in ("ms_graph", "ms_eager", "ms_two", "dec_ms", "e2e_ms"):
-            t = torch.tensor([res[k]], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            res[k] = float(t.item())
+        reduce_max(res, ("ms_graph", "ms_eager", "ms_two", "dec_ms", "e2e_ms"), dist, dev)
     return res
 
 
@@ -643,7 +655,7 @@ def run_ours(args):
     m = measure_decode(inp, args, dev, dist, clocks_index=local)
     b = m["bench"]
     kv_bytes = b.kv_bytes
-    value = kv_bytes * world / (m["ms_graph"] * 1e-3) / 1e9
+    value = job_value(kv_bytes, world, m["ms_graph"])
     pref = measure_prefill(args, dev) if (args.workload == "llama3_8b" and not args.no_prefill) \
         else None
     if rank != 0:
