@@ -406,12 +406,26 @@ def measure_decode(inp, args, dev, dist=None, clocks_index=None):
     d_out, d_lse = view(d_res, 0, ob, b.out), view(d_res, al(ob), lb, b.lse)
     h_res = torch.empty(al(ob) + lb, dtype=torch.uint8).pin_memory()
 
+    # the C-ABI call itself, its arguments marshalled once (the buffers do not move)
+    import ctypes
+    fn = pgqa._handle().pgqa_paged_attention_decode_append
+    vp = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
+    NB, Hkv, bs, D = b.kc.shape
+    B, Hq, _ = inp.q.shape
+    ws = b.ws if b.ws_n else None
+    c_args = (vp(d_out), vp(d_lse), vp(d_q), vp(d_k), vp(d_v), vp(b.kc), vp(b.vc), vp(d_bt),
+              ctypes.c_int(d_bt.shape[1]), vp(d_cl), ctypes.c_int(B), ctypes.c_int(Hq),
+              ctypes.c_int(Hkv), ctypes.c_int(D), ctypes.c_int(NB), ctypes.c_int(bs),
+              ctypes.c_float(inp.scale), ctypes.c_int(pgqa._cache_dtype(b.kc)), vp(b.ks),
+              vp(b.vs), ctypes.c_int(inp.max_context_len), vp(ws),
+              ctypes.c_size_t(0 if ws is None else ws.numel()), vp(b.status),
+              ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
     def e2e_step(i):
         d_in.copy_(h_in[i % b.R], non_blocking=True)
-        pgqa.paged_attention_decode_append(
-            d_out, d_lse, d_q, d_k, d_v, b.kc, b.vc, d_bt, d_cl, inp.scale, inp.max_context_len,
-            k_scale=b.ks, v_scale=b.vs, workspace=b.ws if b.ws_n else None,
-            dev_status=b.status)
+        rc = fn(*c_args)
+        if rc != 0:
+            raise RuntimeError(f"paged_attention_decode_append: {pgqa.status_string(rc)}")
         h_res.copy_(d_res, non_blocking=True)
 
     h2d = total
@@ -710,8 +724,9 @@ def run_ours(args):
         "e2e": {"value": kv_bytes * world / (m["e2e_ms"] * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"],
                 "ms_per_step": m["e2e_ms"],
-                "calls": "eager C-ABI call per step; inputs packed in one pinned buffer (one "
-                         "host-to-device copy), out and lse read back with one copy"},
+                "calls": "eager C-ABI call per step (arguments marshalled once); inputs packed "
+                         "in one pinned buffer (one host-to-device copy), out and lse read back "
+                         "with one copy"},
         "gpu_launches": args.steps,
         "clocks": m["clocks"],
     }
