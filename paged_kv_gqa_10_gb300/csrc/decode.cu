@@ -16,15 +16,25 @@
 //    a unit cut by range boundaries is finished by whichever of its CTAs arrives
 //    last (an atomic ticket: no CTA waits for another), which merges the partial
 //    results with their LSEs. Only the first and the last unit of a range can be
-//    cut, so each CTA owns two partial slots.
+//    cut, so each CTA owns two partial slots. A CTA takes its range as runs: the unit
+//    holding its last page, then the unit holding its first page, then the whole
+//    units between, so the shared units are merged mid-kernel and the range ends,
+//    when it can, on a unit no other CTA touches.
+//  - The range plan (context-length scan, unit search, first block-table rows) reads
+//    only context lengths and block tables and runs before the wait for the stream's
+//    previous kernel (programmatic launch); q, K/V and the workspace come after it.
+//  - Fused append (optional): the warp that reads the page holding key L-1 writes the
+//    step's new K/V row into the cache and over that row of its shared-memory copy.
 //  - Warp roles: one producer warp streams pages with TMA (2-D tensor map over the
 //    cache viewed as [num_blocks*Hkv*16 rows][head_dim], 128-byte swizzle) into
 //    mbarrier-guarded stages; 4 consumer warps take pages round-robin. Each consumer
 //    warp owns its own sub-ring of stages, so consecutive uses of a stage belong to
 //    one warp and a parity wait can never be two phases behind. The producer reads
-//    the block table up to 256 pages ahead (coalesced, into a shared ring of row
+//    the block table 64 pages ahead (coalesced, into a shared ring of row
 //    coordinates) and refills each consumer warp's stages as soon as that warp frees
-//    one (non-blocking polls), so a slow warp never holds back the others' loads.
+//    one (non-blocking polls), so a slow warp never holds back the others' loads. A
+//    merge warp takes each finished unit's per-warp states and writes its output or
+//    partial, so the consumers go straight on to the next unit.
 //    Consumers read each unit's query rows straight from global memory, one unit
 //    ahead.
 //  - Math per 16-token page on the warp-level tensor path (mma.m16n8k16):

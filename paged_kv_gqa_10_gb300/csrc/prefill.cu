@@ -25,6 +25,10 @@
 //    SM) takes items from the list with an atomic ticket counter, so the load
 //    balances itself whatever the length mix; the last CTA to finish resets the
 //    counter for the next call.
+//  - Short chunks of groups of 4 or 8 heads (at most 256/G tokens, as in speculative
+//    verification) use the grouped layout: an item is one (sequence, kv-head), tile A
+//    holds the group's first G/2 heads and tile B the rest, one row per (token, head)
+//    of the chunk, token-major.
 // Warp roles (12 warps; warp 11 only waits: at 384 threads the register allocator
 // fits the softmax in 167 registers without spilling)
 //  - warp 10 (planner): takes tickets, decodes the items and checks their block ids,
