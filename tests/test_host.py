@@ -160,3 +160,20 @@ def test_decode_append_argument_validation():
     assert f(*args[:3], P + 8, *args[4:]) == pgqa.EINVAL           # misaligned rows
     assert f(*args[:15], 64, *args[16:]) == pgqa.EUNSUPPORTED      # 64-token blocks
     assert f(*args[:10], 0, *args[11:]) == pgqa.OK                 # nothing to do
+
+
+def test_binding_signatures_match_the_header():
+    """Every function the binding declares takes as many arguments as the header says."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    decl = {m.group(1): m.group(2) for m in
+            re.finditer(r"\b(pgqa_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text)}
+    lib = pgqa._handle()
+    checked = 0
+    for name, params in decl.items():
+        fn = getattr(lib, name)
+        if fn.argtypes is None:
+            continue
+        n = 0 if params.strip() in ("", "void") else params.count(",") + 1
+        assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
+        checked += 1
+    assert checked >= 12
