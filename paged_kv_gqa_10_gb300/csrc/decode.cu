@@ -478,6 +478,8 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
   int* meta = reinterpret_cast<int*>(smem + C::kOffMeta);  // per stage: bad block id seen
   int* yring = reinterpret_cast<int*>(smem + C::kOffY);    // row coordinate of page i % kYRing
   int* yring2 = reinterpret_cast<int*>(smem + C::kOffY2);  // its second 8-row block (block 8)
+  // misc[0]: the sequence holding r0 (scan result); [1]: the last-unit ticket result;
+  // [2]: number of runs
   int* misc = reinterpret_cast<int*>(smem + C::kOffMisc);
   long long* scratch = reinterpret_cast<long long*>(misc + 32);  // kScanSlots slots
   Run* runs = reinterpret_cast<Run*>(smem + C::kOffRuns);         // the range's order
