@@ -36,7 +36,9 @@ def assert_attention_close(out, lse, ref_out, ref_lse, what=""):
     if lse is not None:
         gl = lse.detach().cpu().double().numpy()
         same_inf = np.isinf(gl) & np.isinf(ref_lse) & (np.sign(gl) == np.sign(ref_lse))
-        lerr = np.where(same_inf, 0.0, np.abs(gl - ref_lse))
+        # equal infinities count as no error (and are not subtracted); a NaN or an
+        # unmatched infinity stays an error
+        lerr = np.abs(np.where(same_inf, 0.0, gl) - np.where(same_inf, 0.0, ref_lse))
         assert np.all(lerr <= LSE_ATOL), f"{what}: lse max abs err {np.nanmax(lerr):.3e}"
     return float(err.max())
 
