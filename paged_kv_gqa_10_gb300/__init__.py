@@ -9,10 +9,12 @@ raises ImportError if the library has not been built
 (``python -m paged_kv_gqa_10_gb300.build``).
 
 Functions (same names as the C entry points, without the ``pgqa_`` prefix):
-  kv_cache_write, paged_kv_gather, paged_attention_decode,
-  paged_attention_decode_noalloc, paged_prefill_varlen, decode_workspace_size,
-  decode_grid_size,
-  prefill_workspace_size, kv_cache_bytes, status_string, abi_version.
+  kv_cache_write, paged_kv_gather,
+  paged_attention_decode, paged_attention_decode_append,
+  paged_attention_decode_window, paged_attention_decode_noalloc,
+  paged_prefill_varlen, paged_prefill_varlen_kv, paged_prefill_varlen_e4m3,
+  decode_workspace_size, decode_grid_size, prefill_workspace_size, kv_cache_bytes,
+  status_string, abi_version.
 """
 import ctypes
 import os
@@ -21,10 +23,11 @@ import torch
 
 __all__ = [
     "PgqaError", "BF16", "E4M3", "kv_cache_write", "paged_kv_gather",
-    "paged_attention_decode", "paged_attention_decode_noalloc", "paged_prefill_varlen",
-    "decode_workspace_size",
-    "decode_grid_size", "prefill_workspace_size", "kv_cache_bytes", "status_string",
-    "abi_version", "library_path", "lib",
+    "paged_attention_decode", "paged_attention_decode_append", "paged_attention_decode_window",
+    "paged_attention_decode_noalloc", "paged_prefill_varlen", "paged_prefill_varlen_kv",
+    "paged_prefill_varlen_e4m3", "decode_workspace_size", "decode_grid_size",
+    "prefill_workspace_size", "kv_cache_bytes", "status_string", "abi_version",
+    "library_path", "lib",
 ]
 
 BF16 = 0

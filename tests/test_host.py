@@ -177,3 +177,12 @@ def test_binding_signatures_match_the_header():
         assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
         checked += 1
     assert checked >= 12
+
+
+def test_every_entry_point_has_a_python_binding():
+    """Each function the header declares is reachable from Python under the same name
+    without the ``pgqa_`` prefix, and is listed in the package's ``__all__``."""
+    for name in declared_functions():
+        short = name[len("pgqa_"):]
+        assert callable(getattr(pgqa, short, None)), short
+        assert short in pgqa.__all__, short
