@@ -154,28 +154,61 @@ def job_value(bytes_per_rank, world, ms):
     return bytes_per_rank * world / (ms * 1e-3) / 1e9
 
 
-def _cpu_baseline(inp, target_s=10.0):
-    """The oracle, as it stands, on the host cores: the whole batch, repeated
-    until about target_s seconds of CPU work have been timed."""
+def _finite(x):
+    """A float for the JSON line (NaN / inf as their names: strict JSON has neither)."""
+    x = float(x)
+    return x if x == x and abs(x) != float("inf") else str(x)
+
+
+def _parity_summary(gpu_res, ref_out, ref_lse):
+    """One decode step's GPU output against the oracle's, element by element, with the
+    parity tolerance: out within 1e-2 + 1e-2 |ref|, lse within 1e-3."""
+    import numpy as np
+    if isinstance(gpu_res, str):
+        return {"error": gpu_res}
+    out, lse = gpu_res
+    err = np.abs(np.asarray(out, np.float64) - ref_out)
+    ratio = err / (1e-2 + 1e-2 * np.abs(ref_out))
+    gl = np.asarray(lse, np.float64)
+    same_inf = np.isinf(gl) & np.isinf(ref_lse) & (np.sign(gl) == np.sign(ref_lse))
+    lerr = np.abs(np.where(same_inf, 0.0, gl) - np.where(same_inf, 0.0, ref_lse))
+    ok = bool(np.all(ratio <= 1.0) and np.all(lerr <= 1e-3))
+    return {"rows": int(ref_lse.size), "out_max_abs_err": _finite(err.max()),
+            "out_max_err_over_tolerance": _finite(ratio.max()),
+            "lse_max_abs_err": _finite(lerr.max()), "within_tolerance": ok}
+
+
+def _cpu_baseline(inp, target_s=10.0, gpu_res=None):
+    """The oracle, as it stands, on the host cores: the whole batch over its cache with
+    the step's new rows appended, repeated until about target_s seconds of CPU work
+    have been timed. The first result is also compared with the GPU's output of the
+    same step (gpu_res: (out, lse) as arrays, or the text of the error that kept the
+    GPU side from producing it)."""
     import oracle
     cores = oracle.default_threads()
-    args = (inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale)
-    kw = dict(threads=cores)
-    if inp.cache_dtype == "e4m3":
-        kw.update(dtype=oracle.E4M3, k_scale=inp.k_scale, v_scale=inp.v_scale)
+    dt = oracle.E4M3 if inp.cache_dtype == "e4m3" else oracle.BF16
+    kc, vc = oracle.kv_cache_write(inp.step_key, inp.step_value, inp.step_slots, inp.k_cache,
+                                   inp.v_cache, dtype=dt, k_scale=inp.k_scale,
+                                   v_scale=inp.v_scale)
+    args = (inp.q, kc, vc, inp.block_tables, inp.context_lens, inp.scale)
+    kw = dict(threads=cores, dtype=dt, k_scale=inp.k_scale, v_scale=inp.v_scale)
     t0 = time.perf_counter()
-    oracle.paged_decode(*args, **kw)
+    ref_out, ref_lse = oracle.paged_decode(*args, **kw)
     one = time.perf_counter() - t0
     reps = max(1, int(target_s / max(one, 1e-3)))
     t0 = time.perf_counter()
     for _ in range(reps):
         oracle.paged_decode(*args, **kw)
-    dt = (time.perf_counter() - t0) / reps
-    gbs = workloads.kv_read_bytes(inp) / dt / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"the whole batch ({inp.num_seqs} sequences, "
-                      f"{int(inp.context_lens.sum())} cached tokens) x {reps} repetitions, "
-                      f"fp64 C oracle, OpenMP over (sequence, kv-head), {dt * reps:.1f} s"}
+    dt_s = (time.perf_counter() - t0) / reps
+    gbs = workloads.kv_read_bytes(inp) / dt_s / 1e9
+    res = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+           "sample": f"the whole batch ({inp.num_seqs} sequences, "
+                     f"{int(inp.context_lens.sum())} cached tokens, the step's new rows "
+                     f"appended) x {reps} repetitions, fp64 C oracle, OpenMP over "
+                     f"(sequence, kv-head), {dt_s * reps:.1f} s"}
+    if gpu_res is not None:
+        res["parity"] = _parity_summary(gpu_res, ref_out, ref_lse)
+    return res
 
 
 def run_reference(args):
@@ -736,7 +769,14 @@ def run_ours(args):
         line["next"]["sliding_window_decode"] = measure_window_decode(args, dev)
         line["next"]["e4m3_prefill"] = measure_e4m3_prefill(args, dev)
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = _cpu_baseline(inp, args.cpu_seconds)
+        # one more step on the first block-table set, read back for the oracle to check
+        try:
+            b.decode_append(0)
+            b.check()
+            gpu_res = (b.out.float().cpu().numpy(), b.lse.cpu().numpy())
+        except Exception as e:  # reported in the line, never fatal to it
+            gpu_res = f"GPU step failed: {e!r}"
+        line["cpu_baseline"] = _cpu_baseline(inp, args.cpu_seconds, gpu_res)
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
