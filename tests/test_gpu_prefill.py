@@ -143,6 +143,14 @@ def test_ragged_lengths_full_compare(G, D):
     assert_attention_close(run.out, run.lse, ref_out, ref_lse, f"G={G} D={D}")
 
 
+def test_empty_sequences_in_the_batch():
+    """Sequences with no token (repeated cu_seqlens values, at the start, in the
+    middle and at the end) take no work, report nothing, and every other row is the
+    oracle's."""
+    run, ref_out, ref_lse = _full_case([0, 17, 0, 130, 1, 0], 8, 2, 128, seed=60)
+    assert_attention_close(run.out, run.lse, ref_out, ref_lse, "empty sequences")
+
+
 def test_one_long_sequence_full_compare():
     run, ref_out, ref_lse = _full_case([1000], 4, 1, 128, seed=50)
     assert_attention_close(run.out, run.lse, ref_out, ref_lse)

@@ -83,6 +83,16 @@ def test_chunks_full_compare(G, D):
     assert_attention_close(run.out, run.lse, ref_out, ref_lse, f"G={G} D={D}")
 
 
+@pytest.mark.parametrize("G", [1, 4])
+def test_empty_chunks_in_the_batch(G):
+    """Sequences with a cached prefix but no new token take no work and report
+    nothing; the other chunks match the oracle (G = 4: the grouped-rows layout)."""
+    inp, run, kc, vc = _case([40, 300, 17, 129, 5], [0, 5, 0, 3, 0], 2 * G, 2, 128,
+                             seed=310 + G)
+    ref_out, ref_lse = oracle_rows(inp, kc, vc)
+    assert_attention_close(run.out, run.lse, ref_out, ref_lse, f"empty chunks G={G}")
+
+
 def test_speculative_verification_full_compare():
     lens_k = [37, 256, 513, 1000, 64, 129]
     inp, run, kc, vc = _case(lens_k, [5] * len(lens_k), 32, 8, 128, seed=320)
