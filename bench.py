@@ -1,15 +1,22 @@
 """Benchmark of the paged GQA attention hot path on GB300.
 
-One step = one decode step of the Llama-3-8B-shaped batch (64 sequences, 32 query
-/ 8 kv heads, head_dim 128, contexts uniform on [256, 1024], 16-token blocks
-shuffled over an 8192-block pool): append the new token's K/V into the paged
-cache (kv_cache_write) and run paged decode attention over every cached token.
-The metric is decode KV-read GB/s: the K and V bytes of every cached token of
-every kv-head, read once per step, divided by the step time.
+One step = one decode step of the 70B-shaped batch (32 sequences, 64 query / 8 kv
+heads, head_dim 128, contexts uniform on [1024, 4096], 16-token blocks shuffled over
+the pool, bf16 cache): append the new token's K/V into the paged cache and run paged
+decode attention over every cached token, as one fused launch. The metric is decode
+KV-read GB/s: the K and V bytes of every cached token of every kv-head, read once
+per step, divided by the step time.
 
-Three block-table sets over disjoint physical blocks rotate from step to step, so
-each step reads ~156 MB that the previous two steps did not touch (> the 129 MB
-L2): the numbers are HBM numbers, not L2 numbers.
+Every other decode workload is measured the same way and reported beside it (the
+Llama-3-8B batch, the 70B batch over an E4M3 cache, the prefix-sharing batch), each
+with an element-by-element oracle check of one step; then the varlen prefill and
+the rows past it (chunked prefill, speculative verification, sliding-window decode,
+E4M3 prefill).
+
+Three block-table sets over disjoint physical blocks (or three disjoint caches)
+rotate from launch to launch, so each reads data that the previous two did not touch
+(> the 129 MB L2): the decode and cached-prefix numbers are HBM numbers, not L2
+numbers.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank runs the same per-GPU batch (weak scaling, no
@@ -34,7 +41,7 @@ import torch  # noqa: E402
 import workloads  # noqa: E402
 
 METRIC = "paged GQA decode KV-read GB/s (% of HBM peak); prefill TFLOP/s (% peak)"
-WORKLOAD = "Llama-3-8B decode: B=64, Hq=32, Hkv=8, D=128, block 16, ctx U[256,1024], pool 8192"
+DATA = "synthetic (seeded N(0,1) bf16 q/K/V, seeded shuffled block tables)"
 ROTATIONS = 2  # extra disjoint table sets -> 3 in rotation
 
 
@@ -211,30 +218,69 @@ def _cpu_baseline(inp, target_s=10.0, gpu_res=None):
     return res
 
 
+DECODE_WORKLOADS = {
+    "70b_bf16": (lambda: workloads.llama70b_decode(rotations=ROTATIONS),
+                 "70B decode: B=32, Hq=64, Hkv=8, D=128, block 16, ctx U[1024,4096], bf16 cache"),
+    "llama3_8b": (lambda: workloads.llama3_8b_decode(rotations=ROTATIONS),
+                  "Llama-3-8B decode: B=64, Hq=32, Hkv=8, D=128, block 16, ctx U[256,1024], "
+                  "pool 8192"),
+    "70b_e4m3": (lambda: workloads.llama70b_decode(cache_dtype="e4m3", rotations=ROTATIONS),
+                 "70B decode: B=32, Hq=64, Hkv=8, D=128, block 16, ctx U[1024,4096], E4M3 cache "
+                 "with per-kv-head scales"),
+    "prefix": (lambda: workloads.prefix_sharing_decode(rotations=ROTATIONS),
+               "prefix-sharing decode: B=16, ctx 8192, Hq=32, Hkv=8, D=128, block 16, groups of 4 "
+               "share the blocks of their first 4096 tokens"),
+}
+# the headline first (the largest single-GPU bf16 decode configuration), then the others
+DECODE_ORDER = ["70b_bf16", "llama3_8b", "70b_e4m3", "prefix"]
+
+
+def decode_config(name, inp):
+    """The static description of a decode workload, identical in both bench arms."""
+    B, Hq, D = inp.q.shape
+    kvb = workloads.kv_read_bytes(inp)
+    return {"workload": DECODE_WORKLOADS[name][1], "batch": B, "q_heads": Hq,
+            "kv_heads": inp.num_kv_heads, "head_dim": D, "block_size": inp.block_size,
+            "cache_dtype": inp.cache_dtype, "kv_bytes_per_step": kvb,
+            "unique_kv_bytes_per_step": workloads.kv_read_bytes(inp, unique=True),
+            "step": "the new token of every sequence appended at position L-1 and attention "
+                    "over the whole context",
+            "l2": f"{ROTATIONS + 1} rotating block-table sets over disjoint blocks "
+                  f"({(ROTATIONS + 1) * kvb / 1e6:.0f} MB > 129 MB L2)",
+            "parallelism": "replica per GPU"}
+
+
 def run_reference(args):
-    """The oracle as the reference arm: the same workload, metric and unit, timed
-    on the host cores (each step = the whole batch through the fp64 oracle)."""
+    """The oracle as the reference arm: the headline decode workload, metric and unit,
+    timed on the host cores (each step = the whole batch through the fp64 oracle, over
+    the cache with the step's new rows appended once before timing)."""
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return 0
     import oracle
-    inp = workloads.llama3_8b_decode()
+    inp = DECODE_WORKLOADS[args.workload][0]()
     cores = oracle.default_threads()
-    a = (inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale)
+    dt = oracle.E4M3 if inp.cache_dtype == "e4m3" else oracle.BF16
+    kc, vc = oracle.kv_cache_write(inp.step_key, inp.step_value, inp.step_slots, inp.k_cache,
+                                   inp.v_cache, dtype=dt, k_scale=inp.k_scale,
+                                   v_scale=inp.v_scale)
+    a = (inp.q, kc, vc, inp.block_tables, inp.context_lens, inp.scale)
+    kw = dict(threads=cores, dtype=dt, k_scale=inp.k_scale, v_scale=inp.v_scale)
     for _ in range(args.warmup):
-        oracle.paged_decode(*a, threads=cores)
+        oracle.paged_decode(*a, **kw)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.paged_decode(*a, threads=cores)
-    dt = (time.perf_counter() - t0) / max(args.steps, 1)
-    v = workloads.kv_read_bytes(inp) / dt / 1e9
-    sample = f"whole batch per step ({int(inp.context_lens.sum())} cached tokens)"
+        oracle.paged_decode(*a, **kw)
+    dt_s = (time.perf_counter() - t0) / max(args.steps, 1)
+    v = workloads.kv_read_bytes(inp) / dt_s / 1e9
+    sample = (f"whole batch per step ({inp.num_seqs} sequences, "
+              f"{int(inp.context_lens.sum())} cached tokens, the step's new rows appended)")
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt_s * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+        "data": DATA, "config": decode_config(args.workload, inp),
         "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -357,9 +403,10 @@ def _elapsed(fn, n):
     return e0.elapsed_time(e1)
 
 
-def measure_decode(inp, args, dev, dist=None, clocks_index=None):
-    """Step time (CUDA-graph replays and eager), decode-kernel time (CUDA events
-    around each eager launch) and the end-to-end step through the public API."""
+def measure_decode(inp, args, dev, dist=None, clocks_index=None, full=True):
+    """Step time (CUDA-graph replays over the rotating table sets) and the step kernel's
+    time (a graph of back-to-back launches); with full=True also the eager step, the
+    same step as two calls, and the end-to-end step through the public API."""
     b = DecodeBench(inp, dev)
     for i in range(args.warmup):
         b.step(i)
@@ -382,15 +429,16 @@ def measure_decode(inp, args, dev, dist=None, clocks_index=None):
     if dist:
         dist.barrier()
     b.check()
-    ms_eager = _elapsed(lambda i: b.step(args.warmup + i), args.steps)
-    # the same steps as two calls (cache write, then decode), for comparison
-    b.fused = False
-    b.capture()
-    b.run_steps(first, b.R)
-    b.check()
-    ms_two = _elapsed(lambda i: b.run_steps(first, args.steps) if i == 0 else None, 1)
-    b.check()
-    b.fused = True
+    if full:
+        ms_eager = _elapsed(lambda i: b.step(args.warmup + i), args.steps)
+        # the same steps as two calls (cache write, then decode), for comparison
+        b.fused = False
+        b.capture()
+        b.run_steps(first, b.R)
+        b.check()
+        ms_two = _elapsed(lambda i: b.run_steps(first, args.steps) if i == 0 else None, 1)
+        b.check()
+        b.fused = True
     # the step's kernel alone: one CUDA graph of back-to-back fused launches cycling
     # over the disjoint block-table sets (no launch finds the previous one's pages in
     # L2), timed with events on the launching stream; every launch appends the same
@@ -412,6 +460,12 @@ def measure_decode(inp, args, dev, dist=None, clocks_index=None):
     torch.cuda.synchronize()
     dec_ms = e0.elapsed_time(e1) / (reps * n_rep)
     b.check()
+    if not full:
+        res = {"bench": b, "ms_graph": ms_graph / args.steps, "dec_ms": dec_ms,
+               "clocks": clocks}
+        if dist:
+            reduce_max(res, ("ms_graph", "dec_ms"), dist, dev)
+        return res
 
     # end to end through the public API, eager calls: the step's inputs (q, the new K/V
     # rows, the lengths and the block table) packed in one pinned host buffer per
@@ -504,7 +558,7 @@ def measure_prefill(args, dev):
         prefill()
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    n = max(3, args.steps // 5)
+    n = max(20, args.steps)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
     for i in range(n):
         ev[i][0].record(stream)
@@ -524,7 +578,8 @@ def measure_prefill(args, dev):
              "paged_kv_gqa_10_gb300/csrc/ptx.cuh"]
     return {
         "workload": "varlen causal prefill: 16 seqs, L U[128,2048] (T=%d), Hq=32, Hkv=8, D=128" % T,
-        "value": tflops, "unit": "TFLOP/s", "ms": p_ms,
+        "value": tflops, "unit": "TFLOP/s", "ms": p_ms, "launches_timed": n,
+        "timing": "CUDA events around each launch, each after the cache write of the batch",
         "flops": flops, "flops_rule": "4*Hq*D*L(L+1)/2 per sequence (unmasked pairs only)",
         "roofline": {"bound": "tensor", "kernel": "paged_prefill_kernel<128>", "achieved": tflops,
                      "peak": bf16_peak, "unit": "TFLOP/s", "frac": tflops / bf16_peak,
@@ -538,8 +593,10 @@ def measure_prefill(args, dev):
 def measure_cached_prefix(args, dev):
     """The rows past prefill and decode: prefill over a cached prefix (chunked prefill)
     and speculative verification (5 tokens per sequence), each through
-    pgqa_paged_prefill_varlen_kv; the K/V are written once, then a CUDA graph of back to
-    back launches is timed with events."""
+    pgqa_paged_prefill_varlen_kv. The K/V are written once into the cache, which is then
+    copied to ROTATIONS more caches at other addresses; a CUDA graph of back-to-back
+    launches cycling over the copies is timed with events, so no launch finds the
+    previous one's K/V in L2."""
     import paged_kv_gqa_10_gb300 as pgqa
     hbm, bf16_peak, kind = _peaks()
     res = {}
@@ -557,21 +614,23 @@ def measure_cached_prefix(args, dev):
                          dtype=torch.uint8, device=dev)
         pgqa.kv_cache_write(inp.key.to(dev), inp.value.to(dev), inp.slot_mapping.to(dev), kc, vc,
                             dev_status=status)
+        caches = [(kc, vc)] + [(kc.clone(), vc.clone()) for _ in range(ROTATIONS)]
+        R = len(caches)
 
-        def call():
-            pgqa.paged_prefill_varlen_kv(out, lse, q, kc, vc, bt, cu, lk, inp.max_seqlen_q,
-                                         inp.max_seqlen_k, inp.scale, workspace=ws,
-                                         dev_status=status)
+        def call(r):
+            pgqa.paged_prefill_varlen_kv(out, lse, q, caches[r][0], caches[r][1], bt, cu, lk,
+                                         inp.max_seqlen_q, inp.max_seqlen_k, inp.scale,
+                                         workspace=ws, dev_status=status)
 
-        for _ in range(args.warmup):
-            call()
+        for i in range(args.warmup):
+            call(i % R)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
-        reps = 8
+        reps = 4 * R
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            for _ in range(reps):
-                call()
+            for i in range(reps):
+                call(i % R)
         g.replay()
         torch.cuda.synchronize()
         stream = torch.cuda.current_stream()
@@ -589,10 +648,10 @@ def measure_cached_prefix(args, dev):
         tflops = flops / (ms * 1e-3) / 1e12
         gbs = kvb / (ms * 1e-3) / 1e9
         entry = {"workload": inp.name, "ms": ms, "flops": flops, "TFLOP/s": tflops,
-                 "kv_bytes": kvb, "KV GB/s": gbs,
+                 "kv_bytes": kvb, "KV GB/s": gbs, "launches_timed": n * reps,
                  "call": "pgqa_paged_prefill_varlen_kv, a CUDA graph of back-to-back launches "
-                         f"over the same {kvb / 1e6:.0f} MB of K/V (part of it may still be in "
-                         "the 129 MB L2 from the previous launch)"}
+                         f"cycling over {R} copies of the cache at different addresses "
+                         f"({R} x {kvb / 1e6:.0f} MB of K/V > 129 MB L2)"}
         if name == "chunked_prefill":
             entry["roofline"] = {"bound": "tensor", "achieved": tflops, "peak": bf16_peak,
                                  "unit": "TFLOP/s", "frac": tflops / bf16_peak,
@@ -601,6 +660,8 @@ def measure_cached_prefix(args, dev):
             entry["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                                  "frac": gbs / hbm, "peak_kind": kind}
         res[name] = entry
+        del caches
+        torch.cuda.empty_cache()
     return res
 
 
@@ -631,7 +692,7 @@ def measure_e4m3_prefill(args, dev):
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     stream = torch.cuda.current_stream()
-    n = max(3, args.steps // 5)
+    n = max(20, args.steps)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
     for i in range(n):
         ev[i][0].record(stream)
@@ -643,7 +704,8 @@ def measure_e4m3_prefill(args, dev):
     flops = workloads.causal_flops(inp.seq_lens, Hq, D)
     tflops = flops / (ms * 1e-3) / 1e12
     return {"workload": inp.name + ", E4M3 cache", "ms": ms, "flops": flops,
-            "TFLOP/s": tflops, "call": "pgqa_paged_prefill_varlen_e4m3, events around each launch",
+            "TFLOP/s": tflops, "launches_timed": n,
+            "call": "pgqa_paged_prefill_varlen_e4m3, events around each launch",
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16_peak,
                          "unit": "TFLOP/s", "frac": tflops / bf16_peak,
                          "peak_kind": kind + " bf16 burst (cuBLAS); the MMAs run on f16 "
@@ -696,64 +758,119 @@ def measure_window_decode(args, dev, window=2048):
                          "frac": gbs / hbm, "peak_kind": kind}}
 
 
-DECODE_WORKLOADS = {
-    "llama3_8b": (lambda: workloads.llama3_8b_decode(rotations=ROTATIONS), WORKLOAD),
-    "70b_bf16": (lambda: workloads.llama70b_decode(rotations=ROTATIONS),
-                 "70B decode: B=32, Hq=64, Hkv=8, D=128, ctx U[1024,4096], bf16 cache"),
-    "70b_e4m3": (lambda: workloads.llama70b_decode(cache_dtype="e4m3", rotations=ROTATIONS),
-                 "70B decode: B=32, Hq=64, Hkv=8, D=128, ctx U[1024,4096], E4M3 cache"),
-    "prefix": (lambda: workloads.prefix_sharing_decode(rotations=ROTATIONS),
-               "prefix-sharing decode: B=16, ctx 8192, Hq=32, Hkv=8, D=128, groups of 4 share "
-               "4096 tokens"),
-}
+def _oracle_parity(inp, gpu_res):
+    """One decode step's GPU output (out, lse arrays, or the text of the error that kept
+    the GPU side from producing it) against the oracle over the cache with the step's
+    new rows appended."""
+    import oracle
+    if isinstance(gpu_res, str):
+        return {"error": gpu_res}
+    dt = oracle.E4M3 if inp.cache_dtype == "e4m3" else oracle.BF16
+    kc, vc = oracle.kv_cache_write(inp.step_key, inp.step_value, inp.step_slots, inp.k_cache,
+                                   inp.v_cache, dtype=dt, k_scale=inp.k_scale,
+                                   v_scale=inp.v_scale)
+    ref_out, ref_lse = oracle.paged_decode(inp.q, kc, vc, inp.block_tables, inp.context_lens,
+                                           inp.scale, threads=oracle.default_threads(),
+                                           dtype=dt, k_scale=inp.k_scale, v_scale=inp.v_scale)
+    return _parity_summary(gpu_res, ref_out, ref_lse)
+
+
+def _gpu_step_result(b):
+    """One more fused step on the first block-table set, read back for the oracle."""
+    try:
+        b.decode_append(0)
+        b.check()
+        return (b.out.float().cpu().numpy(), b.lse.cpu().numpy())
+    except Exception as e:  # reported in the line, never fatal to it
+        return f"GPU step failed: {e!r}"
+
+
+def decode_entry(name, inp, m, world):
+    """The numbers of one decode workload: step and kernel time, GB/s, roofline."""
+    b = m["bench"]
+    hbm_peak, _, peak_kind = _peaks()
+    kvb = b.kv_bytes
+    unique = workloads.kv_read_bytes(inp, unique=True)
+    shared = kvb - unique  # bytes of shared blocks read more than once (prefix sharing)
+    alg = b.alg_bytes_fused - shared
+    achieved = alg / (m["dec_ms"] * 1e-3) / 1e9
+    D = inp.head_dim
+    dec_files = ["paged_kv_gqa_10_gb300/csrc/decode.cu", "paged_kv_gqa_10_gb300/csrc/ptx.cuh"]
+    e = {"workload": DECODE_WORKLOADS[name][1],
+         "ms_per_step": m["ms_graph"],
+         "GB/s": job_value(kvb, world, m["ms_graph"]),
+         "kernel_ms": m["dec_ms"],
+         "roofline": {"bound": "hbm",
+                      "kernel": f"paged_decode_kernel<{D},{inp.cache_dtype}> with the append",
+                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                      "frac": achieved / hbm_peak, "peak_kind": peak_kind,
+                      "alg_bytes_per_launch": alg, "launch_ms": m["dec_ms"],
+                      "traffic": _profile_traffic(f"decode_{name}.json", dec_files)}}
+    if shared:
+        e["unique_kv_bytes_per_step"] = unique
+        e["unique GB/s"] = job_value(unique, world, m["ms_graph"])
+        e["GB/s_note"] = ("GB/s counts every sequence's context (logical bytes, effective "
+                          "with L2 serving the shared blocks); unique GB/s and the roofline "
+                          "count each shared block once")
+    return e
 
 
 def run_ours(args):
     dist, rank, local, world = _dist()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    make, desc = DECODE_WORKLOADS[args.workload]
-    inp = make()
-    m = measure_decode(inp, args, dev, dist, clocks_index=local)
-    b = m["bench"]
-    kv_bytes = b.kv_bytes
-    value = job_value(kv_bytes, world, m["ms_graph"])
-    pref = measure_prefill(args, dev) if (args.workload == "llama3_8b" and not args.no_prefill) \
-        else None
+    names = [args.workload] + ([] if args.only else
+                               [n for n in DECODE_ORDER if n != args.workload])
+    decode = {}
+    head = None
+    for name in names:
+        inp = DECODE_WORKLOADS[name][0]()
+        full = name == args.workload
+        m = measure_decode(inp, args, dev, dist, clocks_index=local if full else None,
+                           full=full)
+        entry = decode_entry(name, inp, m, world)
+        if rank == 0 and not args.no_cpu_baseline:
+            gpu_res = _gpu_step_result(m["bench"])
+            if full:
+                cpu = _cpu_baseline(inp, args.cpu_seconds, gpu_res)
+                entry["parity"] = cpu["parity"]
+            else:
+                entry["parity"] = _oracle_parity(inp, gpu_res)
+        decode[name] = entry
+        if full:
+            head = (inp, m, cpu if rank == 0 and not args.no_cpu_baseline else None)
+        else:
+            del m
+            torch.cuda.empty_cache()
+    inp, m, cpu = head
+    pref = None if args.no_prefill else measure_prefill(args, dev)
+    nxt = None
+    if not args.no_prefill and not args.only:
+        nxt = measure_cached_prefix(args, dev)
+        nxt["sliding_window_decode"] = measure_window_decode(args, dev)
+        nxt["e4m3_prefill"] = measure_e4m3_prefill(args, dev)
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return 0
-    hbm_peak, _, peak_kind = _peaks()
-    achieved = b.alg_bytes_fused / (m["dec_ms"] * 1e-3) / 1e9
-    dec_files = ["paged_kv_gqa_10_gb300/csrc/decode.cu", "paged_kv_gqa_10_gb300/csrc/ptx.cuh"]
-    B, Hq, D = inp.q.shape
+    b = m["bench"]
+    kv_bytes = b.kv_bytes
+    value = job_value(kv_bytes, world, m["ms_graph"])
     dt = "e4m3 KV, bf16 q/out" if inp.cache_dtype == "e4m3" else "bf16"
+    config = decode_config(args.workload, inp)
+    config["parallelism"] = f"replica per GPU x{world}"
+    head_entry = decode[args.workload]
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["ms_graph"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dt,
-        "data": "synthetic (seeded N(0,1) bf16 q/K/V, seeded shuffled block tables)",
-        "config": {"workload": desc, "batch": B, "q_heads": Hq, "kv_heads": inp.num_kv_heads,
-                   "head_dim": D, "block_size": 16, "kv_bytes_per_step": kv_bytes,
-                   "unique_kv_bytes_per_step": workloads.kv_read_bytes(inp, unique=True),
-                   "step": "one launch of paged_attention_decode_append: each sequence's new "
-                           "token written at position L-1 (the bytes kv_cache_write writes) and "
-                           "attention over the whole context; replayed as CUDA graphs of "
-                           f"{b.R} steps (one per block-table set)",
-                   "eager_ms_per_step": m["ms_eager"],
-                   "two_call_ms_per_step": m["ms_two"],
-                   "two_call_value": kv_bytes * world / (m["ms_two"] * 1e-3) / 1e9,
-                   "l2": f"{b.R} rotating block-table sets over disjoint blocks "
-                         f"({b.R * kv_bytes / 1e6:.0f} MB > 129 MB L2)",
-                   "parallelism": f"replica per GPU x{world}"},
-        "roofline": {"bound": "hbm",
-                     "kernel": f"paged_decode_kernel<{D},{inp.cache_dtype}> with the append",
-                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "peak_kind": peak_kind,
-                     "alg_bytes_per_launch": b.alg_bytes_fused, "launch_ms": m["dec_ms"],
-                     "traffic": _profile_traffic("decode_llama3_8b.json", dec_files)
-                     if args.workload == "llama3_8b" else None},
+        "data": DATA, "config": config,
+        "step": {"launch": "one launch of paged_attention_decode_append per step, replayed as "
+                           f"CUDA graphs of {b.R} steps (one per block-table set)",
+                 "eager_ms_per_step": m["ms_eager"],
+                 "two_call_ms_per_step": m["ms_two"],
+                 "two_call_value": kv_bytes * world / (m["ms_two"] * 1e-3) / 1e9},
+        "roofline": head_entry["roofline"],
         "e2e": {"value": kv_bytes * world / (m["e2e_ms"] * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"],
                 "ms_per_step": m["e2e_ms"],
@@ -762,21 +879,14 @@ def run_ours(args):
                          "with one copy"},
         "gpu_launches": args.steps,
         "clocks": m["clocks"],
+        "decode": decode,
     }
     if pref is not None:
         line["prefill"] = pref
-        line["next"] = measure_cached_prefix(args, dev)
-        line["next"]["sliding_window_decode"] = measure_window_decode(args, dev)
-        line["next"]["e4m3_prefill"] = measure_e4m3_prefill(args, dev)
-    if not args.no_cpu_baseline:
-        # one more step on the first block-table set, read back for the oracle to check
-        try:
-            b.decode_append(0)
-            b.check()
-            gpu_res = (b.out.float().cpu().numpy(), b.lse.cpu().numpy())
-        except Exception as e:  # reported in the line, never fatal to it
-            gpu_res = f"GPU step failed: {e!r}"
-        line["cpu_baseline"] = _cpu_baseline(inp, args.cpu_seconds, gpu_res)
+    if nxt is not None:
+        line["next"] = nxt
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -791,7 +901,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--workload", default="llama3_8b", choices=sorted(DECODE_WORKLOADS))
+    ap.add_argument("--workload", default=DECODE_ORDER[0], choices=sorted(DECODE_WORKLOADS),
+                    help="the headline decode workload (timed end to end, with the oracle "
+                         "baseline); the others are measured beside it")
+    ap.add_argument("--only", action="store_true",
+                    help="measure the headline decode workload and the prefill only")
     ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -95,6 +95,22 @@ int pgqa_abi_version(void);
 /* Static, NUL-terminated description of a status code. Never NULL. */
 const char* pgqa_status_string(pgqa_status_t status);
 
+/*
+ * Failure-detection aid (the pages have no counterpart; it exists so that the bounded
+ * waits can be tested without faulting a GPU). Every wait inside the decode kernels
+ * (pgqa_paged_attention_decode and its window, append and noalloc forms) is bounded: the
+ * consumer and merge warps' barrier waits and the producer's wait for free stages give
+ * up after 2 s by default, store PGQA_ETIMEOUT in *dev_status and let the kernel end.
+ * This sets that limit, in nanoseconds, for the decode launches made after it on any
+ * device (0 restores the 2 s default); a very short limit makes those waits run out.
+ * The producer's final wait for its own copies in flight always keeps the 2 s limit, so
+ * no copy can land after a thread block exits. After a call that reported
+ * PGQA_ETIMEOUT the call's outputs are undefined and its workspace must be zero-filled
+ * again before reuse. Host only; a process-wide setting (not synchronised with launches
+ * made concurrently from other host threads).
+ */
+void pgqa_set_decode_wait_limit_ns(uint64_t ns);
+
 /* Bytes of KV cache for `num_layers` layers of `tokens` cached tokens:
  * 2 (K and V) * layers * tokens * kv-heads * head_dim * element size
  * ("LLaMA structure and inference performance", sec. 5, sizes a 4K-context
@@ -215,7 +231,7 @@ pgqa_status_t pgqa_paged_attention_decode_window(
     int max_context_len, void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
 
 /* Size of the library-owned scratch array used by
- * pgqa_paged_attention_decode_noalloc (8 MiB per GPU that loads the library). */
+ * pgqa_paged_attention_decode_noalloc (8 MiB on each GPU where it has been set up). */
 #define PGQA_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
 
 /*
@@ -230,11 +246,17 @@ pgqa_status_t pgqa_paged_attention_decode_window(
  * Arguments are those of pgqa_paged_attention_decode without the workspace; the
  * caller still passes every input and output. The split-K scratch is a static
  * device array of PGQA_NOALLOC_SCRATCH_BYTES owned by the library:
- *  - sizes whose workspace (pgqa_decode_workspace_size) exceeds that limit are
- *    rejected with PGQA_ENOWORKSPACE before anything is launched;
- *  - the first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture;
+ *  - per-device set-up: the first call on a device, with that device current,
+ *    looks up the array's device address (cudaGetSymbolAddress) and loads the
+ *    decode kernels there. Under the CUDA runtime's lazy module loading (the
+ *    default) that is also when the device allocates the array and the kernels'
+ *    code, so make this first call BEFORE filling the device's free memory, and
+ *    before any stream capture. A call with num_seqs == 0 (the other pointers may
+ *    be NULL) does only this set-up and enqueues nothing; later calls on that
+ *    device allocate nothing;
+ *  - arguments are checked on the host first: a call that returns an error has
+ *    enqueued nothing; sizes whose workspace (pgqa_decode_workspace_size) exceeds
+ *    the array are rejected with PGQA_ENOWORKSPACE;
  *  - each call clears the array's merge counters with cudaMemsetAsync on
  *    `stream`, then launches the decode kernel; it never calls cudaMalloc,
  *    cudaFree or any allocating routine;

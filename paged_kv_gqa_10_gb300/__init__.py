@@ -14,7 +14,7 @@ Functions (same names as the C entry points, without the ``pgqa_`` prefix):
   paged_attention_decode_window, paged_attention_decode_noalloc,
   paged_prefill_varlen, paged_prefill_varlen_kv, paged_prefill_varlen_e4m3,
   decode_workspace_size, decode_grid_size, prefill_workspace_size, kv_cache_bytes,
-  status_string, abi_version.
+  set_decode_wait_limit_ns, status_string, abi_version.
 """
 import ctypes
 import os
@@ -26,7 +26,8 @@ __all__ = [
     "paged_attention_decode", "paged_attention_decode_append", "paged_attention_decode_window",
     "paged_attention_decode_noalloc", "paged_prefill_varlen", "paged_prefill_varlen_kv",
     "paged_prefill_varlen_e4m3", "decode_workspace_size", "decode_grid_size",
-    "prefill_workspace_size", "kv_cache_bytes", "status_string", "abi_version",
+    "prefill_workspace_size", "kv_cache_bytes", "set_decode_wait_limit_ns", "status_string",
+    "abi_version",
     "library_path", "lib",
 ]
 
@@ -58,6 +59,7 @@ def _load():
     sig = {
         "pgqa_abi_version": ([], I),
         "pgqa_status_string": ([I], ctypes.c_char_p),
+        "pgqa_set_decode_wait_limit_ns": ([ctypes.c_uint64], None),
         "pgqa_kv_cache_bytes": ([I, I64, I, I, I], I64),
         "pgqa_kv_cache_write": ([P, P, P, I, I, I, P, P, I, I, I, P, P, P, P], I),
         "pgqa_paged_kv_gather": ([P, P, I, P, I, P, I, I, I, I, I, I, P, P, P, P], I),
@@ -115,6 +117,15 @@ def abi_version() -> int:
 
 def status_string(status: int) -> str:
     return _handle().pgqa_status_string(status).decode()
+
+
+def set_decode_wait_limit_ns(ns: int) -> None:
+    """Limit, in nanoseconds, of the decode kernels' bounded waits for the launches that
+    follow (0 restores the 2 s default); a failure-detection testing aid, see
+    pgqa_set_decode_wait_limit_ns in include/pgqa.h."""
+    if int(ns) < 0:
+        raise ValueError("ns must be >= 0")
+    _handle().pgqa_set_decode_wait_limit_ns(int(ns))
 
 
 # ------------------------------------------------------------------ helpers
@@ -305,7 +316,9 @@ def paged_attention_decode_noalloc(out, lse, q, k_cache, v_cache, block_tables, 
                                    dev_status=None, stream=None):
     """paged_attention_decode for callers that cannot allocate device memory: the
     split-K scratch is a fixed 8 MiB array owned by the library (see
-    pgqa_paged_attention_decode_noalloc in include/pgqa.h). Calls that overlap
+    pgqa_paged_attention_decode_noalloc in include/pgqa.h). The first call on a device
+    loads that array and the decode kernels there (make it before filling the device's
+    memory; the C function called with num_seqs = 0 does only that). Calls that overlap
     on the GPU race on that array."""
     _dev(out, "out", torch.bfloat16)
     _dev(lse, "lse", torch.float32)

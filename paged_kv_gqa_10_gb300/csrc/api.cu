@@ -163,6 +163,41 @@ bool smem_attr_ready(const void* kernel, int bytes) {
   return true;
 }
 
+pgqa_status_t decode_validate(const void* out, const void* q, const void* k_cache,
+                              const void* v_cache, const int32_t* block_tables,
+                              int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                              int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
+                              int block_size, float scale, int cache_dtype, const float* k_scale,
+                              const float* v_scale, int max_context_len, const void* key,
+                              const void* value) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 ||
+      block_size <= 0 || max_context_len < 0 || max_blocks_per_seq < 0 || !isfinite(scale))
+    return PGQA_EINVAL;
+  if (num_q_heads % num_kv_heads != 0) return PGQA_EINVAL;
+  if (cache_dtype == PGQA_DTYPE_E4M3) {
+    if (k_scale == nullptr || v_scale == nullptr) return PGQA_EINVAL;
+  } else if (cache_dtype == PGQA_DTYPE_BF16) {
+    if (k_scale != nullptr || v_scale != nullptr) return PGQA_EINVAL;
+  } else {
+    return PGQA_EUNSUPPORTED;
+  }
+  const int group = num_q_heads / num_kv_heads;
+  if (group > 8 || (block_size != 8 && block_size != 16 && block_size != 32))
+    return PGQA_EUNSUPPORTED;
+  if (!(head_dim == 128 || (head_dim == 64 && cache_dtype == PGQA_DTYPE_BF16)))
+    return PGQA_EUNSUPPORTED;
+  if (static_cast<int64_t>(num_blocks) * num_kv_heads * block_size > INT32_MAX)
+    return PGQA_EUNSUPPORTED;
+  if (num_seqs == 0) return PGQA_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PGQA_EINVAL;
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return PGQA_EINVAL;
+  if ((key == nullptr) != (value == nullptr) || !aligned(key, 16) || !aligned(value, 16))
+    return PGQA_EINVAL;
+  return PGQA_OK;
+}
+
+
 }  // namespace pgqa
 
 using pgqa::aligned;
@@ -170,6 +205,8 @@ using pgqa::aligned;
 extern "C" {
 
 int pgqa_abi_version(void) { return PGQA_ABI_VERSION; }
+
+void pgqa_set_decode_wait_limit_ns(uint64_t ns) { pgqa::set_decode_wait_limit_ns(ns); }
 
 const char* pgqa_status_string(pgqa_status_t s) {
   switch (s) {
@@ -265,6 +302,7 @@ size_t pgqa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_head
   return a > b ? a : b;
 }
 
+
 // Shared by the decode entry points (window 0: the whole context; key/value null: no
 // fused append).
 static pgqa_status_t decode_call(void* out, float* lse, const void* q, const void* k_cache,
@@ -276,30 +314,11 @@ static pgqa_status_t decode_call(void* out, float* lse, const void* q, const voi
                                  int max_context_len, void* workspace, size_t workspace_bytes,
                                  int* dev_status, void* stream, const void* key = nullptr,
                                  const void* value = nullptr) {
-  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 ||
-      block_size <= 0 || max_context_len < 0 || max_blocks_per_seq < 0 || !isfinite(scale))
-    return PGQA_EINVAL;
-  if (num_q_heads % num_kv_heads != 0) return PGQA_EINVAL;
-  if (cache_dtype == PGQA_DTYPE_E4M3) {
-    if (k_scale == nullptr || v_scale == nullptr) return PGQA_EINVAL;
-  } else if (cache_dtype == PGQA_DTYPE_BF16) {
-    if (k_scale != nullptr || v_scale != nullptr) return PGQA_EINVAL;
-  } else {
-    return PGQA_EUNSUPPORTED;
-  }
-  const int group = num_q_heads / num_kv_heads;
-  if (group > 8 || (block_size != 8 && block_size != 16 && block_size != 32))
-    return PGQA_EUNSUPPORTED;
-  if (!(head_dim == 128 || (head_dim == 64 && cache_dtype == PGQA_DTYPE_BF16)))
-    return PGQA_EUNSUPPORTED;
-  if (static_cast<int64_t>(num_blocks) * num_kv_heads * block_size > INT32_MAX)
-    return PGQA_EUNSUPPORTED;
-  if (num_seqs == 0) return PGQA_OK;
-  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PGQA_EINVAL;
-  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
-    return PGQA_EINVAL;
-  if ((key == nullptr) != (value == nullptr) || !aligned(key, 16) || !aligned(value, 16))
-    return PGQA_EINVAL;
+  const pgqa_status_t rc = pgqa::decode_validate(
+      out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+      num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, cache_dtype, k_scale,
+      v_scale, max_context_len, key, value);
+  if (rc != PGQA_OK || num_seqs == 0) return rc;
   const int sms = pgqa::num_sms_current_device();
   if (sms <= 0) return PGQA_ECUDA;
   const pgqa::DecodePlan plan =

@@ -53,6 +53,8 @@
 #include <cuda_bf16.h>
 #include <float.h>
 
+#include <atomic>
+
 #include "host.h"
 #include "ptx.cuh"
 
@@ -88,6 +90,9 @@ struct DecodeParams {
   int block_size;    // 8, 16 or 32 tokens per block; the kernel works on 16-token pages
   int window;        // > 0: each context's last `window` keys only
   float scale_log2;  // scale * log2(e)
+  // limit of the bounded waits while the CTA streams (kWaitLimitNs unless a test set a
+  // shorter one); the producer's final wait for its own copies always uses kWaitLimitNs
+  unsigned long long wait_ns;
 };
 
 // Fused append: the step's new token, key L-1 of every sequence, is written into the
@@ -439,7 +444,7 @@ __device__ __forceinline__ void merge_units(const DecodeParams& p, const Epi epi
     if (!cur.next(p, runs)) return;  // w is the range's last unit
     constexpr int kBufs = Cfg<D, kFp8>::kMergeBufs;
     const int mb = cu % kBufs;
-    if (!__all_sync(0xffffffffu, mbar_wait(&unit_done[mb], (cu / kBufs) & 1))) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&unit_done[mb], (cu / kBufs) & 1, p.wait_ns))) {
       if (lane == 0) record_status(p.dev_status, PGQA_ETIMEOUT);
       return;
     }
@@ -677,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
         idle_since = 0;
       } else if (idle_since == 0) {
         idle_since = globaltimer_ns();
-      } else if (globaltimer_ns() - idle_since > kWaitLimitNs) {
+      } else if (globaltimer_ns() - idle_since > p.wait_ns) {
         if (lane == 0) record_status(p.dev_status, PGQA_ETIMEOUT);
         break;
       }
@@ -794,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
       const int i = i_base + j;
       const int li = i / kNW;
       const int s = warp * SPW + li % SPW;
-      if (!mbar_wait(&full[s], (li / SPW) & 1)) {
+      if (!mbar_wait(&full[s], (li / SPW) & 1, p.wait_ns)) {
         alive = false;
         record_status(p.dev_status, PGQA_ETIMEOUT);
         break;
@@ -942,7 +947,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
     constexpr int kBufs = C::kMergeBufs;
     const int mb = cu % kBufs;
     if (cu >= kBufs &&
-        !__all_sync(0xffffffffu, mbar_wait(&merge_free[mb], ((cu / kBufs) - 1) & 1))) {
+        !__all_sync(0xffffffffu, mbar_wait(&merge_free[mb], ((cu / kBufs) - 1) & 1, p.wait_ns))) {
       alive = false;
       if (lane == 0) record_status(p.dev_status, PGQA_ETIMEOUT);
     }
@@ -1031,6 +1036,7 @@ pgqa_status_t launch_variant(const DecodeArgs& a, const DecodePlan& plan) {
   p.window = a.window;
   p.block_size = a.block_size;
   p.scale_log2 = a.scale * kLog2e;
+  p.wait_ns = decode_wait_limit_ns();
   DecodeAppend ap;
   ap.key = static_cast<const uint4*>(a.new_key);
   ap.value = static_cast<const uint4*>(a.new_value);
@@ -1045,6 +1051,19 @@ pgqa_status_t launch_variant(const DecodeArgs& a, const DecodePlan& plan) {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 }  // namespace
+
+namespace {
+std::atomic<unsigned long long> g_decode_wait_ns{0};  // 0: kWaitLimitNs
+}  // namespace
+
+unsigned long long decode_wait_limit_ns() {
+  const unsigned long long v = g_decode_wait_ns.load(std::memory_order_relaxed);
+  return v ? v : kWaitLimitNs;
+}
+
+void set_decode_wait_limit_ns(unsigned long long ns) {
+  g_decode_wait_ns.store(ns, std::memory_order_relaxed);
+}
 
 int decode_ctas_per_sm(int head_dim, int cache_dtype) {
   if (cache_dtype == PGQA_DTYPE_E4M3) return ctas_per_sm<128, true>();
@@ -1063,6 +1082,15 @@ DecodePlan decode_plan(int num_seqs, int num_kv_heads, int head_dim, int cache_d
   plan.o_off = plan.lse_off + align256(slots * sizeof(float));
   plan.bytes = plan.o_off + align256(slots * static_cast<size_t>(head_dim) * sizeof(float));
   return plan;
+}
+
+bool decode_prepare() {
+  return smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<128, false>),
+                         Cfg<128, false>::kSmem) &&
+         smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<64, false>),
+                         Cfg<64, false>::kSmem) &&
+         smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<128, true>),
+                         Cfg<128, true>::kSmem);
 }
 
 pgqa_status_t launch_paged_decode(const DecodeArgs& a, const DecodePlan& plan) {

@@ -101,6 +101,26 @@ DecodePlan decode_plan(int num_seqs, int num_kv_heads, int head_dim, int cache_d
 
 pgqa_status_t launch_paged_decode(const DecodeArgs& a, const DecodePlan& plan);
 
+// Host-side checks of a decode call's arguments, everything but the workspace (the
+// decode entry points return this status before anything is enqueued). key / value:
+// the fused append's new rows, both null without it.
+pgqa_status_t decode_validate(const void* out, const void* q, const void* k_cache,
+                              const void* v_cache, const int32_t* block_tables,
+                              int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                              int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
+                              int block_size, float scale, int cache_dtype, const float* k_scale,
+                              const float* v_scale, int max_context_len, const void* key,
+                              const void* value);
+
+// Limit of the decode kernels' bounded waits while they stream (the default 2 s, or
+// what pgqa_set_decode_wait_limit_ns set); read at each launch.
+unsigned long long decode_wait_limit_ns();
+void set_decode_wait_limit_ns(unsigned long long ns);
+
+// Loads the decode kernels on the current device and sets their shared-memory limits
+// (what a first decode launch would otherwise do). False if the runtime refuses.
+bool decode_prepare();
+
 struct PrefillArgs {
   void* out;
   float* lse;

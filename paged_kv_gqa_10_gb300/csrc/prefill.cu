@@ -40,7 +40,8 @@
 //    requested while the ring is full, so no load waits on a table read. Pages past
 //    the sequence end are loaded from past the end of the cache view, which TMA
 //    fills with zeros.
-//  - warp 9 (MMA, one thread): tcgen05.mma, M = N = 128, f32 accumulators in TMEM:
+//  - warp 9 (MMA; the warp runs the issue loop, one elected lane issues): tcgen05.mma,
+//    M = N = 128, f32 accumulators in TMEM:
 //    S_X = Q_X K^T for X = A, B (both operands in shared memory) and O_X += P_X V with
 //    P_X read from tensor memory (V MN-major in shared memory). Issue order per key
 //    tile j: P_A V_j, S_A(j+1), P_B V_j, S_B(j+1), so the tensor core works on one
@@ -232,6 +233,11 @@ __device__ __forceinline__ void e4m3x16_to_f16(uint4 v, uint4& lo, uint4& hi) {
 // chunk k of row r at chunk k ^ (r & 7) of the row's 128-byte line, 64-column blocks
 // 16 KB apart). Rows at or past `valid` (keys past the sequence end) become zeros.
 // Every code of the half is loaded before any store: the f16 rows overwrite them.
+// Store order: a 16-byte store is served 8 lanes at a time, and at head_dim 128 the 8
+// lanes of one row write chunks 2(c mod 4) and 2(c mod 4) + 1 of column block c / 4.
+// Lanes c and c + 4 would hit the same chunk position (the same four banks) of lines
+// 16 KB apart, so the lanes of the second column block write their high chunk first:
+// each store then covers the 8 distinct positions (2(c mod 4) + c / 4) ^ (r & 7).
 template <int D>
 __device__ __forceinline__ void widen_tile_half(uint8_t* slot, int h, int lane, int valid) {
   constexpr int kChunks = D / 16;             // 16-byte chunks per code row
@@ -250,9 +256,10 @@ __device__ __forceinline__ void widen_tile_half(uint8_t* slot, int h, int lane, 
     uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
     if (r < valid) e4m3x16_to_f16(v[i], lo, hi);
     uint8_t* line = slot + (c >> 2) * 16384 + r * 128;
-    const int k0 = 2 * (c & 3);
-    *reinterpret_cast<uint4*>(line + ((k0 ^ (r & 7)) << 4)) = lo;
-    *reinterpret_cast<uint4*>(line + (((k0 + 1) ^ (r & 7)) << 4)) = hi;
+    const int hi_first = c >> 2;  // 0 or 1 (always 0 at head_dim 64)
+    const int k_first = 2 * (c & 3) + hi_first, k_second = k_first ^ 1;
+    *reinterpret_cast<uint4*>(line + ((k_first ^ (r & 7)) << 4)) = hi_first ? hi : lo;
+    *reinterpret_cast<uint4*>(line + ((k_second ^ (r & 7)) << 4)) = hi_first ? lo : hi;
   }
 }
 
@@ -662,7 +669,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
     if (!ok && lane == 0) record_status(p.dev_status, PGQA_ETIMEOUT);
   } else if (warp == kWarpMma) {
     // ================================================================ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop (waits, descriptors) and one elected lane
+    // issues each tcgen05 instruction.
+    {
       const uint32_t id_s = F8 ? idesc_f16_f32(128, kBlockN, false) : idesc_bf16_f32(128, kBlockN, false);
       const uint32_t id_o = F8 ? idesc_f16_f32(128, D, true) : idesc_bf16_f32(128, D, true);
       const uint32_t q_addr = smem_u32(smem + C::kQ), ring = smem_u32(smem + C::kRing);
@@ -672,38 +681,38 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       // wait for that P_X V to complete first.
       auto issue_s = [&](int X, int ks) {
         if (pv_issued[X] > 0) {
-          if (!(ok = mbar_wait(&o_full[X], (pv_issued[X] - 1) & 1))) return false;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&o_full[X], (pv_issued[X] - 1) & 1)))) return false;
           tc_fence_after();
         }
         const uint32_t qx = q_addr + X * C::kTile, kx = ring + ks * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_f16_ss(tmem + X * 128, smem_desc_sw128(qx + off, 16, 1024),
+          umma_f16_ss_warp(tmem + X * 128, smem_desc_sw128(qx + off, 16, 1024),
                       smem_desc_sw128(kx + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[X]);
+        umma_commit_warp(&s_full[X]);
         return true;
       };
       // O_X (+)= P_X V: P_X from TMEM (8 columns per 16 keys), V in ring stage vs
       auto issue_pv = [&](int X, int vs, bool accumulate) {
-        if (!(ok = mbar_wait(&p_full[X], np[X] & 1))) return false;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&p_full[X], np[X] & 1)))) return false;
         ++np[X];
         tc_fence_after();
         const uint32_t vx = ring + vs * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
-          umma_f16_ts(tmem + 256 + X * 128, tmem + X * 128 + kk * 8,
+          umma_f16_ts_warp(tmem + 256 + X * 128, tmem + X * 128 + kk * 8,
                       smem_desc_sw128(vx + kk * 2048, 16384, 1024), id_o,
                       (accumulate || kk > 0) ? 1u : 0u);
-        umma_commit(&o_full[X]);
+        umma_commit_warp(&o_full[X]);
         ++pv_issued[X];
         return true;
       };
       // waits for ring load gi to land (E4M3: and be widened); returns its stage in st
       auto take = [&](int gi, int& st) {
         st = gi % kStages;
-        if (!(ok = mbar_wait(F8 ? &conv[st] : &full[st], (gi / kStages) & 1))) return false;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(F8 ? &conv[st] : &full[st], (gi / kStages) & 1)))) return false;
         tc_fence_after();
         return true;
       };
@@ -713,16 +722,16 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       int ks, vs;
       // the first item's S_A(0), S_B(0)
       auto start_item = [&](Item& nw) {
-        if (!(ok = mbar_wait(q_full, it & 1))) return false;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(q_full, it & 1)))) return false;
         nw = read_slot(slots + (it & 1) * 8);
-        if (F8 && nw.ticket >= 0 && !(ok = mbar_wait(q_conv, it & 1))) return false;
+        if (F8 && nw.ticket >= 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(q_conv, it & 1)))) return false;
         ++it;
         tc_fence_after();
         return nw.ticket >= 0;
       };
       if (start_item(w) && take(g++, ks) && issue_s(0, ks) && (!w.active_b || issue_s(1, ks))) {
-        umma_commit(&empty[ks]);
-        if (w.nkt() == 1) umma_commit(q_empty);
+        umma_commit_warp(&empty[ks]);
+        if (w.nkt() == 1) umma_commit_warp(q_empty);
         for (;;) {
           const int nkt = w.nkt();  // both tiles visit key tiles 0..t
           Item nx;
@@ -742,20 +751,20 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
             if (w.active_b && !issue_pv(1, vs, j > 0)) break;
             if (more) {
               if (w.active_b && !issue_s(1, ks)) break;
-              umma_commit(&empty[ks]);
-              if (j + 1 == nkt - 1) umma_commit(q_empty);
+              umma_commit_warp(&empty[ks]);
+              if (j + 1 == nkt - 1) umma_commit_warp(q_empty);
             } else if (nx_valid) {
               if (nx.active_b && !issue_s(1, ks)) break;
-              umma_commit(&empty[ks]);
-              if (nx.nkt() == 1) umma_commit(q_empty);
+              umma_commit_warp(&empty[ks]);
+              if (nx.nkt() == 1) umma_commit_warp(q_empty);
             }
-            umma_commit(&empty[vs]);
+            umma_commit_warp(&empty[vs]);
           }
           if (!ok || !nx_valid) break;
           w = nx;
         }
       }
-      if (!ok) record_status(p.dev_status, PGQA_ETIMEOUT);
+      if (!ok && lane == 0) record_status(p.dev_status, PGQA_ETIMEOUT);
     }
   } else if (warp < kWarpTma) {
     // ================================================================ softmax rows

@@ -187,3 +187,10 @@ def test_every_entry_point_has_a_python_binding():
         short = name[len("pgqa_"):]
         assert callable(getattr(pgqa, short, None)), short
         assert short in pgqa.__all__, short
+
+
+def test_wait_limit_setter_rejects_negative_and_restores_default():
+    with pytest.raises(ValueError):
+        pgqa.set_decode_wait_limit_ns(-1)
+    pgqa.set_decode_wait_limit_ns(5000)
+    pgqa.set_decode_wait_limit_ns(0)   # back to the default; host only, no device touched
