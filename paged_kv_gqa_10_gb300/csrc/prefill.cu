@@ -886,8 +886,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
               for (int q = 0; q < 8; ++q) row[q] = make_uint4(0, 0, 0, 0);
             }
           }
+          fence_proxy_async_smem();  // the MMAs read what these generic stores wrote
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&p_full[X]);
         ++tcnt;
@@ -899,24 +899,37 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(
       const bool store = qpos < w.Lq;
       const size_t orow =
           static_cast<size_t>(w.start + (store ? qpos : 0)) * p.num_q_heads + hq_row;
-      uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D);
+      if (store && p.lse) p.lse[orow] = w.bad ? -INFINITY : (m_ref + log2f(l)) * kLn2;
+      uint8_t* dst = reinterpret_cast<uint8_t*>(p.out + orow * D);
       const float inv = (F8 ? __ldg(v_scale + kvh) : 1.f) / l;
+      // the row's D values in one TMEM load (D = 128: 128 columns; D = 64: 64), then
+      // 32-byte stores when out is 32-byte aligned (a row is D * 2 bytes), else 16-byte
+      uint32_t o[D];
+      if constexpr (D == 128) {
+        tmem_ld128(lane_base + o_col, o);  // every lane: warp-collective
+      } else {
+        tmem_ld64(lane_base + o_col, o);
+      }
+      const uint32_t keep = w.bad ? 0u : 0xffffffffu;  // a bad item's rows are written as zeros
+      if ((reinterpret_cast<uintptr_t>(p.out) & 31) == 0) {
 #pragma unroll
-      for (int half = 0; half < D / 64; ++half) {
-        uint32_t o[64];
-        tmem_ld64(lane_base + o_col + half * 64, o);  // every lane: warp-collective
+        for (int q = 0; q < D / 16; ++q) {  // 16 values = 32 bytes per store
+          const float* f = reinterpret_cast<const float*>(o) + q * 16;
+          uint32_t v[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (!w.bad) {
-            const float* f = reinterpret_cast<const float*>(o) + q * 8;
-            v = make_uint4(pack_bf16(f[0] * inv, f[1] * inv), pack_bf16(f[2] * inv, f[3] * inv),
-                           pack_bf16(f[4] * inv, f[5] * inv), pack_bf16(f[6] * inv, f[7] * inv));
-          }
-          if (store) dst[half * 8 + q] = v;
+          for (int u = 0; u < 8; ++u) v[u] = pack_bf16(f[2 * u] * inv, f[2 * u + 1] * inv) & keep;
+          if (store) st_global_v8(dst + q * 32, v);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < D / 8; ++q) {  // 8 values = 16 bytes per store
+          const float* f = reinterpret_cast<const float*>(o) + q * 8;
+          const uint4 v = make_uint4(
+              pack_bf16(f[0] * inv, f[1] * inv) & keep, pack_bf16(f[2] * inv, f[3] * inv) & keep,
+              pack_bf16(f[4] * inv, f[5] * inv) & keep, pack_bf16(f[6] * inv, f[7] * inv) & keep);
+          if (store) reinterpret_cast<uint4*>(dst)[q] = v;
         }
       }
-      if (store && p.lse) p.lse[orow] = w.bad ? -INFINITY : (m_ref + log2f(l)) * kLn2;
       tc_fence_before();
     }
     if (!ok && lane == 0) record_status(p.dev_status, PGQA_ETIMEOUT);
