@@ -590,7 +590,7 @@ def measure_prefill(args, dev):
     }
 
 
-def measure_cached_prefix(args, dev):
+def measure_cached_prefix(args, dev, names=("chunked_prefill", "speculative_verify")):
     """The rows past prefill and decode: prefill over a cached prefix (chunked prefill)
     and speculative verification (5 tokens per sequence), each through
     pgqa_paged_prefill_varlen_kv. The K/V are written once into the cache, which is then
@@ -600,9 +600,10 @@ def measure_cached_prefix(args, dev):
     import paged_kv_gqa_10_gb300 as pgqa
     hbm, bf16_peak, kind = _peaks()
     res = {}
-    for name, make in (("chunked_prefill", workloads.chunked_prefill),
-                       ("speculative_verify", workloads.speculative_verify)):
-        inp = make()
+    makers = {"chunked_prefill": workloads.chunked_prefill,
+              "speculative_verify": workloads.speculative_verify}
+    for name in names:
+        inp = makers[name]()
         kc, vc = inp.k_cache.to(dev), inp.v_cache.to(dev)
         q, bt = inp.q.to(dev), inp.block_tables.to(dev)
         cu, lk = inp.cu_seqlens_q.to(dev), inp.seq_lens_k.to(dev)
@@ -893,6 +894,33 @@ def run_ours(args):
     return 0
 
 
+ROWS = (["decode:" + n for n in DECODE_ORDER] +
+        ["prefill", "chunked_prefill", "speculative_verify", "sliding_window_decode",
+         "e4m3_prefill"])
+
+
+def run_row(args):
+    """One row of the bench alone, printed as one JSON line: a profiling aid (an ncu
+    capture of one row's kernel runs only that row's launches)."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    r = args.row
+    if r.startswith("decode:"):
+        name = r.split(":", 1)[1]
+        inp = DECODE_WORKLOADS[name][0]()
+        res = decode_entry(name, inp, measure_decode(inp, args, dev, full=False), 1)
+    elif r == "prefill":
+        res = measure_prefill(args, dev)
+    elif r in ("chunked_prefill", "speculative_verify"):
+        res = measure_cached_prefix(args, dev, names=(r,))[r]
+    elif r == "sliding_window_decode":
+        res = measure_window_decode(args, dev)
+    else:
+        res = measure_e4m3_prefill(args, dev)
+    print(json.dumps({"row": r, **res}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -907,11 +935,15 @@ def main():
     ap.add_argument("--only", action="store_true",
                     help="measure the headline decode workload and the prefill only")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--row", choices=ROWS,
+                    help="run one row of the bench alone and print its numbers (profiling aid)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.row:
+        return run_row(args)
     return run_ours(args)
 
 
