@@ -617,11 +617,23 @@ def measure_cached_prefix(args, dev, names=("chunked_prefill", "speculative_veri
                             dev_status=status)
         caches = [(kc, vc)] + [(kc.clone(), vc.clone()) for _ in range(ROTATIONS)]
         R = len(caches)
+        if name == "speculative_verify":
+            # every sequence verifies the same number of draft tokens: the multi-token
+            # decode, whose (sequence, kv-head) query rows share each page read
+            B, nq = inp.num_seqs, inp.max_seqlen_q
+            q4, out4, lse4 = q.view(B, nq, Hq, D), out.view(B, nq, Hq, D), lse.view(B, nq, Hq)
+            ws = torch.zeros(pgqa.decode_multi_workspace_size(B, nq, Hq, inp.key.shape[1], D),
+                             dtype=torch.uint8, device=dev)
 
-        def call(r):
-            pgqa.paged_prefill_varlen_kv(out, lse, q, caches[r][0], caches[r][1], bt, cu, lk,
-                                         inp.max_seqlen_q, inp.max_seqlen_k, inp.scale,
-                                         workspace=ws, dev_status=status)
+            def call(r):
+                pgqa.paged_attention_decode_multi(out4, lse4, q4, caches[r][0], caches[r][1], bt,
+                                                  lk, inp.scale, inp.max_seqlen_k,
+                                                  workspace=ws, dev_status=status)
+        else:
+            def call(r):
+                pgqa.paged_prefill_varlen_kv(out, lse, q, caches[r][0], caches[r][1], bt, cu, lk,
+                                             inp.max_seqlen_q, inp.max_seqlen_k, inp.scale,
+                                             workspace=ws, dev_status=status)
 
         for i in range(args.warmup):
             call(i % R)
@@ -648,9 +660,11 @@ def measure_cached_prefix(args, dev, names=("chunked_prefill", "speculative_veri
         kvb = workloads.chunked_kv_bytes(inp)
         tflops = flops / (ms * 1e-3) / 1e12
         gbs = kvb / (ms * 1e-3) / 1e9
+        fn = ("pgqa_paged_attention_decode_multi" if name == "speculative_verify"
+              else "pgqa_paged_prefill_varlen_kv")
         entry = {"workload": inp.name, "ms": ms, "flops": flops, "TFLOP/s": tflops,
                  "kv_bytes": kvb, "KV GB/s": gbs, "launches_timed": n * reps,
-                 "call": "pgqa_paged_prefill_varlen_kv, a CUDA graph of back-to-back launches "
+                 "call": f"{fn}, a CUDA graph of back-to-back launches "
                          f"cycling over {R} copies of the cache at different addresses "
                          f"({R} x {kvb / 1e6:.0f} MB of K/V > 129 MB L2)"}
         if name == "chunked_prefill":

@@ -298,6 +298,46 @@ pgqa_status_t pgqa_paged_attention_decode_append(
     const float* v_scale, int max_context_len, void* workspace, size_t workspace_bytes,
     int* dev_status, void* stream);
 
+/* Most new tokens per sequence pgqa_paged_attention_decode_multi takes. */
+#define PGQA_MAX_DECODE_TOKENS 8
+
+/* Workspace bytes pgqa_paged_attention_decode_multi needs on the current device for
+ * these sizes (any cache dtype and block size): as for pgqa_decode_workspace_size, with
+ * partial-result slots for the q_len x group query rows of a (sequence, kv-head); or the
+ * prefill workspace when those rows are more than 24 (see below). 0 on a bad argument. */
+size_t pgqa_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_heads,
+                                        int num_kv_heads, int head_dim);
+
+/*
+ * Multi-token paged decode: q_len new tokens per sequence attend to the cached context,
+ * each causally -- speculative verification of draft tokens (the rkmt.cn article's
+ * speculative decoding, sec. 4.2, drafts several tokens per step) as the varlen call
+ * with per-sequence query and key lengths of sec. 2.4, every chunk q_len long. The
+ * drafts' K/V must already be in the cache (pgqa_kv_cache_write): context_lens[b]
+ * counts them, and token t of sequence b attends keys 0 .. context_lens[b] - q_len + t
+ * (bottom-right causal alignment), read through its block table.
+ *
+ *   out           [num_seqs][q_len][num_q_heads][head_dim] bf16, written.
+ *   lse           [num_seqs][q_len][num_q_heads] fp32, written; may be NULL.
+ *   q             [num_seqs][q_len][num_q_heads][head_dim] bf16, read.
+ *   q_len         1 .. PGQA_MAX_DECODE_TOKENS (PGQA_EINVAL below, PGQA_EUNSUPPORTED above).
+ *   context_lens  [num_seqs] int32, read: 0 (nothing to attend: out = 0, lse = -inf) or
+ *                 at least q_len (a shorter context is a device error, PGQA_EINVAL).
+ *   workspace     at least pgqa_decode_multi_workspace_size() bytes, 256-byte aligned,
+ *                 ZERO-FILLED before its first use; every call that completes leaves
+ *                 it ready for the next call.
+ * Every other argument and the error behaviour are as for pgqa_paged_attention_decode.
+ * The q_len x (num_q_heads / num_kv_heads) query rows of a (sequence, kv-head) share
+ * every page read when they are at most 24 (the decode kernel); above that the prefill
+ * kernel runs the call (block_size 16 only, else PGQA_EUNSUPPORTED; scale > 0).
+ */
+pgqa_status_t pgqa_paged_attention_decode_multi(
+    void* out, float* lse, const void* q, int q_len, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int num_blocks, int block_size,
+    float scale, int cache_dtype, const float* k_scale, const float* v_scale, int max_context_len,
+    void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
+
 /* Workspace bytes pgqa_paged_prefill_varlen needs (33024: the ticket counters the
  * CTAs take work items with, and the longest-first item tables each call rebuilds). */
 size_t pgqa_prefill_workspace_size(int num_seqs, int num_q_heads, int max_seqlen);

@@ -12,8 +12,10 @@ Functions (same names as the C entry points, without the ``pgqa_`` prefix):
   kv_cache_write, paged_kv_gather,
   paged_attention_decode, paged_attention_decode_append,
   paged_attention_decode_window, paged_attention_decode_noalloc,
+  paged_attention_decode_multi,
   paged_prefill_varlen, paged_prefill_varlen_kv, paged_prefill_varlen_e4m3,
-  decode_workspace_size, decode_grid_size, prefill_workspace_size, kv_cache_bytes,
+  decode_workspace_size, decode_multi_workspace_size, decode_grid_size,
+  prefill_workspace_size, kv_cache_bytes,
   set_decode_wait_limit_ns, status_string, abi_version.
 """
 import ctypes
@@ -24,8 +26,10 @@ import torch
 __all__ = [
     "PgqaError", "BF16", "E4M3", "kv_cache_write", "paged_kv_gather",
     "paged_attention_decode", "paged_attention_decode_append", "paged_attention_decode_window",
-    "paged_attention_decode_noalloc", "paged_prefill_varlen", "paged_prefill_varlen_kv",
-    "paged_prefill_varlen_e4m3", "decode_workspace_size", "decode_grid_size",
+    "paged_attention_decode_noalloc", "paged_attention_decode_multi", "paged_prefill_varlen",
+    "paged_prefill_varlen_kv",
+    "paged_prefill_varlen_e4m3", "decode_workspace_size", "decode_multi_workspace_size",
+    "decode_grid_size",
     "prefill_workspace_size", "kv_cache_bytes", "set_decode_wait_limit_ns", "status_string",
     "abi_version",
     "library_path", "lib",
@@ -35,6 +39,7 @@ BF16 = 0
 E4M3 = 1
 ABI_VERSION = 1
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
+MAX_DECODE_TOKENS = 8
 
 OK, EINVAL, EUNSUPPORTED, ENOWORKSPACE, ECUDA, EBADINDEX, ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
 
@@ -73,6 +78,9 @@ def _load():
                                                 I, F, I, P, P, I, P, SZ, P, P], I),
         "pgqa_paged_attention_decode_noalloc": ([P, P, P, P, P, P, I, P, I, I, I, I, I, I, F,
                                                  I, P, P, I, P, P], I),
+        "pgqa_decode_multi_workspace_size": ([I, I, I, I, I], SZ),
+        "pgqa_paged_attention_decode_multi": ([P, P, P, I, P, P, P, I, P, I, I, I, I, I, I, F,
+                                               I, P, P, I, P, SZ, P, P], I),
         "pgqa_prefill_workspace_size": ([I, I, I], SZ),
         "pgqa_paged_prefill_varlen": ([P, P, P, I, P, P, P, I, P, I, I, I, I, I, I, I, F, P,
                                        SZ, P, P], I),
@@ -182,6 +190,11 @@ def decode_grid_size(num_sms, head_dim=128, cache_dtype=BF16):
 def decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len) -> int:
     return _handle().pgqa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                                 max_context_len)
+
+
+def decode_multi_workspace_size(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim) -> int:
+    return int(_handle().pgqa_decode_multi_workspace_size(num_seqs, q_len, num_q_heads,
+                                                          num_kv_heads, head_dim))
 
 
 def prefill_workspace_size(num_seqs, num_q_heads, max_seqlen) -> int:
@@ -338,6 +351,34 @@ def paged_attention_decode_noalloc(out, lse, q, k_cache, v_cache, block_tables, 
         _cache_dtype(k_cache), _ptr(k_scale), _ptr(v_scale), int(max_context_len),
         _ptr(dev_status), _stream(stream))
     _check(rc, "paged_attention_decode_noalloc")
+
+
+def paged_attention_decode_multi(out, lse, q, k_cache, v_cache, block_tables, context_lens,
+                                 scale, max_context_len, k_scale=None, v_scale=None,
+                                 workspace=None, dev_status=None, stream=None):
+    """Multi-token decode (speculative verification): q and out [B, q_len, Hq, D] bf16,
+    lse [B, q_len, Hq] fp32 (or None); token t of sequence b attends keys
+    0 .. context_lens[b] - q_len + t."""
+    _dev(out, "out", torch.bfloat16)
+    _dev(lse, "lse", torch.float32)
+    _dev(q, "q", torch.bfloat16)
+    _dev(k_cache, "k_cache")
+    _dev(v_cache, "v_cache")
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(context_lens, "context_lens", torch.int32)
+    _dev(k_scale, "k_scale", torch.float32)
+    _dev(v_scale, "v_scale", torch.float32)
+    _dev(workspace, "workspace")
+    _dev(dev_status, "dev_status", torch.int32)
+    B, T, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = _handle().pgqa_paged_attention_decode_multi(
+        _ptr(out), _ptr(lse), _ptr(q), T, _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, NB, bs, float(scale),
+        _cache_dtype(k_cache), _ptr(k_scale), _ptr(v_scale), int(max_context_len),
+        _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
+    _check(rc, "paged_attention_decode_multi")
 
 
 def paged_prefill_varlen(out, lse, q, k_cache, v_cache, block_tables, cu_seqlens, max_seqlen,

@@ -346,6 +346,7 @@ static pgqa_status_t decode_call(void* out, float* lse, const void* q, const voi
   a.v_scale = v_scale;
   a.max_context_len = max_context_len;
   a.window = window;
+  a.q_len = 1;
   a.new_key = key;
   a.new_value = value;
   a.workspace = workspace;
@@ -396,6 +397,110 @@ pgqa_status_t pgqa_paged_attention_decode_append(
                      context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks,
                      block_size, scale, 0, cache_dtype, k_scale, v_scale, max_context_len,
                      workspace, workspace_bytes, dev_status, stream, key, value);
+}
+
+size_t pgqa_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_heads,
+                                        int num_kv_heads, int head_dim) {
+  if (num_seqs <= 0 || q_len <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      num_q_heads % num_kv_heads != 0)
+    return 0;
+  const int nt = pgqa::decode_row_tiles(q_len, num_q_heads / num_kv_heads);
+  if (nt == 0) return pgqa::kPrefillWorkspaceBytes;  // the prefill kernel runs these
+  const int sms = pgqa::num_sms_current_device();
+  const size_t a =
+      pgqa::decode_plan(num_seqs, num_kv_heads, head_dim, PGQA_DTYPE_BF16, sms, nt).bytes;
+  const size_t b =
+      pgqa::decode_plan(num_seqs, num_kv_heads, head_dim, PGQA_DTYPE_E4M3, sms, nt).bytes;
+  return a > b ? a : b;
+}
+
+pgqa_status_t pgqa_paged_attention_decode_multi(
+    void* out, float* lse, const void* q, int q_len, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int num_blocks, int block_size,
+    float scale, int cache_dtype, const float* k_scale, const float* v_scale, int max_context_len,
+    void* workspace, size_t workspace_bytes, int* dev_status, void* stream) {
+  if (q_len < 1 || q_len > PGQA_MAX_DECODE_TOKENS) return q_len < 1 ? PGQA_EINVAL
+                                                                      : PGQA_EUNSUPPORTED;
+  const pgqa_status_t rc = pgqa::decode_validate(
+      out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+      num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, cache_dtype, k_scale,
+      v_scale, max_context_len, nullptr, nullptr);
+  if (rc != PGQA_OK || num_seqs == 0) return rc;
+  const int nt = pgqa::decode_row_tiles(q_len, num_q_heads / num_kv_heads);
+  if (nt == 0) {
+    // more query rows per (sequence, kv-head) than the decode kernel holds: the
+    // prefill kernel, in its grouped-rows layout, with q_len new tokens per sequence
+    if (block_size != 16) return PGQA_EUNSUPPORTED;
+    if (!(scale > 0.f)) return PGQA_EINVAL;
+    if (workspace == nullptr || workspace_bytes < pgqa::kPrefillWorkspaceBytes)
+      return PGQA_ENOWORKSPACE;
+    if (!aligned(workspace, 16)) return PGQA_EINVAL;
+    if (num_seqs > pgqa::prefill_max_seqs() || max_context_len > (1 << 26))
+      return PGQA_EUNSUPPORTED;
+    pgqa::PrefillArgs a;
+    a.out = out;
+    a.lse = lse;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.cu_seqlens = nullptr;  // q_len tokens per sequence, in order
+    a.seq_lens_k = context_lens;
+    a.max_seqlen_k = max_context_len;
+    a.workspace = workspace;
+    a.num_tokens = num_seqs * q_len;
+    a.num_seqs = num_seqs;
+    a.max_seqlen = q_len;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.num_blocks = num_blocks;
+    a.block_size = block_size;
+    a.scale = scale;
+    a.cache_dtype = cache_dtype;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.dev_status = dev_status;
+    a.stream = static_cast<cudaStream_t>(stream);
+    return pgqa::launch_paged_prefill(a);
+  }
+  const int sms = pgqa::num_sms_current_device();
+  if (sms <= 0) return PGQA_ECUDA;
+  const pgqa::DecodePlan plan =
+      pgqa::decode_plan(num_seqs, num_kv_heads, head_dim, cache_dtype, sms, nt);
+  if (workspace == nullptr || workspace_bytes < plan.bytes) return PGQA_ENOWORKSPACE;
+  if (!aligned(workspace, 256)) return PGQA_EINVAL;
+  pgqa::DecodeArgs a;
+  a.out = out;
+  a.lse = lse;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.context_lens = context_lens;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.num_blocks = num_blocks;
+  a.block_size = block_size;
+  a.scale = scale;
+  a.cache_dtype = cache_dtype;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.max_context_len = max_context_len;
+  a.window = 0;
+  a.q_len = q_len;
+  a.new_key = nullptr;
+  a.new_value = nullptr;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.dev_status = dev_status;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return pgqa::launch_paged_decode(a, plan);
 }
 
 size_t pgqa_prefill_workspace_size(int num_seqs, int num_q_heads, int max_seqlen) {

@@ -85,6 +85,9 @@ struct DecodeParams {
   int* dev_status;
   int max_blocks_per_seq;
   int num_seqs, num_q_heads, num_kv_heads, group;
+  int q_len;  // new tokens per sequence: 1 (decode), or the tokens a multi-token decode
+              // verifies (q is [num_seqs][q_len][num_q_heads][D], token t sees keys
+              // 0 .. L - q_len + t)
   int num_blocks;
   int max_context_len;
   int block_size;    // 8, 16 or 32 tokens per block; the kernel works on 16-token pages
@@ -106,24 +109,31 @@ struct DecodeAppend {
   uint8_t* v_cache;
 };
 
-template <int D, bool kFp8>
+template <int D, bool kFp8, int NT = 1>
 struct Cfg {
+  // query rows of a unit, in 8-row n-tiles: the group's G <= 8 heads (NT = 1), or
+  // q_len tokens x G heads for multi-token decode (NT = 3: up to 24 rows)
+  static constexpr int kRows = 8 * NT;
   static constexpr int kElem = kFp8 ? 1 : 2;
   static constexpr int kRowBytes = D * kElem;      // one token row of one head
   static constexpr int kSub = kRowBytes / 128;     // 128-byte TMA boxes per row
   static constexpr int kPageBytes = 16 * kRowBytes;
   static constexpr int kStageBytes = 2 * kPageBytes;  // K page + V page
   // about 16 KB of pages in flight per consumer warp (E4M3: 20 KB, with one merge
-  // buffer instead of two paying for the fifth stage)
-  static constexpr int kStagesPerWarp = kStageBytes >= 8192 ? 2 : kFp8 ? 5 : 16384 / kStageBytes;
-  static constexpr int kMergeBufs = kFp8 ? 1 : 2;  // unit states in flight to the merge warp
+  // buffer instead of two paying for the fifth stage); multi-token decode runs one CTA
+  // per SM and gives each warp 32-40 KB
+  static constexpr int kStagesPerWarp =
+      NT > 1 ? (kStageBytes >= 8192 ? 5 : 8)
+             : (kStageBytes >= 8192 ? 2 : kFp8 ? 5 : 16384 / kStageBytes);
+  static constexpr int kMergeBufs = (kFp8 || NT > 1) ? 1 : 2;  // unit states in flight to
+                                                                // the merge warp
   static constexpr int kStages = kNW * kStagesPerWarp;
   static constexpr int kNkc = D / 16;              // 16-wide chunks of head_dim
   static constexpr int kRing = kStages * kStageBytes;
-  static constexpr int kMerge = kNW * 8 * D * 4;   // per-warp O of one unit
-  static constexpr int kOffMerge = kRing;          // [2] by unit parity
-  static constexpr int kOffMl = kOffMerge + kMergeBufs * kMerge;      // [bufs][kNW][8][2] float
-  static constexpr int kOffBar = kOffMl + kMergeBufs * kNW * 8 * 2 * 4;  // full[S], empty[S],
+  static constexpr int kMerge = kNW * kRows * D * 4;  // per-warp O of one unit
+  static constexpr int kOffMerge = kRing;             // [bufs] by unit parity
+  static constexpr int kOffMl = kOffMerge + kMergeBufs * kMerge;  // [bufs][kNW][rows][2] float
+  static constexpr int kOffBar = kOffMl + kMergeBufs * kNW * kRows * 2 * 4;  // full[S], empty[S],
                                                                       // unit_done[2], merge_free[2]
   static constexpr int kOffMeta = kOffBar + (2 * kStages + 4) * 8;    // [S] int
   static constexpr int kOffY = kOffMeta + kStages * 4;                // [kYRing] int
@@ -135,9 +145,10 @@ struct Cfg {
 };
 
 // CTAs of one decode kernel resident per SM (the grid is this times the SM count).
-template <int D, bool kFp8>
+template <int D, bool kFp8, int NT = 1>
 constexpr int ctas_per_sm() {
-  return (227 * 1024) / (Cfg<D, kFp8>::kSmem + 1024) >= 2 ? 2 : 1;
+  static_assert(Cfg<D, kFp8, NT>::kSmem + 1024 <= 227 * 1024, "shared memory");
+  return (227 * 1024) / (Cfg<D, kFp8, NT>::kSmem + 1024) >= 2 ? 2 : 1;
 }
 
 // First key attended in a context of L keys: L - window with a sliding window (the
@@ -151,7 +162,7 @@ __device__ __forceinline__ int first_key(const DecodeParams& p, int L) {
 __device__ __forceinline__ int pages_of(const DecodeParams& p, int b, bool* valid = nullptr) {
   const int L = __ldg(p.context_lens + b);
   const int n = (L + 15) >> 4;
-  const bool ok = L >= 0 && L <= p.max_context_len &&
+  const bool ok = L >= 0 && L <= p.max_context_len && (L == 0 || L >= p.q_len) &&
                   (L + p.block_size - 1) / p.block_size <= p.max_blocks_per_seq;
   if (valid) *valid = ok;
   return ok && L > 0 ? n - (first_key(p, L) >> 4) : 0;
@@ -290,41 +301,47 @@ struct Epi {
   float* part_lse;
   float* part_o;
   const float* v_scale;
-  int num_q_heads, group;
+  int num_q_heads, group, q_len;
+  // output row of query row i = t * group + g of unit (b, h): token t, head h * group + g
+  __device__ __forceinline__ size_t out_row(int b, int h, int i) const {
+    const int t = i / group, g = i - t * group;
+    return (static_cast<size_t>(b) * q_len + t) * num_q_heads + h * group + g;
+  }
 };
 
 // Unit epilogue, run by nt threads (t = this thread's index among them).
 // combine_unit: the consumer warps' states of unit (b, h) from the merge buffer
 // (M = max m_w, l = sum l_w 2^(m_w - M), O likewise) -> the output, or, for a unit cut
 // by range boundaries (nseg > 1), this CTA's partial (slot 0 or 1).
-template <int D, bool kFp8>
+template <int D, bool kFp8, int NT>
 __device__ __noinline__ void combine_unit(const Epi e, int b, int h, int nseg, int slot,
                                           const float* wob, const float* wmlb, int t, int nt) {
-  const int G = e.group;
+  constexpr int kRows = Cfg<D, kFp8, NT>::kRows;
+  const int R = e.group * e.q_len;  // the unit's query rows (<= kRows)
   constexpr int kChunks = D / 8;  // 8 consecutive d per work item
   const float vsc = kFp8 ? __ldg(e.v_scale + h) : 1.f;
-  for (int it = t; it < G * kChunks; it += nt) {
-    const int g = it / kChunks, cc = it % kChunks;
+  for (int it = t; it < R * kChunks; it += nt) {
+    const int g = it / kChunks, cc = it % kChunks;  // g: the query row
     float M = -INFINITY;
     bool poisoned = false;
 #pragma unroll
     for (int ww = 0; ww < kNW; ++ww) {
-      M = fmaxf(M, wmlb[(ww * 8 + g) * 2]);
-      poisoned |= isnan(wmlb[(ww * 8 + g) * 2 + 1]);
+      M = fmaxf(M, wmlb[(ww * kRows + g) * 2]);
+      poisoned |= isnan(wmlb[(ww * kRows + g) * 2 + 1]);
     }
     float lsum = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ww = 0; ww < kNW; ++ww) {
-      const float mw = wmlb[(ww * 8 + g) * 2];
+      const float mw = wmlb[(ww * kRows + g) * 2];
       const float wt = mw == -INFINITY ? 0.f : ex2(mw - M);
-      lsum += wmlb[(ww * 8 + g) * 2 + 1] * wt;
-      const float4* src = reinterpret_cast<const float4*>(wob + (ww * 8 + g) * D + cc * 8);
+      lsum += wmlb[(ww * kRows + g) * 2 + 1] * wt;
+      const float4* src = reinterpret_cast<const float4*>(wob + (ww * kRows + g) * D + cc * 8);
       const float4 x = src[0], y = src[1];
       o[0] += x.x * wt; o[1] += x.y * wt; o[2] += x.z * wt; o[3] += x.w * wt;
       o[4] += y.x * wt; o[5] += y.y * wt; o[6] += y.z * wt; o[7] += y.w * wt;
     }
     const float inv = 1.f / lsum;
-    const size_t row = static_cast<size_t>(b) * e.num_q_heads + h * G + g;
+    const size_t row = e.out_row(b, h, g);
     if (nseg == 1) {
       uint4 pk = make_uint4(0, 0, 0, 0);
       if (!poisoned) {
@@ -335,7 +352,7 @@ __device__ __noinline__ void combine_unit(const Epi e, int b, int h, int nseg, i
       reinterpret_cast<uint4*>(e.out + row * D)[cc] = pk;
       if (cc == 0 && e.lse) e.lse[row] = poisoned ? -INFINITY : (M + log2f(lsum)) * kLn2;
     } else {
-      const size_t ps = (static_cast<size_t>(blockIdx.x) * 2 + slot) * 8 + g;
+      const size_t ps = (static_cast<size_t>(blockIdx.x) * 2 + slot) * kRows + g;
       float4* dst = reinterpret_cast<float4*>(e.part_o + ps * D + cc * 8);
       dst[0] = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
       dst[1] = make_float4(o[4] * inv, o[5] * inv, o[6] * inv, o[7] * inv);
@@ -349,16 +366,17 @@ __device__ __noinline__ void combine_unit(const Epi e, int b, int h, int nseg, i
 // starts at or before its range (its first unit), else in slot 1 (its last). Partials
 // are taken four at a time: a group's loads are all issued before any is used, then
 // merged into a running (M, l, O).
-template <int D, bool kFp8>
+template <int D, bool kFp8, int NT>
 __device__ __noinline__ void merge_partials(const Epi e, int b, int h, long long S, int P,
                                             long long chunk, int t, int nt) {
-  const int G = e.group;
+  constexpr int kRows = Cfg<D, kFp8, NT>::kRows;
+  const int R = e.group * e.q_len;
   constexpr int kChunks = D / 8;
   constexpr int kGroup = 4;
   const float vsc = kFp8 ? __ldg(e.v_scale + h) : 1.f;
   const long long c_first = S / chunk, c_last = (S + P - 1) / chunk;
-  for (int it = t; it < G * kChunks; it += nt) {
-    const int g = it / kChunks, cc = it % kChunks;
+  for (int it = t; it < R * kChunks; it += nt) {
+    const int g = it / kChunks, cc = it % kChunks;  // g: the query row
     float M = -INFINITY, lsum = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     bool any_bad = false;
     for (long long base = c_first; base <= c_last; base += kGroup) {
@@ -370,7 +388,8 @@ __device__ __noinline__ void merge_partials(const Epi e, int b, int h, long long
         ls[k] = -INFINITY;
         x[k] = y[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (cta <= c_last) {
-          const size_t ps = static_cast<size_t>(cta * 2 + (S <= cta * chunk ? 0 : 1)) * 8 + g;
+          const size_t ps =
+              static_cast<size_t>(cta * 2 + (S <= cta * chunk ? 0 : 1)) * kRows + g;
           const float4* src = reinterpret_cast<const float4*>(e.part_o + ps * D + cc * 8);
           ls[k] = __ldcg(e.part_lse + ps);
           x[k] = __ldcg(src);
@@ -397,7 +416,7 @@ __device__ __noinline__ void merge_partials(const Epi e, int b, int h, long long
       }
       M = Mn;
     }
-    const size_t row = static_cast<size_t>(b) * e.num_q_heads + h * G + g;
+    const size_t row = e.out_row(b, h, g);
     uint4 pk = make_uint4(0, 0, 0, 0);
     if (!any_bad) {
       const float f = vsc / lsum;
@@ -430,7 +449,7 @@ __device__ __forceinline__ int unit_segments(const Walk& w, long long chunk) {
 // The merge warp: the epilogue of every unit of this CTA's range but the last (the
 // consumer warps, which have nothing left to stream then, do that one with 128
 // threads), so the consumers hand a unit over and go straight on to the next.
-template <int D, bool kFp8>
+template <int D, bool kFp8, int NT>
 __device__ __forceinline__ void merge_units(const DecodeParams& p, const Epi epi,
                                             const Run* runs, int nruns, long long r0,
                                             long long chunk, const float* wo,
@@ -442,15 +461,17 @@ __device__ __forceinline__ void merge_units(const DecodeParams& p, const Epi epi
   for (int cu = 0;; ++cu) {
     const Walk w = cur.w;
     if (!cur.next(p, runs)) return;  // w is the range's last unit
-    constexpr int kBufs = Cfg<D, kFp8>::kMergeBufs;
+    using C = Cfg<D, kFp8, NT>;
+    constexpr int kBufs = C::kMergeBufs;
     const int mb = cu % kBufs;
     if (!__all_sync(0xffffffffu, mbar_wait(&unit_done[mb], (cu / kBufs) & 1, p.wait_ns))) {
       if (lane == 0) record_status(p.dev_status, PGQA_ETIMEOUT);
       return;
     }
     const int nseg = unit_segments(w, chunk);
-    combine_unit<D, kFp8>(epi, w.b, w.h, nseg, w.S <= r0 ? 0 : 1, wo + mb * (kNW * 8 * D),
-                          wml + mb * (kNW * 8 * 2), lane, 32);
+    combine_unit<D, kFp8, NT>(epi, w.b, w.h, nseg, w.S <= r0 ? 0 : 1,
+                              wo + mb * (kNW * C::kRows * D), wml + mb * (kNW * C::kRows * 2),
+                              lane, 32);
     __syncwarp();  // every lane has read the buffer and issued its writes
     if (lane == 0) mbar_arrive(&merge_free[mb]);
     if (nseg > 1) {
@@ -458,24 +479,25 @@ __device__ __forceinline__ void merge_units(const DecodeParams& p, const Epi epi
       if (lane == 0) last = ticket_last(p.counters + w.b * p.num_kv_heads + w.h, nseg);
       last = __shfl_sync(0xffffffffu, last, 0);
       __syncwarp();  // the lanes' reads of the partials come after lane 0's acquire
-      if (last) merge_partials<D, kFp8>(epi, w.b, w.h, w.S, w.P, chunk, lane, 32);
+      if (last) merge_partials<D, kFp8, NT>(epi, w.b, w.h, w.S, w.P, chunk, lane, 32);
     }
   }
 }
 
-template <int D, bool kFp8>
-__global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_decode_kernel(
+template <int D, bool kFp8, int NT>
+__global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT>())) paged_decode_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const DecodeParams p, const DecodeAppend ap) {
-  using C = Cfg<D, kFp8>;
+  using C = Cfg<D, kFp8, NT>;
+  constexpr int kRows = C::kRows;
   constexpr int S = C::kStages;
   constexpr int SPW = C::kStagesPerWarp;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* ring = smem;
-  float* wo = reinterpret_cast<float*>(smem + C::kOffMerge);  // [kNW][8][D]
-  float* wml = reinterpret_cast<float*>(smem + C::kOffMl);    // [2][kNW][8][2] (m, l) base 2
+  float* wo = reinterpret_cast<float*>(smem + C::kOffMerge);  // [bufs][kNW][kRows][D]
+  float* wml = reinterpret_cast<float*>(smem + C::kOffMl);    // [bufs][kNW][kRows][2] (m, l)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* empty = full + S;
   uint64_t* unit_done = empty + S;       // [2] the consumer warps' states of a unit are in
@@ -492,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, ncta = gridDim.x;
   const int G = p.group, Hkv = p.num_kv_heads, B = p.num_seqs;
-  const Epi epi{p.out, p.lse, p.part_lse, p.part_o, p.v_scale, p.num_q_heads, p.group};
+  const Epi epi{p.out, p.lse, p.part_lse, p.part_o, p.v_scale, p.num_q_heads, p.group, p.q_len};
   if (warp == kWarpProd && lane == 0) {
     tma_prefetch_desc(&kmap);
     tma_prefetch_desc(&vmap);
@@ -614,8 +636,8 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
     bool valid;
     if (pages_of(p, b, &valid) != 0) continue;
     if (!valid && tid == 0) record_status(p.dev_status, PGQA_EINVAL);
-    for (int i = tid; i < p.num_q_heads * (D / 8); i += kThreads) {
-      const size_t row = static_cast<size_t>(b) * p.num_q_heads + i / (D / 8);
+    for (int i = tid; i < p.q_len * p.num_q_heads * (D / 8); i += kThreads) {
+      const size_t row = static_cast<size_t>(b) * p.q_len * p.num_q_heads + i / (D / 8);
       reinterpret_cast<uint4*>(p.out + row * D)[i % (D / 8)] = make_uint4(0, 0, 0, 0);
       if (i % (D / 8) == 0 && p.lse) p.lse[row] = -INFINITY;
     }
@@ -701,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
 
   // ================================================================ merge warp
   if (warp == kWarpMerge) {
-    merge_units<D, kFp8>(p, epi, runs, nruns, r0, chunk, wo, wml, unit_done, merge_free);
+    merge_units<D, kFp8, NT>(p, epi, runs, nruns, r0, chunk, wo, wml, unit_done, merge_free);
     return;
   }
 
@@ -711,34 +733,46 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
   const uint32_t cK = lane >> 4;
   const uint32_t rowV = (lane & 7) + ((lane >> 4) << 3);
   const uint32_t cV = (lane >> 3) & 1;
+  const int R = G * p.q_len;  // query rows of a unit: row i = token i / G, head i % G
   bool alive = true;  // false once one of this warp's waits gave up
   int i_base = 0;     // CTA-local index of the unit's first page
   int cu = 0;         // units of this CTA done so far
-  // raw query words of a unit, column n = query head gid of the group:
+  // raw query words of a unit, column n = query row 8 nt + gid of the unit:
   //   bf16: the two B-fragment registers per 16-wide chunk as stored;
   //   E4M3: k index 2tig+{0,1} <-> d = 16kc + 4tig + {0,1}; 2tig+8+{0,1} <-> +{2,3}
-  uint32_t qraw[C::kNkc][2];
+  uint32_t qraw[C::kNkc][NT][2];
   auto load_q = [&](const Walk& u) {
-    const bool live = gid < G;
-    const __nv_bfloat16* qrow =
-        p.q + (static_cast<size_t>(u.b) * p.num_q_heads + u.h * G + (live ? gid : 0)) * D;
 #pragma unroll
-    for (int kc = 0; kc < C::kNkc; ++kc) {
-      if constexpr (!kFp8) {
-        const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow + 16 * kc + 2 * tig);
-        qraw[kc][0] = live ? __ldg(q32) : 0u;
-        qraw[kc][1] = live ? __ldg(q32 + 4) : 0u;
-      } else {
-        const uint2 q4 = live ? __ldg(reinterpret_cast<const uint2*>(qrow + 16 * kc + 4 * tig))
-                              : make_uint2(0, 0);
-        qraw[kc][0] = q4.x;
-        qraw[kc][1] = q4.y;
+    for (int nt = 0; nt < NT; ++nt) {
+      const int i = 8 * nt + gid;
+      const bool live = i < R;
+      const int t = live ? i / G : 0, g = live ? i - t * G : 0;
+      const __nv_bfloat16* qrow =
+          p.q + ((static_cast<size_t>(u.b) * p.q_len + t) * p.num_q_heads + u.h * G + g) * D;
+#pragma unroll
+      for (int kc = 0; kc < C::kNkc; ++kc) {
+        if constexpr (!kFp8) {
+          const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow + 16 * kc + 2 * tig);
+          qraw[kc][nt][0] = live ? __ldg(q32) : 0u;
+          qraw[kc][nt][1] = live ? __ldg(q32 + 4) : 0u;
+        } else {
+          const uint2 q4 = live ? __ldg(reinterpret_cast<const uint2*>(qrow + 16 * kc + 4 * tig))
+                                : make_uint2(0, 0);
+          qraw[kc][nt][0] = q4.x;
+          qraw[kc][nt][1] = q4.y;
+        }
       }
     }
   };
+  // keys a column of the fragment (query row 8 nt + 2 tig + c) sees fewer than the last
+  // key of the context: q_len - 1 - its token (0 for single-token decode)
+  auto key_shift = [&](int nt, int c) {
+    const int i = 8 * nt + 2 * tig + c;
+    return i < R ? p.q_len - 1 - i / G : 0;
+  };
   Cursor cur;
   cur.start(runs, nruns);
-  load_q(cur.w);
+  if (NT == 1) load_q(cur.w);
   for (bool more = true; more;) {
     const Walk w = cur.w;
     const int seg0 = cur.seg0, npg = cur.npg();
@@ -747,19 +781,30 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
     const int L = __ldg(p.context_lens + w.b);
     const int kfirst = first_key(p, L);
 
-    // Q^T fragments (B operand) of this unit, then start loading the next unit's
-    uint32_t qf[C::kNkc][2];
+    // Q^T fragments (B operand) of this unit; single-row-tile units start loading the
+    // next unit's here (the multi-token form loads its larger fragments unit by unit)
+    if (NT > 1) load_q(w);
+    uint32_t qf[C::kNkc][NT][2];
 #pragma unroll
     for (int kc = 0; kc < C::kNkc; ++kc) {
-      if constexpr (!kFp8) {
-        qf[kc][0] = qraw[kc][0];
-        qf[kc][1] = qraw[kc][1];
-      } else {
-        qf[kc][0] = pack_f16(bf16_lo(qraw[kc][0]), bf16_hi(qraw[kc][0]));
-        qf[kc][1] = pack_f16(bf16_lo(qraw[kc][1]), bf16_hi(qraw[kc][1]));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        if constexpr (!kFp8) {
+          qf[kc][nt][0] = qraw[kc][nt][0];
+          qf[kc][nt][1] = qraw[kc][nt][1];
+        } else {
+          qf[kc][nt][0] = pack_f16(bf16_lo(qraw[kc][nt][0]), bf16_hi(qraw[kc][nt][0]));
+          qf[kc][nt][1] = pack_f16(bf16_lo(qraw[kc][nt][1]), bf16_hi(qraw[kc][nt][1]));
+        }
       }
     }
-    if (more) load_q(nxt.w);
+    if (NT == 1 && more) load_q(nxt.w);
+    int dq[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      dq[nt][0] = key_shift(nt, 0);
+      dq[nt][1] = key_shift(nt, 1);
+    }
 
     // fused append: the page holding key L-1, if this warp reads it (segment-relative),
     // this lane's 16-byte chunk of the new K (lanes 0..kAppLanes-1) or V row, still
@@ -788,10 +833,16 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
     }
 
     const float sl2 = p.scale_log2 * (kFp8 ? __ldg(p.k_scale + w.h) : 1.f);
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    float acc[C::kNkc][4];
+    float m_run[NT][2], l_run[NT][2];
+    float acc[C::kNkc][NT][4];
 #pragma unroll
-    for (int i = 0; i < C::kNkc; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt) {
+      m_run[nt][0] = m_run[nt][1] = -INFINITY;
+      l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+      for (int i = 0; i < C::kNkc; ++i)
+        acc[i][nt][0] = acc[i][nt][1] = acc[i][nt][2] = acc[i][nt][3] = 0.f;
+    }
     int bad = 0;
 
     // this warp's pages of the unit: CTA-local index i = i_base + j with i % kNW == warp
@@ -834,59 +885,83 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
       const int nv = min(16, L - pk0);               // rows below nv hold keys < L
       const int lo = max(0, kfirst - pk0);           // rows below lo are outside the window
 
-      // ---- S^T = K Q^T, over two accumulators (even / odd 16-wide chunks of head_dim)
-      //      so the MMA chain is half as long
-      float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+      // ---- S^T = K Q^T per row tile, over two accumulators (even / odd 16-wide chunks
+      //      of head_dim) so the MMA chain is half as long; each K fragment is loaded
+      //      (and, E4M3, widened) once for all row tiles
+      float sc[NT][4], sd[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sc[nt][q] = sd[nt][q] = 0.f;
       if constexpr (!kFp8) {
 #pragma unroll
         for (int kc = 0; kc < C::kNkc; ++kc) {
           uint32_t a0, a1, a2, a3;
           ldsm_x4(stK + (kc >> 2) * 2048 + swz128(rowK, (kc & 3) * 2 + cK), a0, a1, a2, a3);
-          mma_bf16((kc & 1) ? sd : sc, a0, a1, a2, a3, qf[kc][0], qf[kc][1]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma_bf16((kc & 1) ? sd[nt] : sc[nt], a0, a1, a2, a3, qf[kc][nt][0], qf[kc][nt][1]);
         }
       } else {
 #pragma unroll
         for (int kc = 0; kc < C::kNkc; kc += 2) {
           uint32_t r0v, r1v, r2v, r3v;
           ldsm_x4(stK + swz128(rowK, kc + cK), r0v, r1v, r2v, r3v);
-          mma_f16(sc, e4m3x2_to_f16x2(r0v & 0xffff), e4m3x2_to_f16x2(r1v & 0xffff),
-                  e4m3x2_to_f16x2(r0v >> 16), e4m3x2_to_f16x2(r1v >> 16), qf[kc][0], qf[kc][1]);
-          mma_f16(sd, e4m3x2_to_f16x2(r2v & 0xffff), e4m3x2_to_f16x2(r3v & 0xffff),
-                  e4m3x2_to_f16x2(r2v >> 16), e4m3x2_to_f16x2(r3v >> 16), qf[kc + 1][0],
-                  qf[kc + 1][1]);
+          const uint32_t a0 = e4m3x2_to_f16x2(r0v & 0xffff), a1 = e4m3x2_to_f16x2(r1v & 0xffff),
+                         a2 = e4m3x2_to_f16x2(r0v >> 16), a3 = e4m3x2_to_f16x2(r1v >> 16);
+          const uint32_t b0 = e4m3x2_to_f16x2(r2v & 0xffff), b1 = e4m3x2_to_f16x2(r3v & 0xffff),
+                         b2 = e4m3x2_to_f16x2(r2v >> 16), b3 = e4m3x2_to_f16x2(r3v >> 16);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_f16(sc[nt], a0, a1, a2, a3, qf[kc][nt][0], qf[kc][nt][1]);
+            mma_f16(sd[nt], b0, b1, b2, b3, qf[kc + 1][nt][0], qf[kc + 1][nt][1]);
+          }
         }
       }
+      // ---- per row tile: masks, the online softmax, P^T as the B operand
+      //      fragment: sc[0] (tok gid, row 2tig), sc[1] (gid, 2tig+1),
+      //                sc[2] (gid+8, 2tig),    sc[3] (gid+8, 2tig+1)
+      uint32_t pb0[NT], pb1[NT];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) sc[q] += sd[q];
-      // fragment: sc[0] (tok gid, head 2tig), sc[1] (gid, 2tig+1),
-      //           sc[2] (gid+8, 2tig),      sc[3] (gid+8, 2tig+1)
-      float s0 = sc[0] * sl2, s1 = sc[1] * sl2, s2 = sc[2] * sl2, s3 = sc[3] * sl2;
-      if (gid >= nv || gid < lo) s0 = s1 = -INFINITY;
-      if (gid + 8 >= nv || gid + 8 < lo) s2 = s3 = -INFINITY;
-      float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+      for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        for (int q = 0; q < 4; ++q) sc[nt][q] += sd[nt][q];
+        // rows below nv0 / nv1 hold keys the column attends (multi-token: token t of q_len
+        // sees keys up to L - q_len + t)
+        const int nv0 = min(16, L - dq[nt][0] - pk0), nv1 = min(16, L - dq[nt][1] - pk0);
+        float s0 = sc[nt][0] * sl2, s1 = sc[nt][1] * sl2, s2 = sc[nt][2] * sl2,
+              s3 = sc[nt][3] * sl2;
+        if (gid >= nv0 || gid < lo) s0 = -INFINITY;
+        if (gid >= nv1 || gid < lo) s1 = -INFINITY;
+        if (gid + 8 >= nv0 || gid + 8 < lo) s2 = -INFINITY;
+        if (gid + 8 >= nv1 || gid + 8 < lo) s3 = -INFINITY;
+        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        }
+        const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
+        // a column that has seen no key yet (a page past a draft token's last key) keeps
+        // m = -inf; 0 as the reference then gives 2^-inf = 0 instead of NaN
+        const float rf0 = mn0 == -INFINITY ? 0.f : mn0, rf1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = ex2(m_run[nt][0] - rf0), al1 = ex2(m_run[nt][1] - rf1);
+        m_run[nt][0] = mn0;
+        m_run[nt][1] = mn1;
+        const float p0v = ex2(s0 - rf0), p1v = ex2(s1 - rf1), p2v = ex2(s2 - rf0),
+                    p3v = ex2(s3 - rf1);
+        l_run[nt][0] = l_run[nt][0] * al0 + (p0v + p2v);
+        l_run[nt][1] = l_run[nt][1] * al1 + (p1v + p3v);
+#pragma unroll
+        for (int dc = 0; dc < C::kNkc; ++dc) {
+          acc[dc][nt][0] *= al0;
+          acc[dc][nt][1] *= al1;
+          acc[dc][nt][2] *= al0;
+          acc[dc][nt][3] *= al1;
+        }
+        pb0[nt] = movmatrix_t(kFp8 ? pack_f16(p0v, p1v) : pack_bf16(p0v, p1v));
+        pb1[nt] = movmatrix_t(kFp8 ? pack_f16(p2v, p3v) : pack_bf16(p2v, p3v));
       }
-      const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-      const float al0 = ex2(m_run[0] - mn0), al1 = ex2(m_run[1] - mn1);
-      m_run[0] = mn0;
-      m_run[1] = mn1;
-      const float p0v = ex2(s0 - mn0), p1v = ex2(s1 - mn1), p2v = ex2(s2 - mn0),
-                  p3v = ex2(s3 - mn1);
-      l_run[0] = l_run[0] * al0 + (p0v + p2v);
-      l_run[1] = l_run[1] * al1 + (p1v + p3v);
-#pragma unroll
-      for (int dc = 0; dc < C::kNkc; ++dc) {
-        acc[dc][0] *= al0;
-        acc[dc][1] *= al1;
-        acc[dc][2] *= al0;
-        acc[dc][3] *= al1;
-      }
-      // ---- P^T as the B operand (k = token, n = head)
-      const uint32_t pb0 = movmatrix_t(kFp8 ? pack_f16(p0v, p1v) : pack_bf16(p0v, p1v));
-      const uint32_t pb1 = movmatrix_t(kFp8 ? pack_f16(p2v, p3v) : pack_bf16(p2v, p3v));
 
       // ---- O^T += V^T P^T; rows past the context are zeroed (they may hold NaN)
       const uint32_t m01 =
@@ -906,7 +981,8 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
             v2 &= m89;
             v3 &= m89;
           }
-          mma_bf16(acc[dc], v0, v1, v2, v3, pb0, pb1);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16(acc[dc][nt], v0, v1, v2, v3, pb0[nt], pb1[nt]);
         }
       } else {
         // thread rows d in [16 gid, 16 gid + 16): row r of chunk dc <-> d = 16 (r & 7) + 2 dc + (r >> 3)
@@ -927,8 +1003,10 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
           const uint32_t sel = (dc & 1) ? 0x7362u : 0x5140u;
           const uint32_t lo = prmt(w0[dc >> 1], w1[dc >> 1], sel);
           const uint32_t hi = prmt(w8[dc >> 1], w9[dc >> 1], sel);
-          mma_f16(acc[dc], e4m3x2_to_f16x2(lo & 0xffff), e4m3x2_to_f16x2(lo >> 16),
-                  e4m3x2_to_f16x2(hi & 0xffff), e4m3x2_to_f16x2(hi >> 16), pb0, pb1);
+          const uint32_t v0 = e4m3x2_to_f16x2(lo & 0xffff), v1 = e4m3x2_to_f16x2(lo >> 16),
+                         v2 = e4m3x2_to_f16x2(hi & 0xffff), v3 = e4m3x2_to_f16x2(hi >> 16);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_f16(acc[dc][nt], v0, v1, v2, v3, pb0[nt], pb1[nt]);
         }
       }
       __syncwarp();
@@ -939,9 +1017,12 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
     // ---- this warp's state for the unit -> the merge buffer of the unit's parity;
     //      the merge warp takes it from there and this warp goes on to the next unit
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], o);
-      l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], o);
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        l_run[nt][0] += __shfl_xor_sync(0xffffffffu, l_run[nt][0], o);
+        l_run[nt][1] += __shfl_xor_sync(0xffffffffu, l_run[nt][1], o);
+      }
     }
     const bool poisoned_w = __any_sync(0xffffffffu, bad != 0) || !__all_sync(0xffffffffu, alive);
     constexpr int kBufs = C::kMergeBufs;
@@ -951,31 +1032,34 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
       alive = false;
       if (lane == 0) record_status(p.dev_status, PGQA_ETIMEOUT);
     }
-    float* wob = wo + mb * (kNW * 8 * D);
-    float* wmlb = wml + mb * (kNW * 8 * 2);
+    float* wob = wo + mb * (kNW * kRows * D);
+    float* wmlb = wml + mb * (kNW * kRows * 2);
 #pragma unroll
-    for (int dc = 0; dc < C::kNkc; ++dc) {
-      int d0, d1;
-      if constexpr (!kFp8) {
-        d0 = 16 * dc + gid;
-        d1 = d0 + 8;
-      } else {
-        d0 = 16 * gid + 2 * dc;
-        d1 = d0 + 1;
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int dc = 0; dc < C::kNkc; ++dc) {
+        int d0, d1;
+        if constexpr (!kFp8) {
+          d0 = 16 * dc + gid;
+          d1 = d0 + 8;
+        } else {
+          d0 = 16 * gid + 2 * dc;
+          d1 = d0 + 1;
+        }
+        float* o0 = wob + (warp * kRows + 8 * nt + 2 * tig) * D;
+        float* o1 = o0 + D;
+        o0[d0] = acc[dc][nt][0];
+        o1[d0] = acc[dc][nt][1];
+        o0[d1] = acc[dc][nt][2];
+        o1[d1] = acc[dc][nt][3];
       }
-      float* o0 = wob + (warp * 8 + 2 * tig) * D;
-      float* o1 = o0 + D;
-      o0[d0] = acc[dc][0];
-      o1[d0] = acc[dc][1];
-      o0[d1] = acc[dc][2];
-      o1[d1] = acc[dc][3];
-    }
-    if (gid == 0) {
-      float* ml = wmlb + (warp * 8 + 2 * tig) * 2;
-      ml[0] = m_run[0];
-      ml[1] = poisoned_w ? NAN : l_run[0];  // NaN l marks a poisoned warp state
-      ml[2] = m_run[1];
-      ml[3] = poisoned_w ? NAN : l_run[1];
+      if (gid == 0) {
+        float* ml = wmlb + (warp * kRows + 8 * nt + 2 * tig) * 2;
+        ml[0] = m_run[nt][0];
+        ml[1] = poisoned_w ? NAN : l_run[nt][0];  // NaN l marks a poisoned warp state
+        ml[2] = m_run[nt][1];
+        ml[3] = poisoned_w ? NAN : l_run[nt][1];
+      }
     }
     __syncwarp();
     cur = nxt;
@@ -987,20 +1071,20 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8>())) paged_deco
     // the range's last unit: nothing left to stream, so the consumer warps finish it
     const int nseg = unit_segments(w, chunk);
     bar_consumers();
-    combine_unit<D, kFp8>(epi, w.b, w.h, nseg, w.S <= r0 ? 0 : 1, wob, wmlb, tid, kNW * 32);
+    combine_unit<D, kFp8, NT>(epi, w.b, w.h, nseg, w.S <= r0 ? 0 : 1, wob, wmlb, tid, kNW * 32);
     if (nseg > 1) {
       bar_consumers();  // this CTA's partial writes are issued
       if (tid == 0) misc[1] = ticket_last(p.counters + w.b * Hkv + w.h, nseg);
       bar_consumers();  // (and the reads below come after the acquire)
-      if (misc[1]) merge_partials<D, kFp8>(epi, w.b, w.h, w.S, w.P, chunk, tid, kNW * 32);
+      if (misc[1]) merge_partials<D, kFp8, NT>(epi, w.b, w.h, w.S, w.P, chunk, tid, kNW * 32);
     }
     ++cu;
   }
 }
 
-template <int D, bool kFp8>
+template <int D, bool kFp8, int NT>
 pgqa_status_t launch_variant(const DecodeArgs& a, const DecodePlan& plan) {
-  using C = Cfg<D, kFp8>;
+  using C = Cfg<D, kFp8, NT>;
   const CUtensorMapDataType dt =
       kFp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.num_kv_heads * a.block_size;
@@ -1011,7 +1095,8 @@ pgqa_status_t launch_variant(const DecodeArgs& a, const DecodePlan& plan) {
       !tensor_map_2d(&vmap, a.v_cache, dt, D, rows, C::kRowBytes, 128 / C::kElem, box_rows,
                      CU_TENSOR_MAP_SWIZZLE_128B))
     return PGQA_ECUDA;
-  if (!smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<D, kFp8>), C::kSmem))
+  if (!smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<D, kFp8, NT>),
+                       C::kSmem))
     return PGQA_ECUDA;
   DecodeParams p;
   p.out = static_cast<__nv_bfloat16*>(a.out);
@@ -1031,6 +1116,7 @@ pgqa_status_t launch_variant(const DecodeArgs& a, const DecodePlan& plan) {
   p.num_q_heads = a.num_q_heads;
   p.num_kv_heads = a.num_kv_heads;
   p.group = a.num_q_heads / a.num_kv_heads;
+  p.q_len = a.q_len;
   p.num_blocks = a.num_blocks;
   p.max_context_len = a.max_context_len;
   p.window = a.window;
@@ -1042,7 +1128,7 @@ pgqa_status_t launch_variant(const DecodeArgs& a, const DecodePlan& plan) {
   ap.value = static_cast<const uint4*>(a.new_value);
   ap.k_cache = static_cast<uint8_t*>(const_cast<void*>(a.k_cache));
   ap.v_cache = static_cast<uint8_t*>(const_cast<void*>(a.v_cache));
-  if (launch_after_previous(paged_decode_kernel<D, kFp8>, dim3(plan.grid), dim3(kThreads),
+  if (launch_after_previous(paged_decode_kernel<D, kFp8, NT>, dim3(plan.grid), dim3(kThreads),
                             C::kSmem, a.stream, kmap, vmap, p, ap) != cudaSuccess)
     return PGQA_ECUDA;
   return cudaPeekAtLastError() == cudaSuccess ? PGQA_OK : PGQA_ECUDA;
@@ -1065,18 +1151,28 @@ void set_decode_wait_limit_ns(unsigned long long ns) {
   g_decode_wait_ns.store(ns, std::memory_order_relaxed);
 }
 
-int decode_ctas_per_sm(int head_dim, int cache_dtype) {
+int decode_row_tiles(int q_len, int group) {
+  const int rows = q_len * group;
+  return rows <= 8 ? 1 : rows <= 24 ? 3 : 0;
+}
+
+int decode_ctas_per_sm(int head_dim, int cache_dtype, int row_tiles) {
+  if (row_tiles == 3) {
+    if (cache_dtype == PGQA_DTYPE_E4M3) return ctas_per_sm<128, true, 3>();
+    return head_dim == 64 ? ctas_per_sm<64, false, 3>() : ctas_per_sm<128, false, 3>();
+  }
   if (cache_dtype == PGQA_DTYPE_E4M3) return ctas_per_sm<128, true>();
   return head_dim == 64 ? ctas_per_sm<64, false>() : ctas_per_sm<128, false>();
 }
 
 DecodePlan decode_plan(int num_seqs, int num_kv_heads, int head_dim, int cache_dtype,
-                       int num_sms) {
+                       int num_sms, int row_tiles) {
   DecodePlan plan{};
-  plan.grid = (num_sms > 0 ? num_sms : 1) * decode_ctas_per_sm(head_dim, cache_dtype);
+  plan.row_tiles = row_tiles;
+  plan.grid = (num_sms > 0 ? num_sms : 1) * decode_ctas_per_sm(head_dim, cache_dtype, row_tiles);
   const size_t units = static_cast<size_t>(num_seqs > 0 ? num_seqs : 0) *
                        static_cast<size_t>(num_kv_heads > 0 ? num_kv_heads : 0);
-  const size_t slots = static_cast<size_t>(plan.grid) * 2 * 8;
+  const size_t slots = static_cast<size_t>(plan.grid) * 2 * 8 * row_tiles;
   plan.counters_off = 0;
   plan.lse_off = align256(units * sizeof(int));
   plan.o_off = plan.lse_off + align256(slots * sizeof(float));
@@ -1085,20 +1181,29 @@ DecodePlan decode_plan(int num_seqs, int num_kv_heads, int head_dim, int cache_d
 }
 
 bool decode_prepare() {
-  return smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<128, false>),
+  return smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<128, false, 1>),
                          Cfg<128, false>::kSmem) &&
-         smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<64, false>),
+         smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<64, false, 1>),
                          Cfg<64, false>::kSmem) &&
-         smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<128, true>),
+         smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<128, true, 1>),
                          Cfg<128, true>::kSmem);
 }
 
 pgqa_status_t launch_paged_decode(const DecodeArgs& a, const DecodePlan& plan) {
-  if (a.cache_dtype == PGQA_DTYPE_BF16) {
-    if (a.head_dim == 128) return launch_variant<128, false>(a, plan);
-    if (a.head_dim == 64) return launch_variant<64, false>(a, plan);
-  } else if (a.cache_dtype == PGQA_DTYPE_E4M3) {
-    if (a.head_dim == 128) return launch_variant<128, true>(a, plan);
+  if (plan.row_tiles == 1) {
+    if (a.cache_dtype == PGQA_DTYPE_BF16) {
+      if (a.head_dim == 128) return launch_variant<128, false, 1>(a, plan);
+      if (a.head_dim == 64) return launch_variant<64, false, 1>(a, plan);
+    } else if (a.cache_dtype == PGQA_DTYPE_E4M3) {
+      if (a.head_dim == 128) return launch_variant<128, true, 1>(a, plan);
+    }
+  } else if (plan.row_tiles == 3) {
+    if (a.cache_dtype == PGQA_DTYPE_BF16) {
+      if (a.head_dim == 128) return launch_variant<128, false, 3>(a, plan);
+      if (a.head_dim == 64) return launch_variant<64, false, 3>(a, plan);
+    } else if (a.cache_dtype == PGQA_DTYPE_E4M3) {
+      if (a.head_dim == 128) return launch_variant<128, true, 3>(a, plan);
+    }
   }
   return PGQA_EUNSUPPORTED;
 }

@@ -78,6 +78,9 @@ struct DecodeArgs {
   const float* v_scale;
   int max_context_len;
   int window;  // > 0: only the last `window` keys of each context are attended
+  int q_len;   // new tokens per sequence (1: decode; more: multi-token decode, q is
+               // [num_seqs][q_len][num_q_heads][head_dim] and token t sees keys
+               // 0 .. L - q_len + t)
   // fused append (both null: none): the new token's K/V rows [num_seqs][Hkv][D] bf16,
   // written at position context_len - 1 of each sequence before it is attended
   const void* new_key;
@@ -93,11 +96,15 @@ struct DecodeArgs {
 // kv-head) and two partial-result slots per CTA.
 struct DecodePlan {
   int grid;
+  int row_tiles;  // 8-row tiles of query rows per unit the kernel variant holds (1 or 3)
   size_t counters_off, lse_off, o_off, bytes;
 };
-int decode_ctas_per_sm(int head_dim, int cache_dtype);
+// 8-row tiles the decode kernel needs for q_len x group query rows per unit: 1 (up to 8
+// rows), 3 (up to 24), or 0 when the decode kernel does not take that many
+int decode_row_tiles(int q_len, int group);
+int decode_ctas_per_sm(int head_dim, int cache_dtype, int row_tiles = 1);
 DecodePlan decode_plan(int num_seqs, int num_kv_heads, int head_dim, int cache_dtype,
-                       int num_sms);
+                       int num_sms, int row_tiles = 1);
 
 pgqa_status_t launch_paged_decode(const DecodeArgs& a, const DecodePlan& plan);
 
@@ -129,7 +136,7 @@ struct PrefillArgs {
   const void* v_cache;
   const int32_t* block_tables;
   int max_blocks_per_seq;
-  const int32_t* cu_seqlens;
+  const int32_t* cu_seqlens;  // null: every sequence has max_seqlen new tokens, in order
   const int32_t* seq_lens_k;  // cached tokens per sequence, or null (no cached prefix)
   int max_seqlen_k;
   void* workspace;  // >= prefill_workspace_bytes(), zero before first use

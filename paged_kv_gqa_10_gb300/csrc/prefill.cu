@@ -115,7 +115,7 @@ static_assert(kScrOff + kMaxLevels * 4 <= 5 * 128 * 64 * 2, "table scratch");
 struct PrefillParams {
   __nv_bfloat16* out;
   float* lse;
-  const int32_t* cu_seqlens;
+  const int32_t* cu_seqlens;  // null: every sequence has max_seqlen new tokens, in order
   const int32_t* seq_lens_k;  // cached tokens per sequence (Lk), or null: Lk = Lq
   const int32_t* block_tables;
   int* dev_status;
@@ -135,7 +135,8 @@ struct PrefillParams {
 // it has no new token or is inconsistent.
 __device__ __forceinline__ bool seq_ok(const PrefillParams& p, int s, int* start, int* lq,
                                        int* lk) {
-  const int st = __ldg(p.cu_seqlens + s), Lq = __ldg(p.cu_seqlens + s + 1) - st;
+  const int st = p.cu_seqlens ? __ldg(p.cu_seqlens + s) : s * p.max_seqlen;
+  const int Lq = p.cu_seqlens ? __ldg(p.cu_seqlens + s + 1) - st : p.max_seqlen;
   const int Lk = p.seq_lens_k ? __ldg(p.seq_lens_k + s) : Lq;
   *start = st;
   *lq = Lq;
