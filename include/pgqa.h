@@ -304,7 +304,7 @@ pgqa_status_t pgqa_paged_attention_decode_append(
 /* Workspace bytes pgqa_paged_attention_decode_multi needs on the current device for
  * these sizes (any cache dtype and block size): as for pgqa_decode_workspace_size, with
  * partial-result slots for the q_len x group query rows of a (sequence, kv-head); or the
- * prefill workspace when those rows are more than 24 (see below). 0 on a bad argument. */
+ * prefill workspace when those rows are more than 32 (see below). 0 on a bad argument. */
 size_t pgqa_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_heads,
                                         int num_kv_heads, int head_dim);
 
@@ -328,7 +328,7 @@ size_t pgqa_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_heads
  *                 it ready for the next call.
  * Every other argument and the error behaviour are as for pgqa_paged_attention_decode.
  * The q_len x (num_q_heads / num_kv_heads) query rows of a (sequence, kv-head) share
- * every page read when they are at most 24 (the decode kernel); above that the prefill
+ * every page read when they are at most 32 (the decode kernel); above that the prefill
  * kernel runs the call (block_size 16 only, else PGQA_EUNSUPPORTED; scale > 0).
  */
 pgqa_status_t pgqa_paged_attention_decode_multi(

@@ -48,6 +48,13 @@
 //    The head-dimension order inside an MMA is a free permutation (it is the
 //    contraction index for QK^T and a row relabelling for PV), chosen so that each
 //    thread's bytes are contiguous in shared memory.
+//  - Multi-token decode (speculative verification): a unit then has q_len x G query
+//    rows (row i = token i / G, head i % G), token t seeing keys 0 .. L - q_len + t
+//    (each fragment column has its own causal limit). Up to 8 rows run as above. Up to
+//    32 run in the row-split form: consumer warp w holds rows 8w .. 8w+7 and reads every
+//    page, from one ring filled in page order whose stages every warp with rows frees;
+//    each warp finishes its own rows (no merge warp), with a ticket per (unit, row tile)
+//    for units cut by range boundaries.
 //  - Every wait is bounded; a warp whose wait gives up records PGQA_ETIMEOUT, stops
 //    computing, but keeps taking part in every CTA barrier, so nothing can hang.
 #include <cuda_bf16.h>
@@ -109,11 +116,13 @@ struct DecodeAppend {
   uint8_t* v_cache;
 };
 
-template <int D, bool kFp8, int NT = 1>
+template <int D, bool kFp8, int NT = 1, bool kRS = false>
 struct Cfg {
-  // query rows of a unit, in 8-row n-tiles: the group's G <= 8 heads (NT = 1), or
-  // q_len tokens x G heads for multi-token decode (NT = 3: up to 24 rows)
-  static constexpr int kRows = 8 * NT;
+  // query rows of a unit, in NT 8-row n-tiles per warp: the group's G <= 8 heads, or
+  // q_len tokens x G heads for multi-token decode (up to 8 rows with NT = 1; the
+  // row-split form kRS: one 8-row tile per consumer warp, up to 32 rows, every warp
+  // reading every page of one shared ring)
+  static constexpr int kRows = kRS ? 8 * kNW : 8 * NT;
   static constexpr int kElem = kFp8 ? 1 : 2;
   static constexpr int kRowBytes = D * kElem;      // one token row of one head
   static constexpr int kSub = kRowBytes / 128;     // 128-byte TMA boxes per row
@@ -123,11 +132,14 @@ struct Cfg {
   // buffer instead of two paying for the fifth stage); multi-token decode runs one CTA
   // per SM and gives each warp 32-40 KB
   static constexpr int kStagesPerWarp =
-      NT > 1 ? (kStageBytes >= 8192 ? 5 : 8)
-             : (kStageBytes >= 8192 ? 2 : kFp8 ? 5 : 16384 / kStageBytes);
-  static constexpr int kMergeBufs = (kFp8 || NT > 1) ? 1 : 2;  // unit states in flight to
-                                                                // the merge warp
-  static constexpr int kStages = kNW * kStagesPerWarp;
+      kRS ? 0
+          : NT > 1 ? (kStageBytes >= 8192 ? 5 : 8)
+                   : (kStageBytes >= 8192 ? 2 : kFp8 ? 5 : 16384 / kStageBytes);
+  // unit states in flight to the merge warp (none in the row-split form: each warp
+  // finishes its own rows)
+  static constexpr int kMergeBufs = kRS ? 0 : (kFp8 || NT > 1) ? 1 : 2;
+  // the row-split form: one ring of about 96 KB, filled in page order
+  static constexpr int kStages = kRS ? 98304 / kStageBytes : kNW * kStagesPerWarp;
   static constexpr int kNkc = D / 16;              // 16-wide chunks of head_dim
   static constexpr int kRing = kStages * kStageBytes;
   static constexpr int kMerge = kNW * kRows * D * 4;  // per-warp O of one unit
@@ -145,10 +157,10 @@ struct Cfg {
 };
 
 // CTAs of one decode kernel resident per SM (the grid is this times the SM count).
-template <int D, bool kFp8, int NT = 1>
+template <int D, bool kFp8, int NT = 1, bool kRS = false>
 constexpr int ctas_per_sm() {
-  static_assert(Cfg<D, kFp8, NT>::kSmem + 1024 <= 227 * 1024, "shared memory");
-  return (227 * 1024) / (Cfg<D, kFp8, NT>::kSmem + 1024) >= 2 ? 2 : 1;
+  static_assert(Cfg<D, kFp8, NT, kRS>::kSmem + 1024 <= 227 * 1024, "shared memory");
+  return (227 * 1024) / (Cfg<D, kFp8, NT, kRS>::kSmem + 1024) >= 2 ? 2 : 1;
 }
 
 // First key attended in a context of L keys: L - window with a sliding window (the
@@ -340,7 +352,9 @@ __device__ __noinline__ void combine_unit(const Epi e, int b, int h, int nseg, i
       o[0] += x.x * wt; o[1] += x.y * wt; o[2] += x.z * wt; o[3] += x.w * wt;
       o[4] += y.x * wt; o[5] += y.y * wt; o[6] += y.z * wt; o[7] += y.w * wt;
     }
-    const float inv = 1.f / lsum;
+    // (a row that saw no key in this CTA's part of a unit, e.g. a draft token whose last
+    // key lies before the part, has lsum = 0: its partial is 0 with lse -inf)
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
     const size_t row = e.out_row(b, h, g);
     if (nseg == 1) {
       uint4 pk = make_uint4(0, 0, 0, 0);
@@ -366,17 +380,18 @@ __device__ __noinline__ void combine_unit(const Epi e, int b, int h, int nseg, i
 // starts at or before its range (its first unit), else in slot 1 (its last). Partials
 // are taken four at a time: a group's loads are all issued before any is used, then
 // merged into a running (M, l, O).
-template <int D, bool kFp8, int NT>
+template <int D, bool kFp8, int NT, bool kRS = false>
 __device__ __noinline__ void merge_partials(const Epi e, int b, int h, long long S, int P,
-                                            long long chunk, int t, int nt) {
-  constexpr int kRows = Cfg<D, kFp8, NT>::kRows;
-  const int R = e.group * e.q_len;
+                                            long long chunk, int t, int nt, int row0 = 0,
+                                            int row1 = 1 << 30) {
+  constexpr int kRows = Cfg<D, kFp8, NT, kRS>::kRows;
+  const int R = min(e.group * e.q_len, row1) - row0;  // rows row0 .. row1-1 of the unit
   constexpr int kChunks = D / 8;
   constexpr int kGroup = 4;
   const float vsc = kFp8 ? __ldg(e.v_scale + h) : 1.f;
   const long long c_first = S / chunk, c_last = (S + P - 1) / chunk;
   for (int it = t; it < R * kChunks; it += nt) {
-    const int g = it / kChunks, cc = it % kChunks;  // g: the query row
+    const int g = row0 + it / kChunks, cc = it % kChunks;  // g: the query row
     float M = -INFINITY, lsum = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     bool any_bad = false;
     for (long long base = c_first; base <= c_last; base += kGroup) {
@@ -484,11 +499,15 @@ __device__ __forceinline__ void merge_units(const DecodeParams& p, const Epi epi
   }
 }
 
-template <int D, bool kFp8, int NT>
-__global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT>())) paged_decode_kernel(
-    const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-    const DecodeParams p, const DecodeAppend ap) {
-  using C = Cfg<D, kFp8, NT>;
+template <int D, bool kFp8, int NT, bool kRS>
+__global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
+    paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const DecodeParams p,
+                        const DecodeAppend ap) {
+  using C = Cfg<D, kFp8, NT, kRS>;
+  // row-split: consumer warp w holds row tile w (rows 8w .. 8w+7) of every unit and
+  // reads every page; kRT of them have rows (the others leave at once)
+  const int kRT = kRS ? (p.group * p.q_len + 7) / 8 : 1;
   constexpr int kRows = C::kRows;
   constexpr int S = C::kStages;
   constexpr int SPW = C::kStagesPerWarp;
@@ -574,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT>())) paged_
     misc[2] = r0 < r1 ? plan_runs(p, w0, r0, r1, runs) : 0;
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], kRS ? kRT : 1);  // row-split: every warp with rows frees it
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&unit_done[s], kNW);
@@ -646,19 +665,22 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT>())) paged_
 
   // ================================================================ producer
   if (warp == kWarpProd) {
-    // lane w < kNW serves consumer warp w: its pages are w, w + kNW, ...
-    const int nw_pages = lane < kNW && n > lane ? (n - lane + kNW - 1) / kNW : 0;
-    int next_li = 0;  // next local index of that warp to issue
+    // lane w < kNW serves consumer warp w: its pages are w, w + kNW, ... (row-split:
+    // lane 0 serves the one ring every consumer warp reads, all pages in order)
+    constexpr int kPW = kRS ? 1 : kNW;       // page streams
+    constexpr int kSPW = kRS ? S : SPW;      // stages per stream
+    const int nw_pages = lane < kPW && n > lane ? (n - lane + kPW - 1) / kPW : 0;
+    int next_li = 0;  // next local index of that stream to issue
     uint64_t idle_since = 0;
     for (;;) {
       const int pend = __reduce_min_sync(
-          0xffffffffu, lane < kNW && next_li < nw_pages ? lane + kNW * next_li : INT_MAX);
+          0xffffffffu, lane < kPW && next_li < nw_pages ? lane + kPW * next_li : INT_MAX);
       if (pend == INT_MAX) break;  // every page issued
       bool progress = false;
-      // refill consumer warp `lane`'s next stage if it is free
-      if (lane < kNW && next_li < nw_pages) {
-        const int i = lane + kNW * next_li;
-        const int s = lane * SPW + next_li % SPW, use = next_li / SPW;
+      // refill stream `lane`'s next stage if it is free
+      if (lane < kPW && next_li < nw_pages) {
+        const int i = lane + kPW * next_li;
+        const int s = lane * kSPW + next_li % kSPW, use = next_li / kSPW;
         if (i < fetched && (use == 0 || mbar_try_wait(&empty[s], (use - 1) & 1))) {
           int y = yring[i % kYRing], y1 = yring2[i % kYRing];
           int bad = 0;
@@ -711,10 +733,10 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT>())) paged_
     }
     // No TMA write may land after this CTA exits: wait for the last fill of each
     // stage (complete already on the normal path).
-    if (lane < kNW) {
-      for (int k = 0; k < SPW && k < next_li; ++k) {
-        const int last_li = k + ((next_li - 1 - k) / SPW) * SPW;
-        if (!mbar_wait(&full[lane * SPW + k], (last_li / SPW) & 1))
+    if (lane < kPW) {
+      for (int k = 0; k < kSPW && k < next_li; ++k) {
+        const int last_li = k + ((next_li - 1 - k) / kSPW) * kSPW;
+        if (!mbar_wait(&full[lane * kSPW + k], (last_li / kSPW) & 1))
           record_status(p.dev_status, PGQA_ETIMEOUT);
       }
     }
@@ -723,7 +745,8 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT>())) paged_
 
   // ================================================================ merge warp
   if (warp == kWarpMerge) {
-    merge_units<D, kFp8, NT>(p, epi, runs, nruns, r0, chunk, wo, wml, unit_done, merge_free);
+    if constexpr (!kRS)
+      merge_units<D, kFp8, NT>(p, epi, runs, nruns, r0, chunk, wo, wml, unit_done, merge_free);
     return;
   }
 
@@ -734,6 +757,8 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT>())) paged_
   const uint32_t rowV = (lane & 7) + ((lane >> 4) << 3);
   const uint32_t cV = (lane >> 3) & 1;
   const int R = G * p.q_len;  // query rows of a unit: row i = token i / G, head i % G
+  const int rbase = kRS ? 8 * warp : 0;  // row-split: this warp's row tile
+  if (kRS && warp >= kRT) return;        // (no rows: not counted by the stage barriers)
   bool alive = true;  // false once one of this warp's waits gave up
   int i_base = 0;     // CTA-local index of the unit's first page
   int cu = 0;         // units of this CTA done so far
@@ -744,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT>())) paged_
   auto load_q = [&](const Walk& u) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int i = 8 * nt + gid;
+      const int i = rbase + 8 * nt + gid;
       const bool live = i < R;
       const int t = live ? i / G : 0, g = live ? i - t * G : 0;
       const __nv_bfloat16* qrow =
@@ -767,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT>())) paged_
   // keys a column of the fragment (query row 8 nt + 2 tig + c) sees fewer than the last
   // key of the context: q_len - 1 - its token (0 for single-token decode)
   auto key_shift = [&](int nt, int c) {
-    const int i = 8 * nt + 2 * tig + c;
+    const int i = rbase + 8 * nt + 2 * tig + c;
     return i < R ? p.q_len - 1 - i / G : 0;
   };
   Cursor cur;
@@ -846,11 +871,13 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT>())) paged_
     int bad = 0;
 
     // this warp's pages of the unit: CTA-local index i = i_base + j with i % kNW == warp
-    for (int j = (warp - i_base % kNW + kNW) % kNW; j < npg && alive; j += kNW) {
+    // (row-split: every page, from the one ring in page order)
+    for (int j = kRS ? 0 : (warp - i_base % kNW + kNW) % kNW; j < npg && alive;
+         j += kRS ? 1 : kNW) {
       const int i = i_base + j;
       const int li = i / kNW;
-      const int s = warp * SPW + li % SPW;
-      if (!mbar_wait(&full[s], (li / SPW) & 1, p.wait_ns)) {
+      const int s = kRS ? i % S : warp * SPW + li % SPW;
+      if (!mbar_wait(&full[s], kRS ? (i / S) & 1 : (li / SPW) & 1, p.wait_ns)) {
         alive = false;
         record_status(p.dev_status, PGQA_ETIMEOUT);
         break;
@@ -1025,7 +1052,72 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT>())) paged_
       }
     }
     const bool poisoned_w = __any_sync(0xffffffffu, bad != 0) || !__all_sync(0xffffffffu, alive);
-    constexpr int kBufs = C::kMergeBufs;
+    if constexpr (kRS) {
+      // row-split: this warp holds its rows' whole state for the unit's pages in this
+      // CTA: the output, or this CTA's partial and a ticket per (unit, row tile)
+      const int nseg = unit_segments(w, chunk);
+      const int slot = w.S <= r0 ? 0 : 1;
+      const float vsc = kFp8 ? __ldg(p.v_scale + w.h) : 1.f;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int i = rbase + 2 * tig + c;  // this thread's rows: columns c of the tile
+        const float M = m_run[0][c], l = l_run[0][c];
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        if (i < R) {
+          if (nseg == 1) {
+            __nv_bfloat16* orow = p.out + epi.out_row(w.b, w.h, i) * D;
+#pragma unroll
+            for (int dc = 0; dc < C::kNkc; ++dc) {
+              int d0, d1;
+              if constexpr (!kFp8) {
+                d0 = 16 * dc + gid;
+                d1 = d0 + 8;
+              } else {
+                d0 = 16 * gid + 2 * dc;
+                d1 = d0 + 1;
+              }
+              const float f = poisoned_w ? 0.f : inv * vsc;
+              orow[d0] = __float2bfloat16_rn(acc[dc][0][c] * f);
+              orow[d1] = __float2bfloat16_rn(acc[dc][0][2 + c] * f);
+            }
+            if (gid == 0 && p.lse)
+              p.lse[epi.out_row(w.b, w.h, i)] =
+                  poisoned_w ? -INFINITY : (M + log2f(l)) * kLn2;
+          } else {
+            const size_t ps = (static_cast<size_t>(blockIdx.x) * 2 + slot) * kRows + i;
+            float* po = p.part_o + ps * D;
+#pragma unroll
+            for (int dc = 0; dc < C::kNkc; ++dc) {
+              int d0, d1;
+              if constexpr (!kFp8) {
+                d0 = 16 * dc + gid;
+                d1 = d0 + 8;
+              } else {
+                d0 = 16 * gid + 2 * dc;
+                d1 = d0 + 1;
+              }
+              po[d0] = acc[dc][0][c] * inv;
+              po[d1] = acc[dc][0][2 + c] * inv;
+            }
+            if (gid == 0) p.part_lse[ps] = poisoned_w ? INFINITY : M + log2f(l);
+          }
+        }
+      }
+      if (nseg > 1) {
+        __syncwarp();  // every lane's partial writes are issued before the ticket
+        bool last = false;
+        if (lane == 0) last = ticket_last(p.counters + (w.b * Hkv + w.h) * kNW + warp, nseg);
+        last = __shfl_sync(0xffffffffu, last, 0);
+        __syncwarp();  // the lanes' reads of the partials come after lane 0's acquire
+        if (last)
+          merge_partials<D, kFp8, NT, kRS>(epi, w.b, w.h, w.S, w.P, chunk, lane, 32, rbase,
+                                           rbase + 8);
+      }
+      cur = nxt;
+      ++cu;
+      continue;
+    }
+    constexpr int kBufs = C::kMergeBufs > 0 ? C::kMergeBufs : 1;
     const int mb = cu % kBufs;
     if (cu >= kBufs &&
         !__all_sync(0xffffffffu, mbar_wait(&merge_free[mb], ((cu / kBufs) - 1) & 1, p.wait_ns))) {
@@ -1082,9 +1174,9 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT>())) paged_
   }
 }
 
-template <int D, bool kFp8, int NT>
+template <int D, bool kFp8, int NT, bool kRS = false>
 pgqa_status_t launch_variant(const DecodeArgs& a, const DecodePlan& plan) {
-  using C = Cfg<D, kFp8, NT>;
+  using C = Cfg<D, kFp8, NT, kRS>;
   const CUtensorMapDataType dt =
       kFp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.num_kv_heads * a.block_size;
@@ -1095,7 +1187,7 @@ pgqa_status_t launch_variant(const DecodeArgs& a, const DecodePlan& plan) {
       !tensor_map_2d(&vmap, a.v_cache, dt, D, rows, C::kRowBytes, 128 / C::kElem, box_rows,
                      CU_TENSOR_MAP_SWIZZLE_128B))
     return PGQA_ECUDA;
-  if (!smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<D, kFp8, NT>),
+  if (!smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<D, kFp8, NT, kRS>),
                        C::kSmem))
     return PGQA_ECUDA;
   DecodeParams p;
@@ -1128,7 +1220,8 @@ pgqa_status_t launch_variant(const DecodeArgs& a, const DecodePlan& plan) {
   ap.value = static_cast<const uint4*>(a.new_value);
   ap.k_cache = static_cast<uint8_t*>(const_cast<void*>(a.k_cache));
   ap.v_cache = static_cast<uint8_t*>(const_cast<void*>(a.v_cache));
-  if (launch_after_previous(paged_decode_kernel<D, kFp8, NT>, dim3(plan.grid), dim3(kThreads),
+  if (launch_after_previous(paged_decode_kernel<D, kFp8, NT, kRS>, dim3(plan.grid),
+                            dim3(kThreads),
                             C::kSmem, a.stream, kmap, vmap, p, ap) != cudaSuccess)
     return PGQA_ECUDA;
   return cudaPeekAtLastError() == cudaSuccess ? PGQA_OK : PGQA_ECUDA;
@@ -1153,13 +1246,13 @@ void set_decode_wait_limit_ns(unsigned long long ns) {
 
 int decode_row_tiles(int q_len, int group) {
   const int rows = q_len * group;
-  return rows <= 8 ? 1 : rows <= 24 ? 3 : 0;
+  return rows <= 8 ? 1 : rows <= 8 * kNW ? kNW : 0;
 }
 
 int decode_ctas_per_sm(int head_dim, int cache_dtype, int row_tiles) {
-  if (row_tiles == 3) {
-    if (cache_dtype == PGQA_DTYPE_E4M3) return ctas_per_sm<128, true, 3>();
-    return head_dim == 64 ? ctas_per_sm<64, false, 3>() : ctas_per_sm<128, false, 3>();
+  if (row_tiles == kNW) {  // row-split
+    if (cache_dtype == PGQA_DTYPE_E4M3) return ctas_per_sm<128, true, 1, true>();
+    return head_dim == 64 ? ctas_per_sm<64, false, 1, true>() : ctas_per_sm<128, false, 1, true>();
   }
   if (cache_dtype == PGQA_DTYPE_E4M3) return ctas_per_sm<128, true>();
   return head_dim == 64 ? ctas_per_sm<64, false>() : ctas_per_sm<128, false>();
@@ -1173,19 +1266,21 @@ DecodePlan decode_plan(int num_seqs, int num_kv_heads, int head_dim, int cache_d
   const size_t units = static_cast<size_t>(num_seqs > 0 ? num_seqs : 0) *
                        static_cast<size_t>(num_kv_heads > 0 ? num_kv_heads : 0);
   const size_t slots = static_cast<size_t>(plan.grid) * 2 * 8 * row_tiles;
+  // one ticket per unit, or per (unit, row tile) in the row-split form
+  const size_t tickets = units * (row_tiles == kNW ? kNW : 1);
   plan.counters_off = 0;
-  plan.lse_off = align256(units * sizeof(int));
+  plan.lse_off = align256(tickets * sizeof(int));
   plan.o_off = plan.lse_off + align256(slots * sizeof(float));
   plan.bytes = plan.o_off + align256(slots * static_cast<size_t>(head_dim) * sizeof(float));
   return plan;
 }
 
 bool decode_prepare() {
-  return smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<128, false, 1>),
+  return smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<128, false, 1, false>),
                          Cfg<128, false>::kSmem) &&
-         smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<64, false, 1>),
+         smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<64, false, 1, false>),
                          Cfg<64, false>::kSmem) &&
-         smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<128, true, 1>),
+         smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<128, true, 1, false>),
                          Cfg<128, true>::kSmem);
 }
 
@@ -1197,12 +1292,12 @@ pgqa_status_t launch_paged_decode(const DecodeArgs& a, const DecodePlan& plan) {
     } else if (a.cache_dtype == PGQA_DTYPE_E4M3) {
       if (a.head_dim == 128) return launch_variant<128, true, 1>(a, plan);
     }
-  } else if (plan.row_tiles == 3) {
+  } else if (plan.row_tiles == kNW) {
     if (a.cache_dtype == PGQA_DTYPE_BF16) {
-      if (a.head_dim == 128) return launch_variant<128, false, 3>(a, plan);
-      if (a.head_dim == 64) return launch_variant<64, false, 3>(a, plan);
+      if (a.head_dim == 128) return launch_variant<128, false, 1, true>(a, plan);
+      if (a.head_dim == 64) return launch_variant<64, false, 1, true>(a, plan);
     } else if (a.cache_dtype == PGQA_DTYPE_E4M3) {
-      if (a.head_dim == 128) return launch_variant<128, true, 3>(a, plan);
+      if (a.head_dim == 128) return launch_variant<128, true, 1, true>(a, plan);
     }
   }
   return PGQA_EUNSUPPORTED;

@@ -96,11 +96,13 @@ struct DecodeArgs {
 // kv-head) and two partial-result slots per CTA.
 struct DecodePlan {
   int grid;
-  int row_tiles;  // 8-row tiles of query rows per unit the kernel variant holds (1 or 3)
+  int row_tiles;  // 8-row tiles of query rows per unit: 1, or 4 (the row-split form)
   size_t counters_off, lse_off, o_off, bytes;
 };
-// 8-row tiles the decode kernel needs for q_len x group query rows per unit: 1 (up to 8
-// rows), 3 (up to 24), or 0 when the decode kernel does not take that many
+// 8-row tiles the decode kernel holds for q_len x group query rows per unit: 1 (up to 8
+// rows, one tile per warp, warps splitting the pages), 4 (up to 32 rows, the row-split
+// form: one tile per consumer warp, every warp reading every page), or 0 when the decode
+// kernel does not take that many
 int decode_row_tiles(int q_len, int group);
 int decode_ctas_per_sm(int head_dim, int cache_dtype, int row_tiles = 1);
 DecodePlan decode_plan(int num_seqs, int num_kv_heads, int head_dim, int cache_dtype,

@@ -5,8 +5,9 @@ into the cache: token t of a sequence with L cached tokens attends keys 0 .. L -
 The oracle is the chunked-prefill one (each sequence's chunk is its last q_len tokens).
 Small cases are compared in full for q_len 1-8, every group size, head_dim 64 and 128,
 bf16 and E4M3 caches and 8/16/32-token blocks, with contexts that end on and off page
-edges and contexts equal to q_len. When q_len x group exceeds 24 query rows per
-(sequence, kv-head) the call runs on the prefill kernel; the same comparisons cover it.
+edges and contexts equal to q_len: up to 8 query rows per (sequence, kv-head) run the
+decode kernel as a plain decode does, up to 32 its row-split form, and more run on the
+prefill kernel; the same comparisons cover all three.
 Also: repeat calls are bit-identical (the split-merge counters reset themselves), empty
 and too-short contexts, and the full speculative-verification batch on sampled rows."""
 import numpy as np
@@ -132,9 +133,22 @@ def test_repeat_calls_identical_and_counters_reset():
         run.decode()
     assert run.status_code() == 0
     assert torch.equal(first[0], run.out) and torch.equal(first[1], run.lse)
-    nctr = 20 * 8
+    nctr = 20 * 8 * 4  # a ticket per (unit, row tile) in the row-split form
     assert int(run.ws[: 4 * nctr].view(torch.int32).abs().sum()) == 0
     run.compare("repeat calls")
+
+
+@pytest.mark.parametrize("q_len,G", [(2, 4), (5, 4)])
+def test_unit_parts_where_a_draft_sees_no_key(q_len, G):
+    """Contexts of 33 tokens: a unit is 3 pages and the last holds key 32 alone, which
+    the earlier drafts do not attend. The stream-K ranges (at least 8 pages) cut units,
+    so some thread block's part of a unit is that last page only, where those rows see
+    no key: its partial must be zero with lse -inf, not NaN (both the plain scheme, 8
+    rows, and the row-split form, 20 rows)."""
+    run = MultiRun([33] * 300, q_len, 2 * G, 2, 128, seed=680 + q_len)
+    run.decode()
+    assert run.status_code() == 0
+    run.compare(f"parts without keys q_len={q_len} G={G}")
 
 
 def test_empty_and_too_short_contexts():
