@@ -62,6 +62,12 @@ def _kernel_hash(files):
     return h.hexdigest()[:16]
 
 
+DECODE_FILES = ["paged_kv_gqa_10_gb300/csrc/decode.cu", "paged_kv_gqa_10_gb300/csrc/ptx.cuh"]
+PREFILL_FILES = ["paged_kv_gqa_10_gb300/csrc/prefill.cu", "paged_kv_gqa_10_gb300/csrc/tc.cuh",
+                 "paged_kv_gqa_10_gb300/csrc/ptx.cuh"]
+KV_WRITE_FILES = ["paged_kv_gqa_10_gb300/csrc/kv_cache.cu", "paged_kv_gqa_10_gb300/csrc/ptx.cuh"]
+
+
 def _profile_traffic(name, files):
     """Per-launch DRAM bytes from a committed ncu summary, if its kernel hash
     still matches the sources (else None: the counters are stale)."""
@@ -574,8 +580,6 @@ def measure_prefill(args, dev):
     tflops = flops / (p_ms * 1e-3) / 1e12
     _, bf16_peak, kind = _peaks()
     kv_bytes = 2 * 2 * (key.numel() * 2)  # K and V: read from the input, written to the cache
-    files = ["paged_kv_gqa_10_gb300/csrc/prefill.cu", "paged_kv_gqa_10_gb300/csrc/tc.cuh",
-             "paged_kv_gqa_10_gb300/csrc/ptx.cuh"]
     return {
         "workload": "varlen causal prefill: 16 seqs, L U[128,2048] (T=%d), Hq=32, Hkv=8, D=128" % T,
         "value": tflops, "unit": "TFLOP/s", "ms": p_ms, "launches_timed": n,
@@ -584,9 +588,10 @@ def measure_prefill(args, dev):
         "roofline": {"bound": "tensor", "kernel": "paged_prefill_kernel<128>", "achieved": tflops,
                      "peak": bf16_peak, "unit": "TFLOP/s", "frac": tflops / bf16_peak,
                      "peak_kind": kind + " bf16 burst (cuBLAS)",
-                     "traffic": _profile_traffic("prefill_varlen.json", files)},
+                     "traffic": _profile_traffic("prefill_varlen.json", PREFILL_FILES)},
         "kv_cache_write": {"ms": w_ms, "bytes": kv_bytes,
-                           "GB/s": kv_bytes / (w_ms * 1e-3) / 1e9},
+                           "GB/s": kv_bytes / (w_ms * 1e-3) / 1e9,
+                           "traffic": _profile_traffic("kv_cache_write.json", KV_WRITE_FILES)},
     }
 
 
@@ -670,10 +675,14 @@ def measure_cached_prefix(args, dev, names=("chunked_prefill", "speculative_veri
         if name == "chunked_prefill":
             entry["roofline"] = {"bound": "tensor", "achieved": tflops, "peak": bf16_peak,
                                  "unit": "TFLOP/s", "frac": tflops / bf16_peak,
-                                 "peak_kind": kind + " bf16 burst (cuBLAS)"}
+                                 "peak_kind": kind + " bf16 burst (cuBLAS)",
+                                 "traffic": _profile_traffic("prefill_chunked.json",
+                                                             PREFILL_FILES)}
         else:
             entry["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                                 "frac": gbs / hbm, "peak_kind": kind}
+                                 "frac": gbs / hbm, "peak_kind": kind,
+                                 "traffic": _profile_traffic("decode_spec_verify.json",
+                                                             DECODE_FILES)}
         res[name] = entry
         del caches
         torch.cuda.empty_cache()
@@ -724,7 +733,8 @@ def measure_e4m3_prefill(args, dev):
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16_peak,
                          "unit": "TFLOP/s", "frac": tflops / bf16_peak,
                          "peak_kind": kind + " bf16 burst (cuBLAS); the MMAs run on f16 "
-                                             "operands at the same nominal rate"}}
+                                             "operands at the same nominal rate",
+                         "traffic": _profile_traffic("prefill_e4m3_varlen.json", PREFILL_FILES)}}
 
 
 def measure_window_decode(args, dev, window=2048):
@@ -770,7 +780,8 @@ def measure_window_decode(args, dev, window=2048):
     return {"workload": f"sliding-window decode, window {window}: " + inp.name, "ms": ms,
             "kv_bytes": kvb, "KV GB/s": gbs,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                         "frac": gbs / hbm, "peak_kind": kind}}
+                         "frac": gbs / hbm, "peak_kind": kind,
+                         "traffic": _profile_traffic("decode_window.json", DECODE_FILES)}}
 
 
 def _oracle_parity(inp, gpu_res):
@@ -810,7 +821,6 @@ def decode_entry(name, inp, m, world):
     alg = b.alg_bytes_fused - shared
     achieved = alg / (m["dec_ms"] * 1e-3) / 1e9
     D = inp.head_dim
-    dec_files = ["paged_kv_gqa_10_gb300/csrc/decode.cu", "paged_kv_gqa_10_gb300/csrc/ptx.cuh"]
     e = {"workload": DECODE_WORKLOADS[name][1],
          "ms_per_step": m["ms_graph"],
          "GB/s": job_value(kvb, world, m["ms_graph"]),
@@ -820,7 +830,7 @@ def decode_entry(name, inp, m, world):
                       "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                       "frac": achieved / hbm_peak, "peak_kind": peak_kind,
                       "alg_bytes_per_launch": alg, "launch_ms": m["dec_ms"],
-                      "traffic": _profile_traffic(f"decode_{name}.json", dec_files)}}
+                      "traffic": _profile_traffic(f"decode_{name}.json", DECODE_FILES)}}
     if shared:
         e["unique_kv_bytes_per_step"] = unique
         e["unique GB/s"] = job_value(unique, world, m["ms_graph"])

@@ -39,7 +39,9 @@
 //    ahead.
 //  - Math per 16-token page on the warp-level tensor path (mma.m16n8k16):
 //      S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8]   (tokens fill M = 16)
-//      online softmax on the S^T fragment (column = query head)
+//      online softmax on the S^T fragment (column = query head), with a lazy
+//      reference: the max reduction and the rescale of l and O run only on pages
+//      where a score exceeds the column's reference by more than 2^8
 //      P^T fragment -> B operand with movmatrix (an 8x8 transpose in registers)
 //      O^T[D x 8] += V^T[D x 16] . P^T[16 x 8]            (V^T via ldmatrix.trans)
 //    G <= 8 heads sit in N = 8; padded heads have q = 0 and are never stored.
@@ -53,8 +55,8 @@
 //    (each fragment column has its own causal limit). Up to 8 rows run as above. Up to
 //    32 run in the row-split form: consumer warp w holds rows 8w .. 8w+7 and reads every
 //    page, from one ring filled in page order whose stages every warp with rows frees;
-//    each warp finishes its own rows (no merge warp), with a ticket per (unit, row tile)
-//    for units cut by range boundaries.
+//    each warp hands its rows' state to the merge warp, which finishes the units as in
+//    the plain form.
 //  - Every wait is bounded; a warp whose wait gives up records PGQA_ETIMEOUT, stops
 //    computing, but keeps taking part in every CTA barrier, so nothing can hang.
 #include <cuda_bf16.h>
@@ -72,6 +74,9 @@ constexpr int kNW = 4;  // consumer warps per CTA
 constexpr int kWarpProd = kNW, kWarpMerge = kNW + 1;
 constexpr int kThreads = (kNW + 2) * 32;
 constexpr int kMinChunk = 8;  // pages per CTA range, at least
+// online softmax: a column's reference max moves only when a score exceeds it by more
+// than this (log2 units), so P <= 256 and most pages skip the max reduction and rescale
+constexpr float kLazyLog2 = 8.f;
 constexpr int kYRing = 256;   // TMA row coordinates fetched ahead of issue
 static_assert(kYRing >= 64 + 32, "the fetch lookahead must fit the ring");
 constexpr int kScanSlots = kThreads / 32 + 1;  // one per warp, then the found unit start
@@ -135,25 +140,35 @@ struct Cfg {
       kRS ? 0
           : NT > 1 ? (kStageBytes >= 8192 ? 5 : 8)
                    : (kStageBytes >= 8192 ? 2 : kFp8 ? 5 : 16384 / kStageBytes);
-  // unit states in flight to the merge warp (none in the row-split form: each warp
-  // finishes its own rows)
-  static constexpr int kMergeBufs = kRS ? 0 : (kFp8 || NT > 1) ? 1 : 2;
-  // the row-split form: one ring of about 96 KB, filled in page order
-  static constexpr int kStages = kRS ? 98304 / kStageBytes : kNW * kStagesPerWarp;
+  // unit states in flight to the merge warp
+  static constexpr int kMergeBufs = (kRS || kFp8 || NT > 1) ? 1 : 2;
+  // the row-split form: one ring of 88 KB, filled in page order
+  static constexpr int kStages = kRS ? 90112 / kStageBytes : kNW * kStagesPerWarp;
   static constexpr int kNkc = D / 16;              // 16-wide chunks of head_dim
   static constexpr int kRing = kStages * kStageBytes;
-  static constexpr int kMerge = kNW * kRows * D * 4;  // per-warp O of one unit
-  static constexpr int kOffMerge = kRing;             // [bufs] by unit parity
-  static constexpr int kOffMl = kOffMerge + kMergeBufs * kMerge;  // [bufs][kNW][rows][2] float
-  static constexpr int kOffBar = kOffMl + kMergeBufs * kNW * kRows * 2 * 4;  // full[S], empty[S],
+  // a merge buffer holds every consumer warp's O of one unit, [kNW][kRows] rows of D
+  // floats, or in the row-split form each row once (the warp holding it wrote it),
+  // [kRows] rows of D + 4 floats (the padding spreads a warp's stores over the banks)
+  static constexpr int kStateWarps = kRS ? 1 : kNW;
+  static constexpr int kLd = kRS ? D + 4 : D;
+  static constexpr int kMergeFloats = kStateWarps * kRows * kLd;
+  static constexpr int kMlFloats = kStateWarps * kRows * 2;  // (m, l) per state row
+  static constexpr int kOffMerge = kRing;                    // [bufs] by unit parity
+  static constexpr int kOffMl = kOffMerge + kMergeBufs * kMergeFloats * 4;
+  static constexpr int kOffBar = kOffMl + kMergeBufs * kMlFloats * 4;  // full[S], empty[S],
                                                                       // unit_done[2], merge_free[2]
   static constexpr int kOffMeta = kOffBar + (2 * kStages + 4) * 8;    // [S] int
-  static constexpr int kOffY = kOffMeta + kStages * 4;                // [kYRing] int
+  static constexpr int kOffY = (kOffMeta + kStages * 4 + 15) / 16 * 16;  // [kYRing] int
   static constexpr int kOffY2 = kOffY + kYRing * 4;                   // [kYRing] int (block 8)
   static constexpr int kOffMisc = kOffY2 + kYRing * 4;                // 32 ints, kScanSlots int64
   static constexpr int kOffRuns = kOffMisc + 32 * 4 + kScanSlots * 8;   // Run[3]
   static constexpr int kSmem = 1024 + kOffRuns + 3 * 48;
   static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle rows");
+  static_assert(!kRS || 227 * 1024 / (kSmem + 1024) >= 2, "row-split: two CTAs per SM");
+  static_assert(kStageBytes % 1024 == 0 && kOffMerge % 16 == 0 && kOffMl % 16 == 0 &&
+                    kOffBar % 8 == 0 && kOffY % 16 == 0 && (kOffMisc + 32 * 4) % 8 == 0 &&
+                    kOffRuns % 8 == 0 && (kLd * 4) % 16 == 0,
+                "shared-memory regions must be aligned for their types");
 };
 
 // CTAs of one decode kernel resident per SM (the grid is this times the SM count).
@@ -300,8 +315,9 @@ __device__ __forceinline__ int plan_runs(const DecodeParams& p, const Walk& w0, 
   return 3;
 }
 
-__device__ __forceinline__ void bar_consumers() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kNW * 32) : "memory");
+// The consumer warps' barrier: all kNW of them, or those with rows (row-split).
+__device__ __forceinline__ void bar_consumers(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
 // What a unit epilogue reads and writes (passed by value: the epilogue functions are
@@ -323,12 +339,14 @@ struct Epi {
 
 // Unit epilogue, run by nt threads (t = this thread's index among them).
 // combine_unit: the consumer warps' states of unit (b, h) from the merge buffer
-// (M = max m_w, l = sum l_w 2^(m_w - M), O likewise) -> the output, or, for a unit cut
-// by range boundaries (nseg > 1), this CTA's partial (slot 0 or 1).
-template <int D, bool kFp8, int NT>
+// (M = max m_w, l = sum l_w 2^(m_w - M), O likewise; in the row-split form a row has
+// one state) -> the output, or, for a unit cut by range boundaries (nseg > 1), this
+// CTA's partial (slot 0 or 1).
+template <int D, bool kFp8, int NT, bool kRS = false>
 __device__ __noinline__ void combine_unit(const Epi e, int b, int h, int nseg, int slot,
                                           const float* wob, const float* wmlb, int t, int nt) {
-  constexpr int kRows = Cfg<D, kFp8, NT>::kRows;
+  using C = Cfg<D, kFp8, NT, kRS>;
+  constexpr int kRows = C::kRows;
   const int R = e.group * e.q_len;  // the unit's query rows (<= kRows)
   constexpr int kChunks = D / 8;  // 8 consecutive d per work item
   const float vsc = kFp8 ? __ldg(e.v_scale + h) : 1.f;
@@ -337,17 +355,18 @@ __device__ __noinline__ void combine_unit(const Epi e, int b, int h, int nseg, i
     float M = -INFINITY;
     bool poisoned = false;
 #pragma unroll
-    for (int ww = 0; ww < kNW; ++ww) {
+    for (int ww = 0; ww < C::kStateWarps; ++ww) {
       M = fmaxf(M, wmlb[(ww * kRows + g) * 2]);
       poisoned |= isnan(wmlb[(ww * kRows + g) * 2 + 1]);
     }
     float lsum = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int ww = 0; ww < kNW; ++ww) {
+    for (int ww = 0; ww < C::kStateWarps; ++ww) {
       const float mw = wmlb[(ww * kRows + g) * 2];
       const float wt = mw == -INFINITY ? 0.f : ex2(mw - M);
       lsum += wmlb[(ww * kRows + g) * 2 + 1] * wt;
-      const float4* src = reinterpret_cast<const float4*>(wob + (ww * kRows + g) * D + cc * 8);
+      const float4* src =
+          reinterpret_cast<const float4*>(wob + (ww * kRows + g) * C::kLd + cc * 8);
       const float4 x = src[0], y = src[1];
       o[0] += x.x * wt; o[1] += x.y * wt; o[2] += x.z * wt; o[3] += x.w * wt;
       o[4] += y.x * wt; o[5] += y.y * wt; o[6] += y.z * wt; o[7] += y.w * wt;
@@ -462,9 +481,9 @@ __device__ __forceinline__ int unit_segments(const Walk& w, long long chunk) {
 }
 
 // The merge warp: the epilogue of every unit of this CTA's range but the last (the
-// consumer warps, which have nothing left to stream then, do that one with 128
-// threads), so the consumers hand a unit over and go straight on to the next.
-template <int D, bool kFp8, int NT>
+// consumer warps, which have nothing left to stream then, do that one together), so
+// the consumers hand a unit over and go straight on to the next.
+template <int D, bool kFp8, int NT, bool kRS>
 __device__ __forceinline__ void merge_units(const DecodeParams& p, const Epi epi,
                                             const Run* runs, int nruns, long long r0,
                                             long long chunk, const float* wo,
@@ -476,7 +495,7 @@ __device__ __forceinline__ void merge_units(const DecodeParams& p, const Epi epi
   for (int cu = 0;; ++cu) {
     const Walk w = cur.w;
     if (!cur.next(p, runs)) return;  // w is the range's last unit
-    using C = Cfg<D, kFp8, NT>;
+    using C = Cfg<D, kFp8, NT, kRS>;
     constexpr int kBufs = C::kMergeBufs;
     const int mb = cu % kBufs;
     if (!__all_sync(0xffffffffu, mbar_wait(&unit_done[mb], (cu / kBufs) & 1, p.wait_ns))) {
@@ -484,9 +503,8 @@ __device__ __forceinline__ void merge_units(const DecodeParams& p, const Epi epi
       return;
     }
     const int nseg = unit_segments(w, chunk);
-    combine_unit<D, kFp8, NT>(epi, w.b, w.h, nseg, w.S <= r0 ? 0 : 1,
-                              wo + mb * (kNW * C::kRows * D), wml + mb * (kNW * C::kRows * 2),
-                              lane, 32);
+    combine_unit<D, kFp8, NT, kRS>(epi, w.b, w.h, nseg, w.S <= r0 ? 0 : 1,
+                                   wo + mb * C::kMergeFloats, wml + mb * C::kMlFloats, lane, 32);
     __syncwarp();  // every lane has read the buffer and issued its writes
     if (lane == 0) mbar_arrive(&merge_free[mb]);
     if (nseg > 1) {
@@ -494,7 +512,7 @@ __device__ __forceinline__ void merge_units(const DecodeParams& p, const Epi epi
       if (lane == 0) last = ticket_last(p.counters + w.b * p.num_kv_heads + w.h, nseg);
       last = __shfl_sync(0xffffffffu, last, 0);
       __syncwarp();  // the lanes' reads of the partials come after lane 0's acquire
-      if (last) merge_partials<D, kFp8, NT>(epi, w.b, w.h, w.S, w.P, chunk, lane, 32);
+      if (last) merge_partials<D, kFp8, NT, kRS>(epi, w.b, w.h, w.S, w.P, chunk, lane, 32);
     }
   }
 }
@@ -596,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
       mbar_init(&empty[s], kRS ? kRT : 1);  // row-split: every warp with rows frees it
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&unit_done[s], kNW);
+      mbar_init(&unit_done[s], kRS ? kRT : kNW);
       mbar_init(&merge_free[s], 1);
     }
     fence_mbar_init();
@@ -745,8 +763,8 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
 
   // ================================================================ merge warp
   if (warp == kWarpMerge) {
-    if constexpr (!kRS)
-      merge_units<D, kFp8, NT>(p, epi, runs, nruns, r0, chunk, wo, wml, unit_done, merge_free);
+    merge_units<D, kFp8, NT, kRS>(p, epi, runs, nruns, r0, chunk, wo, wml, unit_done,
+                                  merge_free);
     return;
   }
 
@@ -962,30 +980,43 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
         if (gid >= nv1 || gid < lo) s1 = -INFINITY;
         if (gid + 8 >= nv0 || gid + 8 < lo) s2 = -INFINITY;
         if (gid + 8 >= nv1 || gid + 8 < lo) s3 = -INFINITY;
-        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+        // m_run is the column's reference: every score seen so far is at most
+        // m_run + kLazyLog2. Only a score above that (the first page with a key, or a
+        // jump in the maximum) moves it, to the maximum so far, and rescales l and O;
+        // otherwise P = 2^(s - m_run) <= 2^kLazyLog2 as is. Exact either way: l and O
+        // share the reference, and lse = m_run + log2 l.
+        const bool grow = fmaxf(s0, s2) > m_run[nt][0] + kLazyLog2 ||
+                          fmaxf(s1, s3) > m_run[nt][1] + kLazyLog2;
+        if (__any_sync(0xffffffffu, grow)) {
+          float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+          for (int o = 4; o < 32; o <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+          }
+          const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
+          // a column that has seen no key yet (a page past a draft token's last key)
+          // keeps m = -inf; 0 as the reference then gives 2^-inf = 0 instead of NaN
+          const float rf0 = mn0 == -INFINITY ? 0.f : mn0, rf1 = mn1 == -INFINITY ? 0.f : mn1;
+          const float al0 = ex2(m_run[nt][0] - rf0), al1 = ex2(m_run[nt][1] - rf1);
+          m_run[nt][0] = mn0;
+          m_run[nt][1] = mn1;
+          l_run[nt][0] *= al0;
+          l_run[nt][1] *= al1;
+#pragma unroll
+          for (int dc = 0; dc < C::kNkc; ++dc) {
+            acc[dc][nt][0] *= al0;
+            acc[dc][nt][1] *= al1;
+            acc[dc][nt][2] *= al0;
+            acc[dc][nt][3] *= al1;
+          }
         }
-        const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
-        // a column that has seen no key yet (a page past a draft token's last key) keeps
-        // m = -inf; 0 as the reference then gives 2^-inf = 0 instead of NaN
-        const float rf0 = mn0 == -INFINITY ? 0.f : mn0, rf1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = ex2(m_run[nt][0] - rf0), al1 = ex2(m_run[nt][1] - rf1);
-        m_run[nt][0] = mn0;
-        m_run[nt][1] = mn1;
+        const float rf0 = m_run[nt][0] == -INFINITY ? 0.f : m_run[nt][0];
+        const float rf1 = m_run[nt][1] == -INFINITY ? 0.f : m_run[nt][1];
         const float p0v = ex2(s0 - rf0), p1v = ex2(s1 - rf1), p2v = ex2(s2 - rf0),
                     p3v = ex2(s3 - rf1);
-        l_run[nt][0] = l_run[nt][0] * al0 + (p0v + p2v);
-        l_run[nt][1] = l_run[nt][1] * al1 + (p1v + p3v);
-#pragma unroll
-        for (int dc = 0; dc < C::kNkc; ++dc) {
-          acc[dc][nt][0] *= al0;
-          acc[dc][nt][1] *= al1;
-          acc[dc][nt][2] *= al0;
-          acc[dc][nt][3] *= al1;
-        }
+        l_run[nt][0] += p0v + p2v;
+        l_run[nt][1] += p1v + p3v;
         pb0[nt] = movmatrix_t(kFp8 ? pack_f16(p0v, p1v) : pack_bf16(p0v, p1v));
         pb1[nt] = movmatrix_t(kFp8 ? pack_f16(p2v, p3v) : pack_bf16(p2v, p3v));
       }
@@ -1052,82 +1083,19 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
       }
     }
     const bool poisoned_w = __any_sync(0xffffffffu, bad != 0) || !__all_sync(0xffffffffu, alive);
-    if constexpr (kRS) {
-      // row-split: this warp holds its rows' whole state for the unit's pages in this
-      // CTA: the output, or this CTA's partial and a ticket per (unit, row tile)
-      const int nseg = unit_segments(w, chunk);
-      const int slot = w.S <= r0 ? 0 : 1;
-      const float vsc = kFp8 ? __ldg(p.v_scale + w.h) : 1.f;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int i = rbase + 2 * tig + c;  // this thread's rows: columns c of the tile
-        const float M = m_run[0][c], l = l_run[0][c];
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        if (i < R) {
-          if (nseg == 1) {
-            __nv_bfloat16* orow = p.out + epi.out_row(w.b, w.h, i) * D;
-#pragma unroll
-            for (int dc = 0; dc < C::kNkc; ++dc) {
-              int d0, d1;
-              if constexpr (!kFp8) {
-                d0 = 16 * dc + gid;
-                d1 = d0 + 8;
-              } else {
-                d0 = 16 * gid + 2 * dc;
-                d1 = d0 + 1;
-              }
-              const float f = poisoned_w ? 0.f : inv * vsc;
-              orow[d0] = __float2bfloat16_rn(acc[dc][0][c] * f);
-              orow[d1] = __float2bfloat16_rn(acc[dc][0][2 + c] * f);
-            }
-            if (gid == 0 && p.lse)
-              p.lse[epi.out_row(w.b, w.h, i)] =
-                  poisoned_w ? -INFINITY : (M + log2f(l)) * kLn2;
-          } else {
-            const size_t ps = (static_cast<size_t>(blockIdx.x) * 2 + slot) * kRows + i;
-            float* po = p.part_o + ps * D;
-#pragma unroll
-            for (int dc = 0; dc < C::kNkc; ++dc) {
-              int d0, d1;
-              if constexpr (!kFp8) {
-                d0 = 16 * dc + gid;
-                d1 = d0 + 8;
-              } else {
-                d0 = 16 * gid + 2 * dc;
-                d1 = d0 + 1;
-              }
-              po[d0] = acc[dc][0][c] * inv;
-              po[d1] = acc[dc][0][2 + c] * inv;
-            }
-            if (gid == 0) p.part_lse[ps] = poisoned_w ? INFINITY : M + log2f(l);
-          }
-        }
-      }
-      if (nseg > 1) {
-        __syncwarp();  // every lane's partial writes are issued before the ticket
-        bool last = false;
-        if (lane == 0) last = ticket_last(p.counters + (w.b * Hkv + w.h) * kNW + warp, nseg);
-        last = __shfl_sync(0xffffffffu, last, 0);
-        __syncwarp();  // the lanes' reads of the partials come after lane 0's acquire
-        if (last)
-          merge_partials<D, kFp8, NT, kRS>(epi, w.b, w.h, w.S, w.P, chunk, lane, 32, rbase,
-                                           rbase + 8);
-      }
-      cur = nxt;
-      ++cu;
-      continue;
-    }
-    constexpr int kBufs = C::kMergeBufs > 0 ? C::kMergeBufs : 1;
+    constexpr int kBufs = C::kMergeBufs;
     const int mb = cu % kBufs;
     if (cu >= kBufs &&
         !__all_sync(0xffffffffu, mbar_wait(&merge_free[mb], ((cu / kBufs) - 1) & 1, p.wait_ns))) {
       alive = false;
       if (lane == 0) record_status(p.dev_status, PGQA_ETIMEOUT);
     }
-    float* wob = wo + mb * (kNW * kRows * D);
-    float* wmlb = wml + mb * (kNW * kRows * 2);
+    float* wob = wo + mb * C::kMergeFloats;
+    float* wmlb = wml + mb * C::kMlFloats;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
+      // state rows of this thread's columns: per warp, or (row-split) the rows themselves
+      const int srow = (kRS ? rbase : warp * kRows + 8 * nt) + 2 * tig;
 #pragma unroll
       for (int dc = 0; dc < C::kNkc; ++dc) {
         int d0, d1;
@@ -1138,15 +1106,15 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
           d0 = 16 * gid + 2 * dc;
           d1 = d0 + 1;
         }
-        float* o0 = wob + (warp * kRows + 8 * nt + 2 * tig) * D;
-        float* o1 = o0 + D;
+        float* o0 = wob + srow * C::kLd;
+        float* o1 = o0 + C::kLd;
         o0[d0] = acc[dc][nt][0];
         o1[d0] = acc[dc][nt][1];
         o0[d1] = acc[dc][nt][2];
         o1[d1] = acc[dc][nt][3];
       }
       if (gid == 0) {
-        float* ml = wmlb + (warp * kRows + 8 * nt + 2 * tig) * 2;
+        float* ml = wmlb + srow * 2;
         ml[0] = m_run[nt][0];
         ml[1] = poisoned_w ? NAN : l_run[nt][0];  // NaN l marks a poisoned warp state
         ml[2] = m_run[nt][1];
@@ -1160,15 +1128,19 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
       ++cu;
       continue;
     }
-    // the range's last unit: nothing left to stream, so the consumer warps finish it
+    // the range's last unit: nothing left to stream, so the consumer warps (those with
+    // rows, in the row-split form) finish it
     const int nseg = unit_segments(w, chunk);
-    bar_consumers();
-    combine_unit<D, kFp8, NT>(epi, w.b, w.h, nseg, w.S <= r0 ? 0 : 1, wob, wmlb, tid, kNW * 32);
+    const int nthr = (kRS ? kRT : kNW) * 32;
+    bar_consumers(nthr);
+    combine_unit<D, kFp8, NT, kRS>(epi, w.b, w.h, nseg, w.S <= r0 ? 0 : 1, wob, wmlb, tid,
+                                   nthr);
     if (nseg > 1) {
-      bar_consumers();  // this CTA's partial writes are issued
+      bar_consumers(nthr);  // this CTA's partial writes are issued
       if (tid == 0) misc[1] = ticket_last(p.counters + w.b * Hkv + w.h, nseg);
-      bar_consumers();  // (and the reads below come after the acquire)
-      if (misc[1]) merge_partials<D, kFp8, NT>(epi, w.b, w.h, w.S, w.P, chunk, tid, kNW * 32);
+      bar_consumers(nthr);  // (and the reads below come after the acquire)
+      if (misc[1])
+        merge_partials<D, kFp8, NT, kRS>(epi, w.b, w.h, w.S, w.P, chunk, tid, nthr);
     }
     ++cu;
   }
@@ -1266,8 +1238,7 @@ DecodePlan decode_plan(int num_seqs, int num_kv_heads, int head_dim, int cache_d
   const size_t units = static_cast<size_t>(num_seqs > 0 ? num_seqs : 0) *
                        static_cast<size_t>(num_kv_heads > 0 ? num_kv_heads : 0);
   const size_t slots = static_cast<size_t>(plan.grid) * 2 * 8 * row_tiles;
-  // one ticket per unit, or per (unit, row tile) in the row-split form
-  const size_t tickets = units * (row_tiles == kNW ? kNW : 1);
+  const size_t tickets = units;  // one per unit
   plan.counters_off = 0;
   plan.lse_off = align256(tickets * sizeof(int));
   plan.o_off = plan.lse_off + align256(slots * sizeof(float));

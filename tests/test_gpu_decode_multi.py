@@ -133,7 +133,7 @@ def test_repeat_calls_identical_and_counters_reset():
         run.decode()
     assert run.status_code() == 0
     assert torch.equal(first[0], run.out) and torch.equal(first[1], run.lse)
-    nctr = 20 * 8 * 4  # a ticket per (unit, row tile) in the row-split form
+    nctr = 20 * 8  # a ticket per unit
     assert int(run.ws[: 4 * nctr].view(torch.int32).abs().sum()) == 0
     run.compare("repeat calls")
 
