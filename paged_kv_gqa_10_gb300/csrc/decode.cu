@@ -161,8 +161,8 @@ struct Cfg {
   static constexpr int kOffY = (kOffMeta + kStages * 4 + 15) / 16 * 16;  // [kYRing] int
   static constexpr int kOffY2 = kOffY + kYRing * 4;                   // [kYRing] int (block 8)
   static constexpr int kOffMisc = kOffY2 + kYRing * 4;                // 32 ints, kScanSlots int64
-  static constexpr int kOffRuns = kOffMisc + 32 * 4 + kScanSlots * 8;   // Run[3]
-  static constexpr int kSmem = 1024 + kOffRuns + 3 * 48;
+  static constexpr int kOffRuns = kOffMisc + 32 * 4 + kScanSlots * 8;   // Run[3], Walk w0
+  static constexpr int kSmem = 1024 + kOffRuns + 4 * 48;
   static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle rows");
   static_assert(!kRS || 227 * 1024 / (kSmem + 1024) >= 2, "row-split: two CTAs per SM");
   static_assert(kStageBytes % 1024 == 0 && kOffMerge % 16 == 0 && kOffMl % 16 == 0 &&
@@ -185,14 +185,19 @@ __device__ __forceinline__ int first_key(const DecodeParams& p, int L) {
   return p.window > 0 && L > p.window ? L - p.window : 0;
 }
 
-// Pages of sequence b the step reads (those holding keys first_key .. L-1).
-__device__ __forceinline__ int pages_of(const DecodeParams& p, int b, bool* valid = nullptr) {
-  const int L = __ldg(p.context_lens + b);
+// Pages the step reads of a sequence of context length L (those holding keys
+// first_key .. L-1); 0 for an invalid length.
+__device__ __forceinline__ int pages_of_len(const DecodeParams& p, int L, bool* valid = nullptr) {
   const int n = (L + 15) >> 4;
   const bool ok = L >= 0 && L <= p.max_context_len && (L == 0 || L >= p.q_len) &&
                   (L + p.block_size - 1) / p.block_size <= p.max_blocks_per_seq;
   if (valid) *valid = ok;
   return ok && L > 0 ? n - (first_key(p, L) >> 4) : 0;
+}
+
+// Pages of sequence b the step reads.
+__device__ __forceinline__ int pages_of(const DecodeParams& p, int b, bool* valid = nullptr) {
+  return pages_of_len(p, __ldg(p.context_lens + b), valid);
 }
 
 // Logical page of sequence b's first page read.
@@ -337,11 +342,40 @@ struct Epi {
   }
 };
 
+// This CTA's state of query row g, columns 8 cc .. 8 cc + 7, from the consumer warps'
+// states in the merge buffer (M = max m_w, l = sum l_w 2^(m_w - M), O likewise; in the
+// row-split form a row has one state); poisoned if a warp's state was.
+template <int D, bool kFp8, int NT, bool kRS>
+__device__ __forceinline__ void cta_state(const float* wob, const float* wmlb, int g, int cc,
+                                          float& M, float& lsum, float (&o)[8],
+                                          bool& poisoned) {
+  using C = Cfg<D, kFp8, NT, kRS>;
+  constexpr int kRows = C::kRows;
+  M = -INFINITY;
+  poisoned = false;
+#pragma unroll
+  for (int ww = 0; ww < C::kStateWarps; ++ww) {
+    M = fmaxf(M, wmlb[(ww * kRows + g) * 2]);
+    poisoned |= isnan(wmlb[(ww * kRows + g) * 2 + 1]);
+  }
+  lsum = 0.f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) o[q] = 0.f;
+#pragma unroll
+  for (int ww = 0; ww < C::kStateWarps; ++ww) {
+    const float mw = wmlb[(ww * kRows + g) * 2];
+    const float wt = mw == -INFINITY ? 0.f : ex2(mw - M);
+    lsum += wmlb[(ww * kRows + g) * 2 + 1] * wt;
+    const float4* src = reinterpret_cast<const float4*>(wob + (ww * kRows + g) * C::kLd + cc * 8);
+    const float4 x = src[0], y = src[1];
+    o[0] += x.x * wt; o[1] += x.y * wt; o[2] += x.z * wt; o[3] += x.w * wt;
+    o[4] += y.x * wt; o[5] += y.y * wt; o[6] += y.z * wt; o[7] += y.w * wt;
+  }
+}
+
 // Unit epilogue, run by nt threads (t = this thread's index among them).
-// combine_unit: the consumer warps' states of unit (b, h) from the merge buffer
-// (M = max m_w, l = sum l_w 2^(m_w - M), O likewise; in the row-split form a row has
-// one state) -> the output, or, for a unit cut by range boundaries (nseg > 1), this
-// CTA's partial (slot 0 or 1).
+// combine_unit: this CTA's state of unit (b, h) (cta_state) -> the output, or, for a
+// unit cut by range boundaries (nseg > 1), this CTA's partial (slot 0 or 1).
 template <int D, bool kFp8, int NT, bool kRS = false>
 __device__ __noinline__ void combine_unit(const Epi e, int b, int h, int nseg, int slot,
                                           const float* wob, const float* wmlb, int t, int nt) {
@@ -352,25 +386,9 @@ __device__ __noinline__ void combine_unit(const Epi e, int b, int h, int nseg, i
   const float vsc = kFp8 ? __ldg(e.v_scale + h) : 1.f;
   for (int it = t; it < R * kChunks; it += nt) {
     const int g = it / kChunks, cc = it % kChunks;  // g: the query row
-    float M = -INFINITY;
-    bool poisoned = false;
-#pragma unroll
-    for (int ww = 0; ww < C::kStateWarps; ++ww) {
-      M = fmaxf(M, wmlb[(ww * kRows + g) * 2]);
-      poisoned |= isnan(wmlb[(ww * kRows + g) * 2 + 1]);
-    }
-    float lsum = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int ww = 0; ww < C::kStateWarps; ++ww) {
-      const float mw = wmlb[(ww * kRows + g) * 2];
-      const float wt = mw == -INFINITY ? 0.f : ex2(mw - M);
-      lsum += wmlb[(ww * kRows + g) * 2 + 1] * wt;
-      const float4* src =
-          reinterpret_cast<const float4*>(wob + (ww * kRows + g) * C::kLd + cc * 8);
-      const float4 x = src[0], y = src[1];
-      o[0] += x.x * wt; o[1] += x.y * wt; o[2] += x.z * wt; o[3] += x.w * wt;
-      o[4] += y.x * wt; o[5] += y.y * wt; o[6] += y.z * wt; o[7] += y.w * wt;
-    }
+    float M, lsum, o[8];
+    bool poisoned;
+    cta_state<D, kFp8, NT, kRS>(wob, wmlb, g, cc, M, lsum, o, poisoned);
     // (a row that saw no key in this CTA's part of a unit, e.g. a draft token whose last
     // key lies before the part, has lsum = 0: its partial is 0 with lse -inf)
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
@@ -398,11 +416,14 @@ __device__ __noinline__ void combine_unit(const Epi e, int b, int h, int nseg, i
 // starts at page S; CTA c (range [c * chunk, ...)) keeps it in slot 0 when the unit
 // starts at or before its range (its first unit), else in slot 1 (its last). Partials
 // are taken four at a time: a group's loads are all issued before any is used, then
-// merged into a running (M, l, O).
+// merged into a running (M, l, O). With wob/wmlb (the merge buffer of this CTA's
+// state) this CTA's partial is not read back but formed from its state, with the
+// arithmetic combine_unit uses to write it, so the result is the same bit for bit.
 template <int D, bool kFp8, int NT, bool kRS = false>
 __device__ __noinline__ void merge_partials(const Epi e, int b, int h, long long S, int P,
                                             long long chunk, int t, int nt, int row0 = 0,
-                                            int row1 = 1 << 30) {
+                                            int row1 = 1 << 30, const float* wob = nullptr,
+                                            const float* wmlb = nullptr) {
   constexpr int kRows = Cfg<D, kFp8, NT, kRS>::kRows;
   const int R = min(e.group * e.q_len, row1) - row0;  // rows row0 .. row1-1 of the unit
   constexpr int kChunks = D / 8;
@@ -421,7 +442,15 @@ __device__ __noinline__ void merge_partials(const Epi e, int b, int h, long long
         const long long cta = base + k;
         ls[k] = -INFINITY;
         x[k] = y[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (cta <= c_last) {
+        if (wob != nullptr && cta == blockIdx.x) {
+          float Mo, lo, oo[8];
+          bool po;
+          cta_state<D, kFp8, NT, kRS>(wob, wmlb, g, cc, Mo, lo, oo, po);
+          const float inv = lo > 0.f ? 1.f / lo : 0.f;
+          ls[k] = po ? INFINITY : Mo + log2f(lo);
+          x[k] = make_float4(oo[0] * inv, oo[1] * inv, oo[2] * inv, oo[3] * inv);
+          y[k] = make_float4(oo[4] * inv, oo[5] * inv, oo[6] * inv, oo[7] * inv);
+        } else if (cta <= c_last) {
           const size_t ps =
               static_cast<size_t>(cta * 2 + (S <= cta * chunk ? 0 : 1)) * kRows + g;
           const float4* src = reinterpret_cast<const float4*>(e.part_o + ps * D + cc * 8);
@@ -473,6 +502,15 @@ __device__ __forceinline__ bool ticket_last(int* counter, int count) {
                : "l"(counter), "r"(static_cast<unsigned>(count - 1))
                : "memory");
   return old == static_cast<unsigned>(count - 1);
+}
+
+// Arrivals on a unit's ticket so far, read with acquire: when it shows every other CTA
+// of the unit, their partials are visible to this thread (and, through a later CTA
+// barrier, to the others).
+__device__ __forceinline__ unsigned ticket_peek(const int* counter) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+  return v;
 }
 
 // Segments of unit w over the CTA ranges, and which partial slot this CTA uses.
@@ -542,11 +580,10 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
   int* meta = reinterpret_cast<int*>(smem + C::kOffMeta);  // per stage: bad block id seen
   int* yring = reinterpret_cast<int*>(smem + C::kOffY);    // row coordinate of page i % kYRing
   int* yring2 = reinterpret_cast<int*>(smem + C::kOffY2);  // its second 8-row block (block 8)
-  // misc[0]: the sequence holding r0 (scan result); [1]: the last-unit ticket result;
-  // [2]: number of runs
+  // misc[1]: the last-unit ticket result; [2]: number of runs
   int* misc = reinterpret_cast<int*>(smem + C::kOffMisc);
   long long* scratch = reinterpret_cast<long long*>(misc + 32);  // kScanSlots slots
-  Run* runs = reinterpret_cast<Run*>(smem + C::kOffRuns);         // the range's order
+  Run* runs = reinterpret_cast<Run*>(smem + C::kOffRuns);         // the range's order, w0
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, ncta = gridDim.x;
@@ -561,64 +598,78 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
   // tables, which no kernel of this library writes: the plan below may run while the
   // stream's previous kernel finishes (programmatic launch).
 
-  // ---- block-table entries the producers will read soon: CTA c asks L2 for those of
-  //      sequences c, c + ncta, ... while every CTA scans the context lengths
+  // ---- the barriers, one per thread
+  for (int i = tid; i < 2 * S + 4; i += kThreads) {
+    if (i < S) mbar_init(&full[i], 1);
+    else if (i < 2 * S) mbar_init(&empty[i - S], kRS ? kRT : 1);  // row-split: every warp
+                                                                     // with rows frees it
+    else if (i < 2 * S + 2) mbar_init(&unit_done[i - 2 * S], kRS ? kRT : kNW);
+    else mbar_init(&merge_free[i - 2 * S - 2], 1);
+    fence_mbar_init();
+  }
+
+  // ---- context lengths: sequence tid's (the first kThreads sequences in one load each,
+  //      kept in a register) and sequence c's, whose block-table entries this CTA asks
+  //      L2 for (the producers will read them soon), all loaded together
+  const int L_t = tid < B ? __ldg(p.context_lens + tid) : 0;
+  const int L_c = c < B ? __ldg(p.context_lens + c) : 0;
   for (int b = c; b < B; b += ncta) {
-    const int L = __ldg(p.context_lens + b);
+    const int L = b == c ? L_c : __ldg(p.context_lens + b);
     const int e0 = first_key(p, L) / p.block_size, e1 = (L + p.block_size - 1) / p.block_size;
     const int32_t* row = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq;
     for (int e = e0 + tid * 32; e < e1 && e < p.max_blocks_per_seq; e += kThreads * 32)
       prefetch_l2(row + e);
   }
 
-  // ---- the global page order holds N pages; this CTA owns [r0, r1)
-  long long local = 0;
-  for (int b = tid; b < B; b += kThreads) local += pages_of(p, b);
-  const long long N = static_cast<long long>(Hkv) * block_sum(local, scratch);
+  // ---- the global page order holds N pages; this CTA owns [r0, r1). One scan over the
+  //      sequences' pages gives N and each sequence's place in the order; the thread
+  //      whose sequence holds r0 publishes that unit (w0). Batches of more than kThreads
+  //      sequences take the scan chunk by chunk.
+  Walk* w0s = reinterpret_cast<Walk*>(runs + 3);
+  long long N, incl0, tot0;
+  const long long P_t = tid < B ? pages_of_len(p, L_t) : 0;
+  incl0 = block_scan(P_t, scratch, &tot0);
+  if (B <= kThreads) {
+    N = static_cast<long long>(Hkv) * tot0;
+  } else {
+    long long local = 0;
+    for (int b = tid + kThreads; b < B; b += kThreads) local += pages_of(p, b);
+    N = static_cast<long long>(Hkv) * (tot0 + block_sum(local, scratch));
+  }
   long long chunk = N > 0 ? (N + ncta - 1) / ncta : 0;
   if (chunk > 0 && chunk < kMinChunk) chunk = kMinChunk;
   const long long r0 = static_cast<long long>(c) * chunk;
   const long long r1 = r0 + chunk < N ? r0 + chunk : N;
-
-  // ---- find the unit holding r0 (a CTA-wide scan over the sequences)
-  if (tid == 0) misc[0] = -1;
-  long long running = 0;  // pages of the sequences before `base`
+  // (scan chunk k covers sequences k kThreads ..; the first is scanned already)
+  long long running = 0;  // pages of the sequences before the chunk
   for (int base = 0; r0 < r1 && base < B; base += kThreads) {
     const int b = base + tid;
-    const long long P = b < B ? pages_of(p, b) : 0;
-    long long tot;
-    const long long incl = block_scan(P, scratch, &tot);
+    long long P = P_t, incl = incl0, tot = tot0;
+    int L = L_t;
+    if (base > 0) {
+      L = b < B ? __ldg(p.context_lens + b) : 0;
+      P = b < B ? pages_of_len(p, L) : 0;
+      incl = block_scan(P, scratch, &tot);
+    }
     const long long s0 = static_cast<long long>(Hkv) * (running + incl - P);
     if (P > 0 && s0 <= r0 && r0 < s0 + Hkv * P) {
-      misc[0] = b;
-      scratch[kScanSlots - 1] = s0;
+      Walk w;
+      w.b = b;
+      w.P = static_cast<int>(P);
+      w.fp = first_key(p, L) >> 4;
+      w.L = L;
+      w.h = static_cast<int>((r0 - s0) / P);
+      w.S = s0 + static_cast<long long>(w.h) * P;
+      *w0s = w;
     }
     running += tot;
-    __syncthreads();
-    if (misc[0] >= 0) break;
+    if (running * Hkv > r0) break;  // (uniform: the unit holding r0 is in this chunk)
+    __syncthreads();                // (scratch is reused by the next chunk's scan)
   }
-  Walk w0{};
-  if (r0 < r1) {  // (the scan ran: misc[0] and the slot are set and published)
-    w0.b = misc[0];
-    w0.P = pages_of(p, w0.b);
-    w0.fp = first_page(p, w0.b);
-    w0.L = __ldg(p.context_lens + w0.b);
-    w0.h = static_cast<int>((r0 - scratch[kScanSlots - 1]) / w0.P);
-    w0.S = scratch[kScanSlots - 1] + static_cast<long long>(w0.h) * w0.P;
-  }
+  __syncthreads();
+  const Walk w0 = r0 < r1 ? *w0s : Walk{};
 
-  if (tid == 0) {
-    misc[2] = r0 < r1 ? plan_runs(p, w0, r0, r1, runs) : 0;
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kRS ? kRT : 1);  // row-split: every warp with rows frees it
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&unit_done[s], kRS ? kRT : kNW);
-      mbar_init(&merge_free[s], 1);
-    }
-    fence_mbar_init();
-  }
+  if (tid == 0) misc[2] = r0 < r1 ? plan_runs(p, w0, r0, r1, runs) : 0;
   __syncthreads();
 
   // ---- the producer's fetch cursor: row coordinates of this CTA's pages, read from
@@ -823,6 +874,11 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
     more = nxt.next(p, runs);
     const int L = __ldg(p.context_lens + w.b);
     const int kfirst = first_key(p, L);
+    // the range's last unit, when cut: the other CTAs' arrivals on its ticket, read now
+    // so that the load is out of the way by the unit's end
+    unsigned peek = 0;
+    if (!more && tid == 0 && unit_segments(w, chunk) > 1)
+      peek = ticket_peek(p.counters + w.b * Hkv + w.h);
 
     // Q^T fragments (B operand) of this unit; single-row-tile units start loading the
     // next unit's here (the multi-token form loads its larger fragments unit by unit)
@@ -1132,15 +1188,30 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
     // rows, in the row-split form) finish it
     const int nseg = unit_segments(w, chunk);
     const int nthr = (kRS ? kRT : kNW) * 32;
+    int* const ticket = p.counters + w.b * Hkv + w.h;
+    // When every other CTA of a cut unit has already arrived (as the run order makes
+    // likely: they took their parts first), this CTA is the last one: it merges their
+    // partials with its own state straight into the output and resets the ticket, with
+    // no partial of its own, no ticket update and no reading back (the same arithmetic
+    // as the ticket path below, so the same result bit for bit)
+    if (tid == 0)
+      misc[1] = nseg > 1 && (peek == static_cast<unsigned>(nseg - 1) ||
+                             ticket_peek(ticket) == static_cast<unsigned>(nseg - 1));
     bar_consumers(nthr);
-    combine_unit<D, kFp8, NT, kRS>(epi, w.b, w.h, nseg, w.S <= r0 ? 0 : 1, wob, wmlb, tid,
-                                   nthr);
-    if (nseg > 1) {
-      bar_consumers(nthr);  // this CTA's partial writes are issued
-      if (tid == 0) misc[1] = ticket_last(p.counters + w.b * Hkv + w.h, nseg);
-      bar_consumers(nthr);  // (and the reads below come after the acquire)
-      if (misc[1])
-        merge_partials<D, kFp8, NT, kRS>(epi, w.b, w.h, w.S, w.P, chunk, tid, nthr);
+    if (misc[1]) {
+      merge_partials<D, kFp8, NT, kRS>(epi, w.b, w.h, w.S, w.P, chunk, tid, nthr, 0, 1 << 30,
+                                       wob, wmlb);
+      if (tid == 0) *reinterpret_cast<volatile int*>(ticket) = 0;
+    } else {
+      combine_unit<D, kFp8, NT, kRS>(epi, w.b, w.h, nseg, w.S <= r0 ? 0 : 1, wob, wmlb, tid,
+                                     nthr);
+      if (nseg > 1) {
+        bar_consumers(nthr);  // this CTA's partial writes are issued
+        if (tid == 0) misc[1] = ticket_last(ticket, nseg);
+        bar_consumers(nthr);  // (and the reads below come after the acquire)
+        if (misc[1])
+          merge_partials<D, kFp8, NT, kRS>(epi, w.b, w.h, w.S, w.P, chunk, tid, nthr);
+      }
     }
     ++cu;
   }

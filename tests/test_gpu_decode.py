@@ -88,6 +88,18 @@ def test_ragged_contexts_e4m3(G):
     _step_and_check(inp, what=f"e4m3 G={G}")
 
 
+@pytest.mark.parametrize("B", [193, 500])
+@pytest.mark.parametrize("cache_dtype", ["bf16", "e4m3"])
+def test_more_sequences_than_one_plan_pass(B, cache_dtype):
+    """The kernel's range plan scans the context lengths 192 sequences at a time: with
+    more, the unit holding a range's first page is found in a later pass."""
+    g = np.random.default_rng(B)
+    lens = [int(x) for x in g.integers(1, 400, size=B)]
+    nb = sum(-(-L // 16) for L in lens) + 16
+    inp = workloads.make_decode(lens, 8, 2, 128, nb, seed=B, cache_dtype=cache_dtype)
+    _step_and_check(inp, what=f"B={B} {cache_dtype}")
+
+
 @pytest.mark.parametrize("max_ctx_factor", [1, 2, 8])
 def test_split_counts_agree(max_ctx_factor):
     """Inflating max_context_len changes the split plan, not the result."""
