@@ -48,9 +48,9 @@
  *    Copies, and kernels that do not release early (ordinary kernels), are fully
  *    ordered; no kernel of this library writes either array.
  *  - Supported now: head_dim 64 or 128, bf16 q/out; block_size 8, 16 or 32
- *    and 1 <= num_q_heads / num_kv_heads <= 8 for decode (an E4M3 cache at
- *    head_dim 128 only); block_size 16 and any group size for prefill (bf16 or
- *    E4M3 cache); any block_size for kv_cache_write.
+ *    and 1 <= num_q_heads / num_kv_heads <= 8 for decode (bf16 or E4M3 cache);
+ *    block_size 16 and any group size for prefill (bf16 or E4M3 cache); any
+ *    block_size for kv_cache_write.
  *
  * Errors
  *  - Argument errors found on the host return a negative pgqa_status_t and

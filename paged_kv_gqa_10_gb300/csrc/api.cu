@@ -184,8 +184,7 @@ pgqa_status_t decode_validate(const void* out, const void* q, const void* k_cach
   const int group = num_q_heads / num_kv_heads;
   if (group > 8 || (block_size != 8 && block_size != 16 && block_size != 32))
     return PGQA_EUNSUPPORTED;
-  if (!(head_dim == 128 || (head_dim == 64 && cache_dtype == PGQA_DTYPE_BF16)))
-    return PGQA_EUNSUPPORTED;
+  if (head_dim != 128 && head_dim != 64) return PGQA_EUNSUPPORTED;
   if (static_cast<int64_t>(num_blocks) * num_kv_heads * block_size > INT32_MAX)
     return PGQA_EUNSUPPORTED;
   if (num_seqs == 0) return PGQA_OK;

@@ -130,7 +130,10 @@ struct Cfg {
   static constexpr int kRows = kRS ? 8 * kNW : 8 * NT;
   static constexpr int kElem = kFp8 ? 1 : 2;
   static constexpr int kRowBytes = D * kElem;      // one token row of one head
-  static constexpr int kSub = kRowBytes / 128;     // 128-byte TMA boxes per row
+  // 64-byte rows (E4M3 at head_dim 64) are staged two tokens to a 128-byte swizzled
+  // row: token t of a page is in shared row t / 2, bytes 64 (t % 2) .. 64 (t % 2) + 63
+  static constexpr bool kPack = kRowBytes == 64;
+  static constexpr int kSub = kPack ? 1 : kRowBytes / 128;  // 128-byte TMA boxes per row
   static constexpr int kPageBytes = 16 * kRowBytes;
   static constexpr int kStageBytes = 2 * kPageBytes;  // K page + V page
   // about 16 KB of pages in flight per consumer warp (E4M3: 20 KB, with one merge
@@ -139,7 +142,7 @@ struct Cfg {
   static constexpr int kStagesPerWarp =
       kRS ? 0
           : NT > 1 ? (kStageBytes >= 8192 ? 5 : 8)
-                   : (kStageBytes >= 8192 ? 2 : kFp8 ? 5 : 16384 / kStageBytes);
+                   : (kStageBytes >= 8192 ? 2 : kFp8 ? 20480 / kStageBytes : 16384 / kStageBytes);
   // unit states in flight to the merge warp
   static constexpr int kMergeBufs = (kRS || kFp8 || NT > 1) ? 1 : 2;
   // the row-split form: one ring of 88 KB, filled in page order
@@ -163,7 +166,7 @@ struct Cfg {
   static constexpr int kOffMisc = kOffY2 + kYRing * 4;                // 32 ints, kScanSlots int64
   static constexpr int kOffRuns = kOffMisc + 32 * 4 + kScanSlots * 8;   // Run[3], Walk w0
   static constexpr int kSmem = 1024 + kOffRuns + 4 * 48;
-  static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle rows");
+  static_assert(kPack || kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle rows");
   static_assert(!kRS || 227 * 1024 / (kSmem + 1024) >= 2, "row-split: two CTAs per SM");
   static_assert(kStageBytes % 1024 == 0 && kOffMerge % 16 == 0 && kOffMl % 16 == 0 &&
                     kOffBar % 8 == 0 && kOffY % 16 == 0 && (kOffMisc + 32 * 4) % 8 == 0 &&
@@ -761,6 +764,10 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
           meta[s] = bad;
           uint8_t* st = ring + s * C::kStageBytes;
           mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+          if constexpr (C::kPack) {  // the tensor maps count 128-byte rows
+            y >>= 1;
+            y1 >>= 1;
+          }
           if (p.block_size != 8) {  // one 16-row box per 128-byte column block
 #pragma unroll
             for (int sub = 0; sub < C::kSub; ++sub)
@@ -769,14 +776,15 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
             for (int sub = 0; sub < C::kSub; ++sub)
               tma_load_2d(st + C::kPageBytes + sub * 2048, &vmap, &full[s],
                           sub * (128 / C::kElem), y);
-          } else {  // two 8-row boxes (rows 8-15 land 1 KB in: same swizzle phase)
+          } else {  // two 8-row boxes (rows 8-15 land half a page in: same swizzle phase)
+            constexpr int kHalf = C::kPack ? 512 : 1024;
 #pragma unroll
             for (int sub = 0; sub < C::kSub; ++sub) {
               tma_load_2d(st + sub * 2048, &kmap, &full[s], sub * (128 / C::kElem), y);
-              tma_load_2d(st + sub * 2048 + 1024, &kmap, &full[s], sub * (128 / C::kElem), y1);
+              tma_load_2d(st + sub * 2048 + kHalf, &kmap, &full[s], sub * (128 / C::kElem), y1);
               tma_load_2d(st + C::kPageBytes + sub * 2048, &vmap, &full[s],
                           sub * (128 / C::kElem), y);
-              tma_load_2d(st + C::kPageBytes + sub * 2048 + 1024, &vmap, &full[s],
+              tma_load_2d(st + C::kPageBytes + sub * 2048 + kHalf, &vmap, &full[s],
                           sub * (128 / C::kElem), y1);
             }
           }
@@ -969,7 +977,8 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
             v = make_uint4(a.x, a.y, b.x, b.y);
           }
           uint8_t* srow = ring + s * C::kStageBytes + (isv ? C::kPageBytes : 0) + (c >> 3) * 2048;
-          *reinterpret_cast<uint4*>(srow + swz128(rr, c & 7)) = v;
+          *reinterpret_cast<uint4*>(
+              srow + (C::kPack ? swz128(rr >> 1, (rr & 1) * 4 + c) : swz128(rr, c & 7))) = v;
           if (app_pbn >= 0 && app_pbn < p.num_blocks) {
             const size_t row = (static_cast<size_t>(app_pbn) * Hkv + w.h) * p.block_size +
                                (L - 1) % p.block_size;
@@ -1007,7 +1016,9 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
 #pragma unroll
         for (int kc = 0; kc < C::kNkc; kc += 2) {
           uint32_t r0v, r1v, r2v, r3v;
-          ldsm_x4(stK + swz128(rowK, kc + cK), r0v, r1v, r2v, r3v);
+          ldsm_x4(stK + (C::kPack ? swz128(rowK >> 1, (rowK & 1) * 4 + kc + cK)
+                                  : swz128(rowK, kc + cK)),
+                  r0v, r1v, r2v, r3v);
           const uint32_t a0 = e4m3x2_to_f16x2(r0v & 0xffff), a1 = e4m3x2_to_f16x2(r1v & 0xffff),
                          a2 = e4m3x2_to_f16x2(r0v >> 16), a3 = e4m3x2_to_f16x2(r1v >> 16);
           const uint32_t b0 = e4m3x2_to_f16x2(r2v & 0xffff), b1 = e4m3x2_to_f16x2(r3v & 0xffff),
@@ -1099,11 +1110,25 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
           for (int nt = 0; nt < NT; ++nt) mma_bf16(acc[dc][nt], v0, v1, v2, v3, pb0[nt], pb1[nt]);
         }
       } else {
-        // thread rows d in [16 gid, 16 gid + 16): row r of chunk dc <-> d = 16 (r & 7) + 2 dc + (r >> 3)
-        uint4 R0 = lds128(stV + swz128(2 * tig, gid));
-        uint4 R1 = lds128(stV + swz128(2 * tig + 1, gid));
-        uint4 R2 = lds128(stV + swz128(2 * tig + 8, gid));
-        uint4 R3 = lds128(stV + swz128(2 * tig + 9, gid));
+        // thread rows d in [(D/8) gid, (D/8) (gid + 1)): row r of chunk dc <-> d =
+        // (D/8) (r & 7) + 2 dc + (r >> 3); (D/8) bytes of each of the thread's 4 keys
+        uint4 R0, R1, R2, R3;
+        if constexpr (C::kPack) {  // 8 bytes: rows 2 tig .. (two tokens per shared row)
+          const uint32_t off = (gid & 1) * 8;
+          const uint2 a = lds64(stV + swz128(tig, gid >> 1) + off);
+          const uint2 b = lds64(stV + swz128(tig, 4 + (gid >> 1)) + off);
+          const uint2 c = lds64(stV + swz128(tig + 4, gid >> 1) + off);
+          const uint2 d = lds64(stV + swz128(tig + 4, 4 + (gid >> 1)) + off);
+          R0 = make_uint4(a.x, a.y, 0, 0);
+          R1 = make_uint4(b.x, b.y, 0, 0);
+          R2 = make_uint4(c.x, c.y, 0, 0);
+          R3 = make_uint4(d.x, d.y, 0, 0);
+        } else {
+          R0 = lds128(stV + swz128(2 * tig, gid));
+          R1 = lds128(stV + swz128(2 * tig + 1, gid));
+          R2 = lds128(stV + swz128(2 * tig + 8, gid));
+          R3 = lds128(stV + swz128(2 * tig + 9, gid));
+        }
         if (nv < 16) {
           if (2 * tig >= nv) R0 = make_uint4(0, 0, 0, 0);
           if (2 * tig + 1 >= nv) R1 = make_uint4(0, 0, 0, 0);
@@ -1159,7 +1184,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
           d0 = 16 * dc + gid;
           d1 = d0 + 8;
         } else {
-          d0 = 16 * gid + 2 * dc;
+          d0 = (D / 8) * gid + 2 * dc;
           d1 = d0 + 1;
         }
         float* o0 = wob + srow * C::kLd;
@@ -1224,11 +1249,13 @@ pgqa_status_t launch_variant(const DecodeArgs& a, const DecodePlan& plan) {
       kFp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.num_kv_heads * a.block_size;
   const uint32_t box_rows = a.block_size == 8 ? 8 : 16;
+  // 64-byte rows: the cache viewed as 128-byte rows of two tokens each
+  const int pk = C::kPack ? 2 : 1;
   CUtensorMap kmap, vmap;
-  if (!tensor_map_2d(&kmap, a.k_cache, dt, D, rows, C::kRowBytes, 128 / C::kElem, box_rows,
-                     CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tensor_map_2d(&vmap, a.v_cache, dt, D, rows, C::kRowBytes, 128 / C::kElem, box_rows,
-                     CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!tensor_map_2d(&kmap, a.k_cache, dt, D * pk, rows / pk, C::kRowBytes * pk, 128 / C::kElem,
+                     box_rows / pk, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tensor_map_2d(&vmap, a.v_cache, dt, D * pk, rows / pk, C::kRowBytes * pk, 128 / C::kElem,
+                     box_rows / pk, CU_TENSOR_MAP_SWIZZLE_128B))
     return PGQA_ECUDA;
   if (!smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<D, kFp8, NT, kRS>),
                        C::kSmem))
@@ -1293,12 +1320,13 @@ int decode_row_tiles(int q_len, int group) {
 }
 
 int decode_ctas_per_sm(int head_dim, int cache_dtype, int row_tiles) {
+  const bool e4m3 = cache_dtype == PGQA_DTYPE_E4M3, d64 = head_dim == 64;
   if (row_tiles == kNW) {  // row-split
-    if (cache_dtype == PGQA_DTYPE_E4M3) return ctas_per_sm<128, true, 1, true>();
-    return head_dim == 64 ? ctas_per_sm<64, false, 1, true>() : ctas_per_sm<128, false, 1, true>();
+    if (e4m3) return d64 ? ctas_per_sm<64, true, 1, true>() : ctas_per_sm<128, true, 1, true>();
+    return d64 ? ctas_per_sm<64, false, 1, true>() : ctas_per_sm<128, false, 1, true>();
   }
-  if (cache_dtype == PGQA_DTYPE_E4M3) return ctas_per_sm<128, true>();
-  return head_dim == 64 ? ctas_per_sm<64, false>() : ctas_per_sm<128, false>();
+  if (e4m3) return d64 ? ctas_per_sm<64, true>() : ctas_per_sm<128, true>();
+  return d64 ? ctas_per_sm<64, false>() : ctas_per_sm<128, false>();
 }
 
 DecodePlan decode_plan(int num_seqs, int num_kv_heads, int head_dim, int cache_dtype,
@@ -1323,7 +1351,9 @@ bool decode_prepare() {
          smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<64, false, 1, false>),
                          Cfg<64, false>::kSmem) &&
          smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<128, true, 1, false>),
-                         Cfg<128, true>::kSmem);
+                         Cfg<128, true>::kSmem) &&
+         smem_attr_ready(reinterpret_cast<const void*>(paged_decode_kernel<64, true, 1, false>),
+                         Cfg<64, true>::kSmem);
 }
 
 pgqa_status_t launch_paged_decode(const DecodeArgs& a, const DecodePlan& plan) {
@@ -1333,6 +1363,7 @@ pgqa_status_t launch_paged_decode(const DecodeArgs& a, const DecodePlan& plan) {
       if (a.head_dim == 64) return launch_variant<64, false, 1>(a, plan);
     } else if (a.cache_dtype == PGQA_DTYPE_E4M3) {
       if (a.head_dim == 128) return launch_variant<128, true, 1>(a, plan);
+      if (a.head_dim == 64) return launch_variant<64, true, 1>(a, plan);
     }
   } else if (plan.row_tiles == kNW) {
     if (a.cache_dtype == PGQA_DTYPE_BF16) {
@@ -1340,6 +1371,7 @@ pgqa_status_t launch_paged_decode(const DecodeArgs& a, const DecodePlan& plan) {
       if (a.head_dim == 64) return launch_variant<64, false, 1, true>(a, plan);
     } else if (a.cache_dtype == PGQA_DTYPE_E4M3) {
       if (a.head_dim == 128) return launch_variant<128, true, 1, true>(a, plan);
+      if (a.head_dim == 64) return launch_variant<64, true, 1, true>(a, plan);
     }
   }
   return PGQA_EUNSUPPORTED;

@@ -82,10 +82,11 @@ def test_ragged_contexts_and_groups(G, D):
 
 
 @pytest.mark.parametrize("G", [1, 4, 8])
-def test_ragged_contexts_e4m3(G):
+@pytest.mark.parametrize("D", [64, 128])
+def test_ragged_contexts_e4m3(G, D):
     lens = [1, 7, 16, 17, 40, 257, 999]
-    inp = workloads.make_decode(lens, G * 2, 2, 128, 256, seed=200 + G, cache_dtype="e4m3")
-    _step_and_check(inp, what=f"e4m3 G={G}")
+    inp = workloads.make_decode(lens, G * 2, 2, D, 256, seed=200 + G + D, cache_dtype="e4m3")
+    _step_and_check(inp, what=f"e4m3 G={G} D={D}")
 
 
 @pytest.mark.parametrize("B", [193, 500])

@@ -54,10 +54,11 @@ def test_block_sizes_ragged(bs, G, D):
 
 
 @pytest.mark.parametrize("bs", [8, 32])
-def test_block_sizes_e4m3(bs):
-    inp = workloads.make_decode(LENS, 8, 2, 128, 1024, seed=720 + bs, cache_dtype="e4m3",
+@pytest.mark.parametrize("D", [64, 128])
+def test_block_sizes_e4m3(bs, D):
+    inp = workloads.make_decode(LENS, 8, 2, D, 1024, seed=720 + bs + D, cache_dtype="e4m3",
                                 block_size=bs)
-    _step(inp, what=f"e4m3 bs={bs}")
+    _step(inp, what=f"e4m3 bs={bs} D={D}")
 
 
 @pytest.mark.parametrize("bs", [8, 32])

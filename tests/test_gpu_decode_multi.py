@@ -101,12 +101,13 @@ def test_multi_token_full_compare(q_len, G, D):
 
 @pytest.mark.parametrize("q_len", [2, 5, 6])
 @pytest.mark.parametrize("G", [1, 4, 8])
-def test_multi_token_e4m3(q_len, G):
+@pytest.mark.parametrize("D", [64, 128])
+def test_multi_token_e4m3(q_len, G, D):
     Hkv = 2
-    run = MultiRun(LENS, q_len, G * Hkv, Hkv, 128, seed=500 + 10 * q_len + G, e4m3=True)
+    run = MultiRun(LENS, q_len, G * Hkv, Hkv, D, seed=500 + 10 * q_len + G + D, e4m3=True)
     run.decode()
     assert run.status_code() == 0
-    run.compare(f"E4M3 q_len={q_len} G={G}")
+    run.compare(f"E4M3 q_len={q_len} G={G} D={D}")
 
 
 @pytest.mark.parametrize("bs", [8, 32])

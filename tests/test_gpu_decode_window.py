@@ -45,10 +45,11 @@ def test_ragged_contexts_windows(G, D, window):
 
 
 @pytest.mark.parametrize("window", [5, 100])
-def test_e4m3_windows(window):
+@pytest.mark.parametrize("D", [64, 128])
+def test_e4m3_windows(window, D):
     lens = [1, 7, 16, 17, 40, 257, 999]
-    inp = workloads.make_decode(lens, 8, 2, 128, 256, seed=600 + window, cache_dtype="e4m3")
-    _window_step(inp, window, f"e4m3 W={window}")
+    inp = workloads.make_decode(lens, 8, 2, D, 256, seed=600 + window + D, cache_dtype="e4m3")
+    _window_step(inp, window, f"e4m3 W={window} D={D}")
 
 
 def test_window_of_one_key_returns_its_value_exactly():

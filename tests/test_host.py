@@ -85,7 +85,7 @@ def _call_decode(**over):
     (dict(bs=32, NB=1 << 25), pgqa.EUNSUPPORTED),  # cache rows past int32
     (dict(dtype=7), pgqa.EUNSUPPORTED),
     (dict(dtype=1), pgqa.EINVAL),              # E4M3 without scales
-    (dict(dtype=1, D=64, ks=1 << 20, vs=1 << 20), pgqa.EUNSUPPORTED),  # E4M3 at head_dim 64
+    (dict(dtype=1, D=96, ks=1 << 20, vs=1 << 20), pgqa.EUNSUPPORTED),  # E4M3 at head_dim 96
     (dict(ks=1 << 20, vs=1 << 20), pgqa.EINVAL),  # scales given for bf16
     (dict(B=-1), pgqa.EINVAL),
     (dict(scale=float("nan")), pgqa.EINVAL),
