@@ -126,7 +126,9 @@ struct Cfg {
   // query rows of a unit, in NT 8-row n-tiles per warp: the group's G <= 8 heads, or
   // q_len tokens x G heads for multi-token decode (up to 8 rows with NT = 1; the
   // row-split form kRS: one 8-row tile per consumer warp, up to 32 rows, every warp
-  // reading every page of one shared ring)
+  // reading every page of one shared ring). The launches use NT = 1 only: giving a
+  // warp all the rows of a larger unit (NT = 3, one CTA per SM) ran slower than the
+  // row-split form; the template keeps NT general.
   static constexpr int kRows = kRS ? 8 * kNW : 8 * NT;
   static constexpr int kElem = kFp8 ? 1 : 2;
   static constexpr int kRowBytes = D * kElem;      // one token row of one head
@@ -137,8 +139,8 @@ struct Cfg {
   static constexpr int kPageBytes = 16 * kRowBytes;
   static constexpr int kStageBytes = 2 * kPageBytes;  // K page + V page
   // about 16 KB of pages in flight per consumer warp (E4M3: 20 KB, with one merge
-  // buffer instead of two paying for the fifth stage); multi-token decode runs one CTA
-  // per SM and gives each warp 32-40 KB
+  // buffer instead of two paying for the fifth stage); NT > 1 would run one CTA per SM
+  // and give each warp 32-40 KB
   static constexpr int kStagesPerWarp =
       kRS ? 0
           : NT > 1 ? (kStageBytes >= 8192 ? 5 : 8)
