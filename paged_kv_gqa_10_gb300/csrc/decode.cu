@@ -417,83 +417,121 @@ __device__ __noinline__ void combine_unit(const Epi e, int b, int h, int nseg, i
   }
 }
 
-// merge_partials: the last of the unit's CTAs to arrive merges their partials. The unit
+// merge_rows: the last of the unit's CTAs to arrive merges their partials. The unit
 // starts at page S; CTA c (range [c * chunk, ...)) keeps it in slot 0 when the unit
 // starts at or before its range (its first unit), else in slot 1 (its last). Partials
 // are taken four at a time: a group's loads are all issued before any is used, then
-// merged into a running (M, l, O). With wob/wmlb (the merge buffer of this CTA's
+// merged into a running (M, l, O); kItems work items (row, 8 values) go at once, their
+// loads in flight together (the arithmetic of an item does not depend on kItems, so
+// every caller gets the same bits). With wob/wmlb (the merge buffer of this CTA's
 // state) this CTA's partial is not read back but formed from its state, with the
 // arithmetic combine_unit uses to write it, so the result is the same bit for bit.
-template <int D, bool kFp8, int NT, bool kRS = false>
-__device__ __noinline__ void merge_partials(const Epi e, int b, int h, long long S, int P,
-                                            long long chunk, int t, int nt, int row0 = 0,
-                                            int row1 = 1 << 30, const float* wob = nullptr,
-                                            const float* wmlb = nullptr) {
+template <int D, bool kFp8, int NT, bool kRS, int kItems>
+__device__ __forceinline__ void merge_rows(const Epi& e, int b, int h, long long S, int P,
+                                           long long chunk, int t, int nt, int row0, int row1,
+                                           const float* wob, const float* wmlb) {
   constexpr int kRows = Cfg<D, kFp8, NT, kRS>::kRows;
   const int R = min(e.group * e.q_len, row1) - row0;  // rows row0 .. row1-1 of the unit
   constexpr int kChunks = D / 8;
   constexpr int kGroup = 4;
   const float vsc = kFp8 ? __ldg(e.v_scale + h) : 1.f;
   const long long c_first = S / chunk, c_last = (S + P - 1) / chunk;
-  for (int it = t; it < R * kChunks; it += nt) {
-    const int g = row0 + it / kChunks, cc = it % kChunks;  // g: the query row
-    float M = -INFINITY, lsum = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    bool any_bad = false;
-    for (long long base = c_first; base <= c_last; base += kGroup) {
-      float ls[kGroup];
-      float4 x[kGroup], y[kGroup];
+  for (int it0 = t; it0 < R * kChunks; it0 += kItems * nt) {
+    int g[kItems], cc[kItems];
+    bool live[kItems];
+    float M[kItems], lsum[kItems], o[kItems][8];
+    bool any_bad[kItems];
 #pragma unroll
-      for (int k = 0; k < kGroup; ++k) {
-        const long long cta = base + k;
-        ls[k] = -INFINITY;
-        x[k] = y[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (wob != nullptr && cta == blockIdx.x) {
-          float Mo, lo, oo[8];
-          bool po;
-          cta_state<D, kFp8, NT, kRS>(wob, wmlb, g, cc, Mo, lo, oo, po);
-          const float inv = lo > 0.f ? 1.f / lo : 0.f;
-          ls[k] = po ? INFINITY : Mo + log2f(lo);
-          x[k] = make_float4(oo[0] * inv, oo[1] * inv, oo[2] * inv, oo[3] * inv);
-          y[k] = make_float4(oo[4] * inv, oo[5] * inv, oo[6] * inv, oo[7] * inv);
-        } else if (cta <= c_last) {
-          const size_t ps =
-              static_cast<size_t>(cta * 2 + (S <= cta * chunk ? 0 : 1)) * kRows + g;
-          const float4* src = reinterpret_cast<const float4*>(e.part_o + ps * D + cc * 8);
-          ls[k] = __ldcg(e.part_lse + ps);
-          x[k] = __ldcg(src);
-          y[k] = __ldcg(src + 1);
+    for (int v = 0; v < kItems; ++v) {
+      const int it = it0 + v * nt;
+      live[v] = it < R * kChunks;
+      g[v] = row0 + (live[v] ? it : it0) / kChunks;
+      cc[v] = (live[v] ? it : it0) % kChunks;
+      M[v] = -INFINITY;
+      lsum[v] = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) o[v][q] = 0.f;
+      any_bad[v] = false;
+    }
+    for (long long base = c_first; base <= c_last; base += kGroup) {
+      float ls[kItems][kGroup];
+      float4 x[kItems][kGroup], y[kItems][kGroup];
+#pragma unroll
+      for (int v = 0; v < kItems; ++v) {
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) {
+          const long long cta = base + k;
+          ls[v][k] = -INFINITY;
+          x[v][k] = y[v][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (!live[v]) continue;
+          if (wob != nullptr && cta == blockIdx.x) {
+            float Mo, lo, oo[8];
+            bool po;
+            cta_state<D, kFp8, NT, kRS>(wob, wmlb, g[v], cc[v], Mo, lo, oo, po);
+            const float inv = lo > 0.f ? 1.f / lo : 0.f;
+            ls[v][k] = po ? INFINITY : Mo + log2f(lo);
+            x[v][k] = make_float4(oo[0] * inv, oo[1] * inv, oo[2] * inv, oo[3] * inv);
+            y[v][k] = make_float4(oo[4] * inv, oo[5] * inv, oo[6] * inv, oo[7] * inv);
+          } else if (cta <= c_last) {
+            const size_t ps =
+                static_cast<size_t>(cta * 2 + (S <= cta * chunk ? 0 : 1)) * kRows + g[v];
+            const float4* src = reinterpret_cast<const float4*>(e.part_o + ps * D + cc[v] * 8);
+            ls[v][k] = __ldcg(e.part_lse + ps);
+            x[v][k] = __ldcg(src);
+            y[v][k] = __ldcg(src + 1);
+          }
         }
       }
-      float Mn = M;
 #pragma unroll
-      for (int k = 0; k < kGroup; ++k) {
-        any_bad |= ls[k] == INFINITY;
-        Mn = fmaxf(Mn, ls[k]);
+      for (int v = 0; v < kItems; ++v) {
+        float Mn = M[v];
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) {
+          any_bad[v] |= ls[v][k] == INFINITY;
+          Mn = fmaxf(Mn, ls[v][k]);
+        }
+        if (Mn == INFINITY) continue;  // a poisoned partial: the result is discarded
+        const float a = M[v] == -INFINITY ? 0.f : ex2(M[v] - Mn);
+        lsum[v] *= a;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) o[v][q] *= a;
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) {
+          const float wt = ls[v][k] == -INFINITY ? 0.f : ex2(ls[v][k] - Mn);
+          lsum[v] += wt;
+          o[v][0] += x[v][k].x * wt; o[v][1] += x[v][k].y * wt;
+          o[v][2] += x[v][k].z * wt; o[v][3] += x[v][k].w * wt;
+          o[v][4] += y[v][k].x * wt; o[v][5] += y[v][k].y * wt;
+          o[v][6] += y[v][k].z * wt; o[v][7] += y[v][k].w * wt;
+        }
+        M[v] = Mn;
       }
-      if (Mn == INFINITY) continue;  // a poisoned partial: the result is discarded
-      const float a = M == -INFINITY ? 0.f : ex2(M - Mn);
-      lsum *= a;
+    }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) o[q] *= a;
-#pragma unroll
-      for (int k = 0; k < kGroup; ++k) {
-        const float wt = ls[k] == -INFINITY ? 0.f : ex2(ls[k] - Mn);
-        lsum += wt;
-        o[0] += x[k].x * wt; o[1] += x[k].y * wt; o[2] += x[k].z * wt; o[3] += x[k].w * wt;
-        o[4] += y[k].x * wt; o[5] += y[k].y * wt; o[6] += y[k].z * wt; o[7] += y[k].w * wt;
+    for (int v = 0; v < kItems; ++v) {
+      if (!live[v]) continue;
+      const size_t row = e.out_row(b, h, g[v]);
+      uint4 pk = make_uint4(0, 0, 0, 0);
+      if (!any_bad[v]) {
+        const float f = vsc / lsum[v];
+        pk = make_uint4(pack_bf16(o[v][0] * f, o[v][1] * f), pack_bf16(o[v][2] * f, o[v][3] * f),
+                        pack_bf16(o[v][4] * f, o[v][5] * f), pack_bf16(o[v][6] * f, o[v][7] * f));
       }
-      M = Mn;
+      reinterpret_cast<uint4*>(e.out + row * D)[cc[v]] = pk;
+      if (cc[v] == 0 && e.lse)
+        e.lse[row] = any_bad[v] ? -INFINITY : (M[v] + log2f(lsum[v])) * kLn2;
     }
-    const size_t row = e.out_row(b, h, g);
-    uint4 pk = make_uint4(0, 0, 0, 0);
-    if (!any_bad) {
-      const float f = vsc / lsum;
-      pk = make_uint4(pack_bf16(o[0] * f, o[1] * f), pack_bf16(o[2] * f, o[3] * f),
-                      pack_bf16(o[4] * f, o[5] * f), pack_bf16(o[6] * f, o[7] * f));
-    }
-    reinterpret_cast<uint4*>(e.out + row * D)[cc] = pk;
-    if (cc == 0 && e.lse) e.lse[row] = any_bad ? -INFINITY : (M + log2f(lsum)) * kLn2;
   }
+}
+
+// merge_rows one item at a time, as one non-inlined copy (for the consumer warps'
+// last unit, whose registers are in use around the call)
+template <int D, bool kFp8, int NT, bool kRS = false>
+__device__ __noinline__ void merge_partials(const Epi e, int b, int h, long long S, int P,
+                                            long long chunk, int t, int nt, int row0 = 0,
+                                            int row1 = 1 << 30, const float* wob = nullptr,
+                                            const float* wmlb = nullptr) {
+  merge_rows<D, kFp8, NT, kRS, 1>(e, b, h, S, P, chunk, t, nt, row0, row1, wob, wmlb);
 }
 
 // Arrival on a unit's ticket, wrapping to 0 on the last of `count` arrivals (so the
@@ -555,7 +593,10 @@ __device__ __forceinline__ void merge_units(const DecodeParams& p, const Epi epi
       if (lane == 0) last = ticket_last(p.counters + w.b * p.num_kv_heads + w.h, nseg);
       last = __shfl_sync(0xffffffffu, last, 0);
       __syncwarp();  // the lanes' reads of the partials come after lane 0's acquire
-      if (last) merge_partials<D, kFp8, NT, kRS>(epi, w.b, w.h, w.S, w.P, chunk, lane, 32);
+      // (inline, two items at a time: the merge warp has its registers to itself)
+      if (last)
+        merge_rows<D, kFp8, NT, kRS, 2>(epi, w.b, w.h, w.S, w.P, chunk, lane, 32, 0, 1 << 30,
+                                        nullptr, nullptr);
     }
   }
 }
