@@ -55,6 +55,51 @@ __global__ void __launch_bounds__(256) kv_cache_write_kernel(
   }
 }
 
+// The same scatter with the index arithmetic in 32 bits and shifts: kVecs 16-byte input
+// vectors per row (head_dim 128 or 64), fewer than 2^31 (token, head) rows, and a
+// block size that is a power of two (bs_shift = log2 of it). The general form above
+// spends most of its issue slots on 64-bit divisions; this one is a plain stream.
+template <bool kFp8, int kVecs>
+__global__ void __launch_bounds__(256) kv_cache_write_rows_kernel(
+    const uint4* __restrict__ key, const uint4* __restrict__ value,
+    const int64_t* __restrict__ slot_mapping, int num_tokens, int num_kv_heads,
+    void* __restrict__ k_cache, void* __restrict__ v_cache, int num_blocks, int bs_shift,
+    const float* __restrict__ k_scale, const float* __restrict__ v_scale, int* dev_status) {
+  static_assert(kVecs == 8 || kVecs == 16, "head_dim 64 or 128");
+  constexpr int kVecShift = kVecs == 16 ? 4 : 3;
+  grid_launch_dependents();
+  grid_dependency_wait();
+  const uint32_t hkv = static_cast<uint32_t>(num_kv_heads);
+  const int64_t total = (static_cast<int64_t>(num_tokens) * num_kv_heads) << kVecShift;
+  const int64_t bs_mask = (int64_t{1} << bs_shift) - 1;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint32_t row = static_cast<uint32_t>(i >> kVecShift);  // (token, head)
+    const uint32_t v = static_cast<uint32_t>(i) & (kVecs - 1);
+    const uint32_t t = row / hkv, h = row - t * hkv;
+    const int64_t slot = __ldg(slot_mapping + t);
+    if (slot < 0) continue;
+    const int64_t block = slot >> bs_shift;
+    if (block >= num_blocks) {
+      record_status(dev_status, PGQA_EBADINDEX);
+      continue;
+    }
+    // 16-byte vector of (block, h, row, 8v) in [NB][Hkv][bs][D]
+    const size_t dst = (((static_cast<size_t>(block) * hkv + h) << bs_shift) + (slot & bs_mask))
+                           * kVecs + v;
+    const uint4 kx = __ldg(key + i);
+    const uint4 vx = __ldg(value + i);
+    if constexpr (!kFp8) {
+      reinterpret_cast<uint4*>(k_cache)[dst] = kx;
+      reinterpret_cast<uint4*>(v_cache)[dst] = vx;
+    } else {
+      const float ks = __ldg(k_scale + h), vs = __ldg(v_scale + h);
+      reinterpret_cast<uint2*>(k_cache)[dst] = e4m3_quant8(kx, ks);
+      reinterpret_cast<uint2*>(v_cache)[dst] = e4m3_quant8(vx, vs);
+    }
+  }
+}
+
 // out[b][h][j][:] = cache[block_tables[b][j / bs]][h][j % bs][:] for j < L_b, else 0.
 // Each thread moves one 16-byte vector; `vecs` vectors per row.
 __global__ void __launch_bounds__(256) kv_gather_kernel(
@@ -111,6 +156,23 @@ pgqa_status_t launch_kv_cache_write(const void* key, const void* value,
   const int64_t work = static_cast<int64_t>(num_tokens) * num_kv_heads * (head_dim / 8);
   if (work == 0) return PGQA_OK;
   const int grid = grid_for(work, 256);
+  const bool pow2 = (block_size & (block_size - 1)) == 0;
+  const bool rows32 = static_cast<int64_t>(num_tokens) * num_kv_heads < (int64_t{1} << 31);
+  if (pow2 && rows32 && (head_dim == 128 || head_dim == 64)) {
+    int bs_shift = 0;
+    while ((1 << bs_shift) < block_size) ++bs_shift;
+    const bool fp8 = cache_dtype == PGQA_DTYPE_E4M3;
+    auto kern = head_dim == 128 ? (fp8 ? kv_cache_write_rows_kernel<true, 16>
+                                       : kv_cache_write_rows_kernel<false, 16>)
+                                : (fp8 ? kv_cache_write_rows_kernel<true, 8>
+                                       : kv_cache_write_rows_kernel<false, 8>);
+    const cudaError_t e = launch_after_previous(
+        kern, dim3(grid), dim3(256), 0, stream, static_cast<const uint4*>(key),
+        static_cast<const uint4*>(value), slot_mapping, num_tokens, num_kv_heads, k_cache,
+        v_cache, num_blocks, bs_shift, k_scale, v_scale, dev_status);
+    if (e != cudaSuccess) return PGQA_ECUDA;
+    return cudaPeekAtLastError() == cudaSuccess ? PGQA_OK : PGQA_ECUDA;
+  }
   // programmatic launch: the CTAs may be placed while the previous kernel finishes
   const cudaError_t e = launch_after_previous(
       cache_dtype == PGQA_DTYPE_BF16 ? kv_cache_write_kernel<false> : kv_cache_write_kernel<true>,
