@@ -51,6 +51,41 @@ def test_kv_cache_write_e4m3(D):
     assert np.array_equal(kc.cpu().numpy(), ok) and np.array_equal(vc.cpu().numpy(), ov)
 
 
+@pytest.mark.parametrize("D,bs,e4m3", [(128, 8, False), (64, 32, False), (128, 32, True),
+                                       (96, 16, False), (128, 12, False), (64, 12, True)])
+def test_kv_cache_write_block_sizes_and_head_dims(D, bs, e4m3):
+    """Power-of-two block sizes at head_dim 64/128 take the 32-bit index kernel, the
+    rest (block size 12, head_dim 96) the general one: both bit-exact."""
+    T, Hkv, NB = 1500, 4, 480
+    g = torch.Generator().manual_seed(D * 100 + bs)
+    key = (torch.randn((T, Hkv, D), generator=g) * 2).to(torch.bfloat16)
+    value = torch.randn((T, Hkv, D), generator=g).to(torch.bfloat16)
+    slots = torch.randperm(NB * bs, generator=g)[:T].to(torch.int64)
+    slots[::53] = -1
+    if e4m3:
+        ks = (torch.rand(Hkv, generator=g) * 0.05 + 0.001).to(torch.float32)
+        vs = (torch.rand(Hkv, generator=g) * 0.05 + 0.001).to(torch.float32)
+        kc0 = torch.randint(0, 256, (NB, Hkv, bs, D), generator=g, dtype=torch.uint8)
+        vc0 = torch.randint(0, 256, (NB, Hkv, bs, D), generator=g, dtype=torch.uint8)
+    else:
+        ks = vs = None
+        kc0 = torch.randn((NB, Hkv, bs, D), generator=g).to(torch.bfloat16)
+        vc0 = torch.randn((NB, Hkv, bs, D), generator=g).to(torch.bfloat16)
+    kc, vc = dev(kc0), dev(vc0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pgqa.kv_cache_write(dev(key), dev(value), dev(slots), kc, vc, k_scale=dev(ks),
+                        v_scale=dev(vs), dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ok, ov = oracle.kv_cache_write(key, value, slots, kc0, vc0,
+                                   dtype=oracle.E4M3 if e4m3 else oracle.BF16, k_scale=ks,
+                                   v_scale=vs)
+    if e4m3:
+        assert np.array_equal(kc.cpu().numpy(), ok) and np.array_equal(vc.cpu().numpy(), ov)
+    else:
+        assert np.array_equal(bits(kc), ok) and np.array_equal(bits(vc), ov)
+
+
 def test_kv_cache_write_bad_slot_reported():
     T, Hkv, D, NB = 64, 2, 128, 4
     key = torch.randn((T, Hkv, D)).to(torch.bfloat16)
