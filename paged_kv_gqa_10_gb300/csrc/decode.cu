@@ -876,6 +876,22 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
   const uint32_t cK = lane >> 4;
   const uint32_t rowV = (lane & 7) + ((lane >> 4) << 3);
   const uint32_t cV = (lane >> 3) & 1;
+  // this lane's swizzled fragment offsets within a 128-byte column block, computed once
+  // (per page each load is then one add): K for the four 16-element chunks q = kc & 3
+  // (E4M3: the pair kc = 2q); V for the four chunks (bf16) or the four key rows this
+  // lane reads (E4M3)
+  uint32_t offK[4], offV[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    offK[q] = C::kPack ? swz128(rowK >> 1, (rowK & 1) * 4 + 2 * q + cK) : swz128(rowK, 2 * q + cK);
+    if constexpr (!kFp8) {
+      offV[q] = swz128(rowV, 2 * q + cV);
+    } else if constexpr (C::kPack) {  // 8 bytes: rows 2 tig .. (two tokens per shared row)
+      offV[q] = swz128(tig + (q >> 1) * 4, (q & 1) * 4 + (gid >> 1)) + (gid & 1) * 8;
+    } else {
+      offV[q] = swz128(2 * tig + (q & 1) + (q >> 1) * 8, gid);
+    }
+  }
   const int R = G * p.q_len;  // query rows of a unit: row i = token i / G, head i % G
   const int rbase = kRS ? 8 * warp : 0;  // row-split: this warp's row tile
   if (kRS && warp >= kRT) return;        // (no rows: not counted by the stage barriers)
@@ -1050,7 +1066,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
 #pragma unroll
         for (int kc = 0; kc < C::kNkc; ++kc) {
           uint32_t a0, a1, a2, a3;
-          ldsm_x4(stK + (kc >> 2) * 2048 + swz128(rowK, (kc & 3) * 2 + cK), a0, a1, a2, a3);
+          ldsm_x4(stK + (kc >> 2) * 2048 + offK[kc & 3], a0, a1, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
             mma_bf16((kc & 1) ? sd[nt] : sc[nt], a0, a1, a2, a3, qf[kc][nt][0], qf[kc][nt][1]);
@@ -1059,9 +1075,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
 #pragma unroll
         for (int kc = 0; kc < C::kNkc; kc += 2) {
           uint32_t r0v, r1v, r2v, r3v;
-          ldsm_x4(stK + (C::kPack ? swz128(rowK >> 1, (rowK & 1) * 4 + kc + cK)
-                                  : swz128(rowK, kc + cK)),
-                  r0v, r1v, r2v, r3v);
+          ldsm_x4(stK + offK[kc >> 1], r0v, r1v, r2v, r3v);
           const uint32_t a0 = e4m3x2_to_f16x2(r0v & 0xffff), a1 = e4m3x2_to_f16x2(r1v & 0xffff),
                          a2 = e4m3x2_to_f16x2(r0v >> 16), a3 = e4m3x2_to_f16x2(r1v >> 16);
           const uint32_t b0 = e4m3x2_to_f16x2(r2v & 0xffff), b1 = e4m3x2_to_f16x2(r3v & 0xffff),
@@ -1142,7 +1156,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
 #pragma unroll
         for (int dc = 0; dc < C::kNkc; ++dc) {
           uint32_t v0, v1, v2, v3;
-          ldsm_x4_t(stV + (dc >> 2) * 2048 + swz128(rowV, (dc & 3) * 2 + cV), v0, v1, v2, v3);
+          ldsm_x4_t(stV + (dc >> 2) * 2048 + offV[dc & 3], v0, v1, v2, v3);
           if (nv < 16) {
             v0 &= m01;
             v1 &= m01;
@@ -1157,20 +1171,19 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
         // (D/8) (r & 7) + 2 dc + (r >> 3); (D/8) bytes of each of the thread's 4 keys
         uint4 R0, R1, R2, R3;
         if constexpr (C::kPack) {  // 8 bytes: rows 2 tig .. (two tokens per shared row)
-          const uint32_t off = (gid & 1) * 8;
-          const uint2 a = lds64(stV + swz128(tig, gid >> 1) + off);
-          const uint2 b = lds64(stV + swz128(tig, 4 + (gid >> 1)) + off);
-          const uint2 c = lds64(stV + swz128(tig + 4, gid >> 1) + off);
-          const uint2 d = lds64(stV + swz128(tig + 4, 4 + (gid >> 1)) + off);
+          const uint2 a = lds64(stV + offV[0]);
+          const uint2 b = lds64(stV + offV[1]);
+          const uint2 c = lds64(stV + offV[2]);
+          const uint2 d = lds64(stV + offV[3]);
           R0 = make_uint4(a.x, a.y, 0, 0);
           R1 = make_uint4(b.x, b.y, 0, 0);
           R2 = make_uint4(c.x, c.y, 0, 0);
           R3 = make_uint4(d.x, d.y, 0, 0);
         } else {
-          R0 = lds128(stV + swz128(2 * tig, gid));
-          R1 = lds128(stV + swz128(2 * tig + 1, gid));
-          R2 = lds128(stV + swz128(2 * tig + 8, gid));
-          R3 = lds128(stV + swz128(2 * tig + 9, gid));
+          R0 = lds128(stV + offV[0]);
+          R1 = lds128(stV + offV[1]);
+          R2 = lds128(stV + offV[2]);
+          R3 = lds128(stV + offV[3]);
         }
         if (nv < 16) {
           if (2 * tig >= nv) R0 = make_uint4(0, 0, 0, 0);
