@@ -1053,6 +1053,9 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
       const int pk0 = (w.fp + seg0 + j) * 16;       // key of the page's first row
       const int nv = min(16, L - pk0);               // rows below nv hold keys < L
       const int lo = max(0, kfirst - pk0);           // rows below lo are outside the window
+      // every column attends every key of the page (all pages but a unit's last ones
+      // and a window's first): no masks
+      const bool whole = lo == 0 && pk0 + 16 <= L - (p.q_len - 1);
 
       // ---- S^T = K Q^T per row tile, over two accumulators (even / odd 16-wide chunks
       //      of head_dim) so the MMA chain is half as long; each K fragment is loaded
@@ -1095,15 +1098,17 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
       for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) sc[nt][q] += sd[nt][q];
-        // rows below nv0 / nv1 hold keys the column attends (multi-token: token t of q_len
-        // sees keys up to L - q_len + t)
-        const int nv0 = min(16, L - dq[nt][0] - pk0), nv1 = min(16, L - dq[nt][1] - pk0);
         float s0 = sc[nt][0] * sl2, s1 = sc[nt][1] * sl2, s2 = sc[nt][2] * sl2,
               s3 = sc[nt][3] * sl2;
-        if (gid >= nv0 || gid < lo) s0 = -INFINITY;
-        if (gid >= nv1 || gid < lo) s1 = -INFINITY;
-        if (gid + 8 >= nv0 || gid + 8 < lo) s2 = -INFINITY;
-        if (gid + 8 >= nv1 || gid + 8 < lo) s3 = -INFINITY;
+        if (!whole) {
+          // rows below nv0 / nv1 hold keys the column attends (multi-token: token t of
+          // q_len sees keys up to L - q_len + t)
+          const int nv0 = min(16, L - dq[nt][0] - pk0), nv1 = min(16, L - dq[nt][1] - pk0);
+          if (gid >= nv0 || gid < lo) s0 = -INFINITY;
+          if (gid >= nv1 || gid < lo) s1 = -INFINITY;
+          if (gid + 8 >= nv0 || gid + 8 < lo) s2 = -INFINITY;
+          if (gid + 8 >= nv1 || gid + 8 < lo) s3 = -INFINITY;
+        }
         // m_run is the column's reference: every score seen so far is at most
         // m_run + kLazyLog2. Only a score above that (the first page with a key, or a
         // jump in the maximum) moves it, to the maximum so far, and rescales l and O;
@@ -1146,25 +1151,35 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
       }
 
       // ---- O^T += V^T P^T; rows past the context are zeroed (they may hold NaN)
-      const uint32_t m01 =
-          (2 * tig < nv ? 0x0000ffffu : 0u) | (2 * tig + 1 < nv ? 0xffff0000u : 0u);
-      const uint32_t m89 =
-          (2 * tig + 8 < nv ? 0x0000ffffu : 0u) | (2 * tig + 9 < nv ? 0xffff0000u : 0u);
       // (rows below lo hold real keys and get P = 0; only rows past the context,
       // which may hold NaN, need zeroing)
       if constexpr (!kFp8) {
+        if (nv < 16) {  // the context's last page
+          const uint32_t m01 =
+              (2 * tig < nv ? 0x0000ffffu : 0u) | (2 * tig + 1 < nv ? 0xffff0000u : 0u);
+          const uint32_t m89 =
+              (2 * tig + 8 < nv ? 0x0000ffffu : 0u) | (2 * tig + 9 < nv ? 0xffff0000u : 0u);
 #pragma unroll
-        for (int dc = 0; dc < C::kNkc; ++dc) {
-          uint32_t v0, v1, v2, v3;
-          ldsm_x4_t(stV + (dc >> 2) * 2048 + offV[dc & 3], v0, v1, v2, v3);
-          if (nv < 16) {
+          for (int dc = 0; dc < C::kNkc; ++dc) {
+            uint32_t v0, v1, v2, v3;
+            ldsm_x4_t(stV + (dc >> 2) * 2048 + offV[dc & 3], v0, v1, v2, v3);
             v0 &= m01;
             v1 &= m01;
             v2 &= m89;
             v3 &= m89;
-          }
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_bf16(acc[dc][nt], v0, v1, v2, v3, pb0[nt], pb1[nt]);
+            for (int nt = 0; nt < NT; ++nt)
+              mma_bf16(acc[dc][nt], v0, v1, v2, v3, pb0[nt], pb1[nt]);
+          }
+        } else {
+#pragma unroll
+          for (int dc = 0; dc < C::kNkc; ++dc) {
+            uint32_t v0, v1, v2, v3;
+            ldsm_x4_t(stV + (dc >> 2) * 2048 + offV[dc & 3], v0, v1, v2, v3);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma_bf16(acc[dc][nt], v0, v1, v2, v3, pb0[nt], pb1[nt]);
+          }
         }
       } else {
         // thread rows d in [(D/8) gid, (D/8) (gid + 1)): row r of chunk dc <-> d =
