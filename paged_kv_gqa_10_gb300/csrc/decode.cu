@@ -1015,6 +1015,111 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, kFp8, NT, kRS>()))
     // (row-split: every page, from the one ring in page order)
     for (int j = kRS ? 0 : (warp - i_base % kNW + kNW) % kNW; j < npg && alive;
          j += kRS ? 1 : kNW) {
+      if constexpr (kRS && !kFp8) {
+        // Row-split over a bf16 cache, two pages a step while two are left: both pages'
+        // S^T, one online-softmax step over their 32 keys, both P.V. A page's softmax is
+        // a dependency chain the next page cannot start before; taking two pages per
+        // chain halves the chains. (The row-split form never appends, and only a unit's
+        // last page can be partial, so page a here is whole.)
+        static_assert(!kRS || NT == 1, "one row tile per warp in the row-split form");
+        if (j + 1 < npg) {
+          const int ia = i_base + j, ib = ia + 1;
+          const int sa = ia % S, sb = ib % S;
+          if (!mbar_wait(&full[sa], (ia / S) & 1, p.wait_ns) ||
+              !mbar_wait(&full[sb], (ib / S) & 1, p.wait_ns)) {
+            alive = false;
+            record_status(p.dev_status, PGQA_ETIMEOUT);
+            break;
+          }
+          bad |= meta[sa] | meta[sb];
+          const uint32_t stKa = smem_u32(ring + sa * C::kStageBytes);
+          const uint32_t stKb = smem_u32(ring + sb * C::kStageBytes);
+          float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+          float tc[4] = {0.f, 0.f, 0.f, 0.f}, td[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kc = 0; kc < C::kNkc; ++kc) {
+            uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+            ldsm_x4(stKa + (kc >> 2) * 2048 + offK[kc & 3], a0, a1, a2, a3);
+            ldsm_x4(stKb + (kc >> 2) * 2048 + offK[kc & 3], b0, b1, b2, b3);
+            mma_bf16((kc & 1) ? sd : sc, a0, a1, a2, a3, qf[kc][0][0], qf[kc][0][1]);
+            mma_bf16((kc & 1) ? td : tc, b0, b1, b2, b3, qf[kc][0][0], qf[kc][0][1]);
+          }
+          const int pka = (w.fp + seg0 + j) * 16, pkb = pka + 16;
+          const int nvb = min(16, L - pkb);  // page b's rows holding keys < L
+          const int loa = max(0, kfirst - pka), lob = max(0, kfirst - pkb);
+          float s0 = (sc[0] + sd[0]) * sl2, s1 = (sc[1] + sd[1]) * sl2,
+                s2 = (sc[2] + sd[2]) * sl2, s3 = (sc[3] + sd[3]) * sl2;
+          float u0 = (tc[0] + td[0]) * sl2, u1 = (tc[1] + td[1]) * sl2,
+                u2 = (tc[2] + td[2]) * sl2, u3 = (tc[3] + td[3]) * sl2;
+          if (!(loa == 0 && pkb + 16 <= L - (p.q_len - 1))) {
+            const int a0 = min(16, L - dq[0][0] - pka), a1 = min(16, L - dq[0][1] - pka);
+            const int b0 = min(16, L - dq[0][0] - pkb), b1 = min(16, L - dq[0][1] - pkb);
+            if (gid >= a0 || gid < loa) s0 = -INFINITY;
+            if (gid >= a1 || gid < loa) s1 = -INFINITY;
+            if (gid + 8 >= a0 || gid + 8 < loa) s2 = -INFINITY;
+            if (gid + 8 >= a1 || gid + 8 < loa) s3 = -INFINITY;
+            if (gid >= b0 || gid < lob) u0 = -INFINITY;
+            if (gid >= b1 || gid < lob) u1 = -INFINITY;
+            if (gid + 8 >= b0 || gid + 8 < lob) u2 = -INFINITY;
+            if (gid + 8 >= b1 || gid + 8 < lob) u3 = -INFINITY;
+          }
+          const float x0 = fmaxf(fmaxf(s0, s2), fmaxf(u0, u2));
+          const float x1 = fmaxf(fmaxf(s1, s3), fmaxf(u1, u3));
+          if (__any_sync(0xffffffffu, x0 > m_run[0][0] + kLazyLog2 || x1 > m_run[0][1] + kLazyLog2)) {
+            float mx0 = x0, mx1 = x1;
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+              mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+              mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m_run[0][0], mx0), mn1 = fmaxf(m_run[0][1], mx1);
+            const float rf0 = mn0 == -INFINITY ? 0.f : mn0, rf1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float al0 = ex2(m_run[0][0] - rf0), al1 = ex2(m_run[0][1] - rf1);
+            m_run[0][0] = mn0;
+            m_run[0][1] = mn1;
+            l_run[0][0] *= al0;
+            l_run[0][1] *= al1;
+#pragma unroll
+            for (int dc = 0; dc < C::kNkc; ++dc) {
+              acc[dc][0][0] *= al0;
+              acc[dc][0][1] *= al1;
+              acc[dc][0][2] *= al0;
+              acc[dc][0][3] *= al1;
+            }
+          }
+          const float rf0 = m_run[0][0] == -INFINITY ? 0.f : m_run[0][0];
+          const float rf1 = m_run[0][1] == -INFINITY ? 0.f : m_run[0][1];
+          const float p0 = ex2(s0 - rf0), p1 = ex2(s1 - rf1), p2 = ex2(s2 - rf0), p3 = ex2(s3 - rf1);
+          const float q0 = ex2(u0 - rf0), q1 = ex2(u1 - rf1), q2 = ex2(u2 - rf0), q3 = ex2(u3 - rf1);
+          l_run[0][0] += (p0 + p2) + (q0 + q2);
+          l_run[0][1] += (p1 + p3) + (q1 + q3);
+          const uint32_t pa0 = movmatrix_t(pack_bf16(p0, p1)), pa1 = movmatrix_t(pack_bf16(p2, p3));
+          const uint32_t pb0 = movmatrix_t(pack_bf16(q0, q1)), pb1 = movmatrix_t(pack_bf16(q2, q3));
+          const uint32_t stVa = stKa + C::kPageBytes, stVb = stKb + C::kPageBytes;
+          // (page b's rows past the context may hold NaN: zeroed)
+          const uint32_t m01 = nvb >= 16 ? 0xffffffffu
+                                         : (2 * tig < nvb ? 0x0000ffffu : 0u) |
+                                               (2 * tig + 1 < nvb ? 0xffff0000u : 0u);
+          const uint32_t m89 = nvb >= 16 ? 0xffffffffu
+                                         : (2 * tig + 8 < nvb ? 0x0000ffffu : 0u) |
+                                               (2 * tig + 9 < nvb ? 0xffff0000u : 0u);
+#pragma unroll
+          for (int dc = 0; dc < C::kNkc; ++dc) {
+            uint32_t v0, v1, v2, v3, w0, w1, w2, w3;
+            ldsm_x4_t(stVa + (dc >> 2) * 2048 + offV[dc & 3], v0, v1, v2, v3);
+            ldsm_x4_t(stVb + (dc >> 2) * 2048 + offV[dc & 3], w0, w1, w2, w3);
+            mma_bf16(acc[dc][0], v0, v1, v2, v3, pa0, pa1);
+            mma_bf16(acc[dc][0], w0 & m01, w1 & m01, w2 & m89, w3 & m89, pb0, pb1);
+          }
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&empty[sa]);
+            mbar_arrive(&empty[sb]);
+          }
+          ++j;  // (and the loop's own step)
+          continue;
+        }
+      }
       const int i = i_base + j;
       const int li = i / kNW;
       const int s = kRS ? i % S : warp * SPW + li % SPW;
