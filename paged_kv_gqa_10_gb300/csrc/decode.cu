@@ -56,7 +56,12 @@
 //    32 run in the row-split form: consumer warp w holds rows 8w .. 8w+7 and reads every
 //    page, from one ring filled in page order whose stages every warp with rows frees;
 //    each warp hands its rows' state to the merge warp, which finishes the units as in
-//    the plain form.
+//    the plain form. Over a bf16 cache its warps take two pages a step (one softmax
+//    step over their 32 keys): a page's softmax is a dependency chain the next page
+//    cannot start before, and two pages per chain halve the chains.
+//  - Per page, each lane's swizzled fragment offsets are precomputed, pages that every
+//    column sees whole skip the mask arithmetic, and the V masking of a context's last
+//    page is one branch per page.
 //  - Every wait is bounded; a warp whose wait gives up records PGQA_ETIMEOUT, stops
 //    computing, but keeps taking part in every CTA barrier, so nothing can hang.
 #include <cuda_bf16.h>
